@@ -1,0 +1,261 @@
+"""Seeded synthetic inputs for the DSA sparse-attention path.
+
+This module only *generates* inputs: random draws, the paged-cache layout and the
+cache storage formats (FP8 e4m3 codes with per-row fp32 scales, bf16 bits).  It
+holds none of the method's arithmetic (no scoring, no selection, no attention):
+both the CPU oracle and the CUDA path consume the same bytes produced here.
+
+Storage formats (the "cache format" inputs the pages' quantised paths assume,
+"Day0 Inference Adaptation ... Kimi K3.1 Pro", section 4; the per-token fp32
+scale replaces the pages' MXFP8 group scales, see the workload list below):
+
+* indexer keys  ``k_i``  : ``uint8 [cache_rows, D_I]`` e4m3 codes, ``k_i_scale`` fp32 per row
+* indexer query ``q_i``  : ``uint8 [T, H_I, D_I]`` e4m3 codes, ``q_i_scale`` fp32 per (t, h)
+* head weights  ``w``    : fp32 ``[T, H_I]``
+* MLA query     ``q``    : bf16 bits ``uint16 [T, H, d_latent + d_rope]``
+* latent cache  ``kv``   : bf16 bits ``uint16 [cache_rows, d_latent + d_rope]``, or
+  the 656-byte FP8 row (``uint8 [cache_rows, 656]``): bytes [0, 512) e4m3 latent,
+  [512, 516) fp32 scale, [516, 528) zero, [528, 656) 64 bf16 rope values
+* the tiny check uses fp32 everywhere (``float32`` arrays, no scales)
+
+Quantisation rule used to *produce* e4m3 data: scale = amax / 448 over the row
+(1 for an all-zero row); code = round-to-nearest-even of x / scale, saturated to
++-448, done by ``torch``'s float8_e4m3fn cast.
+
+Draw order for seed ``s`` (one ``torch.Generator`` on the CPU):
+context lengths -> page permutation -> low-rank bases -> indexer keys ->
+indexer queries -> head weights -> latent rows -> MLA queries.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Optional
+
+import numpy as np
+import torch
+
+PAGE_SIZE = 64
+FP8_ROW_BYTES = 656          # 512 e4m3 + 4 scale + 12 reserved + 128 rope
+FP8_SCALE_OFFSET = 512
+FP8_ROPE_OFFSET = 528
+E4M3_MAX = 448.0
+
+
+@dataclasses.dataclass
+class Workload:
+    name: str
+    # sequences, queries and paging
+    B: int
+    T: int
+    K: int
+    page_size: int
+    max_ctx: int                 # upper bound of q_pos[t] + 1 over t
+    q_per_seq: int               # queries per sequence when uniform & consecutive, else 0
+    q_seq: np.ndarray            # int32 [T]
+    q_pos: np.ndarray            # int32 [T]
+    seq_lens: np.ndarray         # int32 [B]
+    block_table: np.ndarray      # int32 [B, max_pages]  (-1 = unused slot)
+    cache_rows: int
+    # lightning indexer
+    idx_dtype: str               # "e4m3" | "f32"
+    H_I: int
+    D_I: int
+    q_i: np.ndarray
+    q_i_scale: np.ndarray        # float32 [T, H_I]
+    w: np.ndarray                # float32 [T, H_I]
+    k_i: np.ndarray
+    k_i_scale: np.ndarray        # float32 [cache_rows]
+    # MLA latent attention
+    mla_dtype: str               # "bf16" | "e4m3" | "f32"
+    H: int
+    d_latent: int
+    d_rope: int
+    q: np.ndarray
+    kv: np.ndarray
+    row_bytes: int
+    softmax_scale: float
+
+    @property
+    def d_qk(self) -> int:
+        return self.d_latent + self.d_rope
+
+    @property
+    def d_v(self) -> int:
+        return self.d_latent
+
+
+@dataclasses.dataclass
+class Spec:
+    """Shape/distribution recipe of one workload."""
+    name: str
+    ctx: list                    # context length per sequence (or None -> drawn)
+    q_len: int                   # query tokens per sequence (the last q_len positions)
+    K: int
+    H_I: int = 64
+    D_I: int = 128
+    idx_dtype: str = "e4m3"
+    w_var: float = 1.0 / 64.0
+    H: int = 128
+    d_latent: int = 512
+    d_rope: int = 64
+    mla_dtype: str = "bf16"
+    softmax_scale: float = 1.0 / math.sqrt(192.0)
+    shuffle_pages: bool = False
+    ctx_range: Optional[tuple] = None   # (lo, hi) inclusive integer-uniform draw
+    B: int = 1
+    low_rank: int = 0            # rank of the structured component (0 = none)
+    low_rank_amp: float = 2.0
+
+
+def spec(name: str, **over) -> Spec:
+    """Named workload recipes (seeded, synthetic)."""
+    base = {
+        # 1 sequence of 256 tokens, 8 queries at 248..255, fp32 throughout
+        "tiny_fp32": dict(ctx=[256], q_len=8, K=32, H_I=4, D_I=32, idx_dtype="f32",
+                          w_var=0.25, H=4, d_latent=64, d_rope=16, mla_dtype="f32",
+                          softmax_scale=1.0 / math.sqrt(80.0)),
+        # one decode token against a 32768-token context, contiguous pages
+        "decode_b1": dict(ctx=[32768], q_len=1, K=2048),
+        # 64 sequences, ctx ~ U{2048..8192}, shuffled 64-token pages
+        "decode_b64": dict(ctx=None, ctx_range=(2048, 8192), B=64, q_len=1, K=2048,
+                           shuffle_pages=True),
+        # causal prefill of 16384 tokens with a rank-8 structured component
+        "prefill_16k": dict(ctx=[16384], q_len=16384, K=2048, low_rank=8),
+        # 4 x 131072 context, FP8 latent cache with per-token fp32 scale
+        "decode_b4_long": dict(ctx=[131072] * 4, B=4, q_len=1, K=2048, mla_dtype="e4m3"),
+    }[name]
+    base.update(over)
+    if base.get("ctx") is not None:
+        base["B"] = len(base["ctx"])
+    return Spec(name=name, **base)
+
+
+def _quant_rows_e4m3(x: torch.Tensor):
+    """Per-row e4m3 quantisation of the last axis: returns (uint8 codes, fp32 scales)."""
+    amax = x.abs().amax(dim=-1, keepdim=True)
+    scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
+    codes = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return codes.view(torch.uint8).numpy(), scale.squeeze(-1).to(torch.float32).numpy()
+
+
+def _bf16_bits(x: torch.Tensor) -> np.ndarray:
+    return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _randn(g: torch.Generator, shape, chunk_rows: int = 1 << 16) -> torch.Tensor:
+    out = torch.empty(shape, dtype=torch.float32)
+    flat = out.view(shape[0], -1)
+    for r0 in range(0, shape[0], chunk_rows):
+        r1 = min(shape[0], r0 + chunk_rows)
+        flat[r0:r1] = torch.randn((r1 - r0, flat.shape[1]), generator=g)
+    return out
+
+
+def _add_low_rank(g, x: torch.Tensor, basis: torch.Tensor, amp: float, chunk_rows: int = 1 << 15):
+    """x[..., :] += amp * z @ basis with z ~ N(0, 1)^rank drawn per row (in place)."""
+    flat = x.view(-1, x.shape[-1])
+    rank = basis.shape[0]
+    for r0 in range(0, flat.shape[0], chunk_rows):
+        r1 = min(flat.shape[0], r0 + chunk_rows)
+        z = torch.randn((r1 - r0, rank), generator=g)
+        flat[r0:r1] += amp * (z @ basis)
+
+
+def make(name_or_spec, seed: int = 0, **over) -> Workload:
+    sp = name_or_spec if isinstance(name_or_spec, Spec) else spec(name_or_spec, **over)
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    P = PAGE_SIZE
+
+    # --- context lengths and paging --------------------------------------
+    if sp.ctx is None:
+        lo, hi = sp.ctx_range
+        ctx = torch.randint(lo, hi + 1, (sp.B,), generator=g).tolist()
+    else:
+        ctx = list(sp.ctx)
+    B = len(ctx)
+    pages_per_seq = [(c + P - 1) // P for c in ctx]
+    n_pages = sum(pages_per_seq)
+    if sp.shuffle_pages:
+        perm = torch.randperm(n_pages, generator=g).numpy().astype(np.int32)
+    else:
+        perm = np.arange(n_pages, dtype=np.int32)
+    max_pages = max(pages_per_seq)
+    block_table = np.full((B, max_pages), -1, dtype=np.int32)
+    off = 0
+    for b, npg in enumerate(pages_per_seq):
+        block_table[b, :npg] = perm[off:off + npg]
+        off += npg
+    cache_rows = n_pages * P
+
+    q_len = sp.q_len
+    q_seq = np.repeat(np.arange(B, dtype=np.int32), q_len)
+    q_pos = np.concatenate([np.arange(c - q_len, c, dtype=np.int32) for c in ctx])
+    T = len(q_seq)
+
+    # --- low-rank bases ----------------------------------------------------
+    dk = sp.d_latent + sp.d_rope
+    if sp.low_rank:
+        u_idx = torch.randn((sp.low_rank, sp.D_I), generator=g) / math.sqrt(sp.low_rank)
+        u_mla = torch.randn((sp.low_rank, dk), generator=g) / math.sqrt(sp.low_rank)
+
+    # --- lightning indexer inputs -----------------------------------------
+    k_f = _randn(g, (cache_rows, sp.D_I))
+    if sp.low_rank:
+        _add_low_rank(g, k_f, u_idx, sp.low_rank_amp)
+    q_f = _randn(g, (T, sp.H_I, sp.D_I))
+    if sp.low_rank:
+        _add_low_rank(g, q_f, u_idx, sp.low_rank_amp)
+    w = (torch.randn((T, sp.H_I), generator=g) * math.sqrt(sp.w_var)).numpy()
+    if sp.idx_dtype == "e4m3":
+        k_i, k_i_scale = _quant_rows_e4m3(k_f)
+        q_i, q_i_scale = _quant_rows_e4m3(q_f)
+    elif sp.idx_dtype == "f32":
+        k_i, k_i_scale = k_f.numpy(), np.ones(cache_rows, np.float32)
+        q_i, q_i_scale = q_f.numpy(), np.ones((T, sp.H_I), np.float32)
+    else:
+        raise ValueError(sp.idx_dtype)
+    del k_f, q_f
+
+    # --- MLA latent cache and queries --------------------------------------
+    kv_f = _randn(g, (cache_rows, dk))
+    if sp.low_rank:
+        _add_low_rank(g, kv_f, u_mla, sp.low_rank_amp)
+    if sp.mla_dtype == "bf16":
+        kv = _bf16_bits(kv_f)
+        row_bytes = dk * 2
+    elif sp.mla_dtype == "e4m3":
+        assert sp.d_latent == 512 and sp.d_rope == 64
+        codes, scale = _quant_rows_e4m3(kv_f[:, :sp.d_latent])
+        kv = np.zeros((cache_rows, FP8_ROW_BYTES), dtype=np.uint8)
+        kv[:, :512] = codes
+        kv[:, FP8_SCALE_OFFSET:FP8_SCALE_OFFSET + 4] = scale.astype("<f4").view(np.uint8).reshape(-1, 4)
+        kv[:, FP8_ROPE_OFFSET:] = _bf16_bits(kv_f[:, sp.d_latent:]).view(np.uint8).reshape(cache_rows, -1)
+        row_bytes = FP8_ROW_BYTES
+    elif sp.mla_dtype == "f32":
+        kv = kv_f.numpy()
+        row_bytes = dk * 4
+    else:
+        raise ValueError(sp.mla_dtype)
+    del kv_f
+    q_m = _randn(g, (T, sp.H, dk))
+    if sp.low_rank:
+        _add_low_rank(g, q_m, u_mla, sp.low_rank_amp)
+    q = q_m.numpy() if sp.mla_dtype == "f32" else _bf16_bits(q_m)
+    del q_m
+
+    return Workload(
+        name=sp.name, B=B, T=T, K=sp.K, page_size=P, max_ctx=int(max(ctx)),
+        q_per_seq=q_len, q_seq=q_seq, q_pos=q_pos,
+        seq_lens=np.asarray(ctx, dtype=np.int32), block_table=block_table,
+        cache_rows=cache_rows,
+        idx_dtype=sp.idx_dtype, H_I=sp.H_I, D_I=sp.D_I, q_i=q_i,
+        q_i_scale=np.ascontiguousarray(q_i_scale, dtype=np.float32),
+        w=np.ascontiguousarray(w, dtype=np.float32), k_i=k_i,
+        k_i_scale=np.ascontiguousarray(k_i_scale, dtype=np.float32),
+        mla_dtype=sp.mla_dtype, H=sp.H, d_latent=sp.d_latent, d_rope=sp.d_rope,
+        q=q, kv=kv, row_bytes=row_bytes, softmax_scale=float(sp.softmax_scale),
+    )
+
+
+NAMES = ("tiny_fp32", "decode_b1", "decode_b64", "prefill_16k", "decode_b4_long")

@@ -1,0 +1,231 @@
+"""Plain CPU oracle for the DSA sparse-attention path.  TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  The product path (the CUDA library and its
+Python binding) never imports, calls or links anything here, and this module
+imports nothing from the product package: the two share only the seeded input
+generator (``dsa_workloads``), which holds none of the method's arithmetic.
+
+Everything is computed in float64 with numpy, one query at a time, in the order
+the method states it:
+
+1. lightning-indexer relevance scores with head-weight weighting
+   (page "Day0 Inference Adaptation ... Kimi K3.1 Pro", section 3: relevance
+   scores between queries and historical positions, head-weight weighting, then
+   Top-K; page "Large Language Model Inference Acceleration in Practice",
+   section 1.2 "DSA", LI sub-module).  Per the spec definition:
+       I[t, s] = sum_h w[t, h] * ReLU(q_I[t, h] . k_I[s])
+   with q_I, k_I the dequantised FP8 values (code * scale).
+2. per-query Top-K over the causal history s in [0, q_pos[t]], ties to the
+   lower index (same page, section 1.2, "selects the Top-K most relevant
+   positions").
+3. sparse MLA attention (MQA form over the latent cache): softmax over the
+   selected rows of scale * q . row[0:576], output sum p * row[0:512]
+   (same page, section 1.2, SFA sub-module; section 3.1 on reading the selected
+   rows from the paged KV cache).
+
+Readings taken where the pages are silent (each also listed in the design doc):
+* a query at position p sees s in [0, p] inclusive (its own key is cached);
+* scores are formed in float64 and then rounded to float32 once -- the Top-K
+  and every comparison downstream use those float32 values;
+* -0.0 and +0.0 compare equal (value comparison), ties go to the lower index;
+* the index list is a set: valid entries first (here in ascending index order),
+  then -1 padding up to K;
+* attention skips -1 entries; an empty selection gives out = 0, lse = -inf.
+
+Parity pins for every function live in ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# storage formats
+# ---------------------------------------------------------------------------
+
+
+def e4m3_table() -> np.ndarray:
+    """float64 value of every FP8 E4M3 code, from the OCP 8-bit floating point
+    definition: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits; exponent
+    field 0 encodes subnormals m/8 * 2**-6; S.1111.111 is NaN; there is no
+    infinity, so the largest finite magnitude is 1.75 * 2**8 = 448."""
+    out = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        exp_field = (code >> 3) & 0xF
+        man = code & 0x7
+        if exp_field == 0xF and man == 0x7:
+            out[code] = math.nan
+        elif exp_field == 0:
+            out[code] = sign * (man / 8.0) * 2.0 ** (1 - 7)
+        else:
+            out[code] = sign * (1.0 + man / 8.0) * 2.0 ** (exp_field - 7)
+    return out
+
+
+_E4M3 = e4m3_table()
+
+
+def decode_e4m3(codes: np.ndarray) -> np.ndarray:
+    return _E4M3[np.asarray(codes, dtype=np.uint8)]
+
+
+def decode_bf16(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 is the upper 16 bits of an IEEE binary32."""
+    wide = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
+    return wide.view(np.float32).astype(np.float64)
+
+
+def physical_rows(block_table_row: np.ndarray, page_size: int, pos: np.ndarray) -> np.ndarray:
+    """Logical position -> cache row through the page table:
+    row = block_table[s // page_size] * page_size + s % page_size."""
+    pos = np.asarray(pos, dtype=np.int64)
+    pages = np.asarray(block_table_row, dtype=np.int64)[pos // page_size]
+    if np.any(pages < 0):
+        raise ValueError("position maps to an unused page-table slot")
+    return pages * page_size + pos % page_size
+
+
+def indexer_keys(wl, rows: np.ndarray) -> np.ndarray:
+    """Dequantised indexer keys k_I[row] = code * k_scale[row] (float64)."""
+    if wl.idx_dtype == "e4m3":
+        return decode_e4m3(wl.k_i[rows]) * wl.k_i_scale[rows].astype(np.float64)[:, None]
+    return wl.k_i[rows].astype(np.float64)
+
+
+def indexer_query(wl, t: int) -> np.ndarray:
+    """Dequantised indexer query q_I[t, h] = code * q_scale[t, h] (float64 [H_I, D_I])."""
+    if wl.idx_dtype == "e4m3":
+        return decode_e4m3(wl.q_i[t]) * wl.q_i_scale[t].astype(np.float64)[:, None]
+    return wl.q_i[t].astype(np.float64)
+
+
+def latent_rows(wl, rows: np.ndarray) -> np.ndarray:
+    """Dequantised latent cache rows (float64 [n, d_latent + d_rope])."""
+    rows = np.asarray(rows, dtype=np.int64)
+    if wl.mla_dtype == "bf16":
+        return decode_bf16(wl.kv[rows])
+    if wl.mla_dtype == "f32":
+        return wl.kv[rows].astype(np.float64)
+    # 656-byte FP8 row: [0,512) e4m3 latent, [512,516) fp32 scale, [528,656) bf16 rope
+    raw = wl.kv[rows]
+    scale = raw[:, 512:516].copy().view("<f4").astype(np.float64)  # [n, 1]
+    latent = decode_e4m3(raw[:, :512]) * scale
+    rope = decode_bf16(raw[:, 528:656].copy().view("<u2"))
+    return np.concatenate([latent, rope], axis=1)
+
+
+def mla_query(wl, t: int) -> np.ndarray:
+    if wl.mla_dtype == "f32":
+        return wl.q[t].astype(np.float64)
+    return decode_bf16(wl.q[t])
+
+
+# ---------------------------------------------------------------------------
+# step 1: lightning indexer scores
+# ---------------------------------------------------------------------------
+
+
+def indexer_scores_row(wl, t: int) -> np.ndarray:
+    """Scores of query t over its causal history s in [0, q_pos[t]]:
+    I[t, s] = sum_h w[t, h] * max(q_I[t, h] . k_I[s], 0), in float64,
+    returned rounded once to float32 (length q_pos[t] + 1)."""
+    b = int(wl.q_seq[t])
+    n = int(wl.q_pos[t]) + 1
+    rows = physical_rows(wl.block_table[b], wl.page_size, np.arange(n))
+    k = indexer_keys(wl, rows)                 # [n, D_I]
+    q = indexer_query(wl, t)                   # [H_I, D_I]
+    dots = q @ k.T                             # [H_I, n]: q_I[t,h] . k_I[s]
+    relu = np.maximum(dots, 0.0)
+    weights = wl.w[t].astype(np.float64)       # [H_I]
+    scores = weights @ relu                    # sum over heads h
+    return scores.astype(np.float32)
+
+
+def indexer_scores(wl, ts=None) -> np.ndarray:
+    """float32 [len(ts), max_ctx]; -inf beyond each query's causal history."""
+    ts = range(wl.T) if ts is None else ts
+    ts = list(ts)
+    out = np.full((len(ts), wl.max_ctx), -np.inf, dtype=np.float32)
+    for i, t in enumerate(ts):
+        row = indexer_scores_row(wl, t)
+        out[i, :row.shape[0]] = row
+    return out
+
+
+# ---------------------------------------------------------------------------
+# step 2: per-query Top-K
+# ---------------------------------------------------------------------------
+
+
+def topk_row(scores: np.ndarray, n: int, K: int) -> np.ndarray:
+    """The K largest of scores[0:n] (float32 values compared as numbers), ties
+    to the lower index; all n kept when n <= K.  Returns int32 [K]: the chosen
+    positions in ascending order, then -1 padding."""
+    vals = np.asarray(scores[:n], dtype=np.float64)
+    order = np.lexsort((np.arange(n), -vals))  # primary: value desc, secondary: index asc
+    chosen = np.sort(order[:min(K, n)])
+    out = np.full(K, -1, dtype=np.int32)
+    out[:chosen.shape[0]] = chosen
+    return out
+
+
+def topk(scores: np.ndarray, q_pos: np.ndarray, K: int) -> np.ndarray:
+    T = scores.shape[0]
+    return np.stack([topk_row(scores[t], int(q_pos[t]) + 1, K) for t in range(T)]) if T else \
+        np.zeros((0, K), np.int32)
+
+
+# ---------------------------------------------------------------------------
+# step 3: sparse MLA attention over the selected latent rows
+# ---------------------------------------------------------------------------
+
+
+def sparse_mla_attn_row(wl, t: int, idx_row: np.ndarray):
+    """For every head h of query t, over the selected positions S (idx >= 0):
+    logit_s = scale * q[t, h] . row_s[0:d_qk]; p = softmax over S;
+    out[h] = sum_s p_s * row_s[0:d_v]; lse[h] = log sum_s exp(logit_s).
+    Returns float64 (out [H, d_v], lse [H])."""
+    sel = np.asarray(idx_row, dtype=np.int64)
+    sel = sel[sel >= 0]
+    H, dv = wl.H, wl.d_v
+    if sel.shape[0] == 0:
+        return np.zeros((H, dv)), np.full(H, -np.inf)
+    b = int(wl.q_seq[t])
+    rows = physical_rows(wl.block_table[b], wl.page_size, sel)
+    kv = latent_rows(wl, rows)                 # [m, d_qk]
+    q = mla_query(wl, t)                       # [H, d_qk]
+    logits = wl.softmax_scale * (q @ kv.T)     # [H, m]
+    mx = logits.max(axis=1, keepdims=True)
+    e = np.exp(logits - mx)
+    denom = e.sum(axis=1, keepdims=True)
+    p = e / denom
+    out = p @ kv[:, :dv]
+    lse = (mx + np.log(denom))[:, 0]
+    return out, lse
+
+
+def sparse_mla_attn(wl, idx: np.ndarray, ts=None):
+    ts = list(range(wl.T)) if ts is None else list(ts)
+    out = np.zeros((len(ts), wl.H, wl.d_v))
+    lse = np.zeros((len(ts), wl.H))
+    for i, t in enumerate(ts):
+        out[i], lse[i] = sparse_mla_attn_row(wl, t, idx[i])
+    return out, lse
+
+
+# ---------------------------------------------------------------------------
+# the whole step
+# ---------------------------------------------------------------------------
+
+
+def decode_step(wl, ts=None):
+    """scores -> Top-K -> sparse attention for the queries ts (default: all)."""
+    ts = list(range(wl.T)) if ts is None else list(ts)
+    scores = indexer_scores(wl, ts)
+    q_pos = np.asarray([wl.q_pos[t] for t in ts])
+    idx = topk(scores, q_pos, wl.K)
+    out, lse = sparse_mla_attn(wl, idx, ts)
+    return scores, idx, out, lse

@@ -1,0 +1,348 @@
+"""Pins for the CPU oracle (no GPU).
+
+Each test checks the oracle against something other than itself: torch's own
+float8/bfloat16 conversions, textbook values of the OCP E4M3 format, closed
+forms of special cases, element-by-element brute force in pure Python on tiny
+inputs, torch's scaled_dot_product_attention and scipy's logsumexp, and
+invariants (page-table layout, K >= context == dense causal attention).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dsa_workloads as W
+from oracle import dsa_oracle as O
+
+
+def small(name="decode_b1", seed=0, **over):
+    base = dict(ctx=[200], K=16, H_I=4, D_I=32, H=4, d_latent=64, d_rope=16)
+    if name == "decode_b4_long":
+        base.update(d_latent=512, d_rope=64)
+    base.update(over)
+    return W.make(name, seed=seed, **base)
+
+
+# --------------------------------------------------------------------------- formats
+
+def test_e4m3_all_codes_match_torch():
+    codes = torch.arange(256, dtype=torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = O.e4m3_table()
+    nan = np.isnan(ref)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF]
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_e4m3_textbook_values():
+    t = O.e4m3_table()
+    assert t[0x7E] == 448.0            # largest finite: 1.75 * 2^8
+    assert t[0x01] == 2.0 ** -9        # smallest subnormal
+    assert t[0x08] == 2.0 ** -6        # smallest normal
+    assert t[0x38] == 1.0 and t[0xB8] == -1.0
+    assert t[0x00] == 0.0 and math.copysign(1.0, t[0x80]) == -1.0
+
+
+def test_bf16_decode_matches_torch():
+    x = torch.randn(10000, generator=torch.Generator().manual_seed(3)) * 100
+    bits = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ref = x.to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(O.decode_bf16(bits), ref)
+
+
+def test_fp8_latent_row_decode():
+    """656-byte row: latent = code * scale, rope = bf16 at byte 528."""
+    wl = small("decode_b4_long", ctx=[64], B=1, K=8)
+    row = wl.kv[5]
+    scale = np.frombuffer(row[512:516].tobytes(), "<f4")[0]
+    lat = torch.from_numpy(row[:512].copy()).view(torch.float8_e4m3fn).double().numpy() * scale
+    rope = torch.from_numpy(row[528:656].copy()).view(torch.bfloat16).double().numpy()
+    got = O.latent_rows(wl, np.array([5]))[0]
+    assert np.array_equal(got[:512], lat) and np.array_equal(got[512:], rope)
+
+
+# --------------------------------------------------------------------------- indexer
+
+def brute_scores(wl, t):
+    """Element-by-element definition, pure Python, decoding with torch."""
+    def deq_q(h, i):
+        if wl.idx_dtype == "e4m3":
+            v = torch.tensor([wl.q_i[t, h, i]], dtype=torch.uint8).view(torch.float8_e4m3fn).item()
+            return v * float(wl.q_i_scale[t, h])
+        return float(wl.q_i[t, h, i])
+
+    def deq_k(row, i):
+        if wl.idx_dtype == "e4m3":
+            v = torch.tensor([wl.k_i[row, i]], dtype=torch.uint8).view(torch.float8_e4m3fn).item()
+            return v * float(wl.k_i_scale[row])
+        return float(wl.k_i[row, i])
+
+    b = wl.q_seq[t]
+    out = []
+    qd = [[deq_q(h, i) for i in range(wl.D_I)] for h in range(wl.H_I)]
+    for s in range(int(wl.q_pos[t]) + 1):
+        row = int(wl.block_table[b, s // wl.page_size]) * wl.page_size + s % wl.page_size
+        kd = [deq_k(row, i) for i in range(wl.D_I)]
+        acc = 0.0
+        for h in range(wl.H_I):
+            dot = 0.0
+            for i in range(wl.D_I):
+                dot += qd[h][i] * kd[i]
+            acc += float(wl.w[t, h]) * (dot if dot > 0 else 0.0)
+        out.append(acc)
+    return np.array(out)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "decode_b1", "decode_b64"])
+def test_indexer_brute_force(name):
+    over = dict(ctx=[70], K=8, H_I=3, D_I=8)
+    if name == "decode_b64":
+        over = dict(ctx=None, ctx_range=(65, 130), B=2, K=8, H_I=3, D_I=8)
+    wl = small(name, **over)
+    for t in range(wl.T):
+        ref = brute_scores(wl, t)
+        got = O.indexer_scores_row(wl, t)
+        assert got.dtype == np.float32 and got.shape == ref.shape
+        np.testing.assert_allclose(got, ref, rtol=1e-6, atol=1e-6 * np.abs(ref).max())
+
+
+def test_indexer_one_hot_closed_form():
+    """H_I = 1, w = 1, q = e_i: I[s] = max(k_I[s, i] * q_scale, 0)."""
+    wl = small(ctx=[130], H_I=1, D_I=32)
+    i = 7
+    wl.q_i[:] = 0
+    wl.q_i[0, 0, i] = 0x38            # e4m3 code of 1.0
+    wl.q_i_scale[0, 0] = 0.5
+    wl.w[0, 0] = 1.0
+    got = O.indexer_scores_row(wl, 0)
+    kcode = torch.from_numpy(wl.k_i[:, i].copy()).view(torch.float8_e4m3fn).double().numpy()
+    expect = np.maximum(kcode * wl.k_i_scale * 0.5, 0.0)[:130]
+    np.testing.assert_allclose(got, expect.astype(np.float32), rtol=0, atol=0)
+
+
+def test_indexer_zero_weight_negative_dots_and_sign():
+    wl = small(ctx=[100])
+    t = 0
+    base = O.indexer_scores_row(wl, t).astype(np.float64)
+    wl2 = small(ctx=[100]); wl2.w[:] = 0
+    assert np.all(O.indexer_scores_row(wl2, t) == 0)
+    # flipping every key's sign... make all dots negative: q and k of opposite sign
+    wl3 = small(ctx=[100]); wl3.idx_dtype = "f32"
+    wl3.q_i = np.abs(np.random.default_rng(0).standard_normal((1, wl3.H_I, wl3.D_I))).astype(np.float32)
+    wl3.k_i = -np.abs(np.random.default_rng(1).standard_normal((wl3.cache_rows, wl3.D_I))).astype(np.float32)
+    wl3.q_i_scale[:] = 1; wl3.k_i_scale[:] = 1
+    assert np.all(O.indexer_scores_row(wl3, t) == 0)
+    # negating all head weights negates the score (linearity in w)
+    wl4 = small(ctx=[100]); wl4.w *= -1
+    np.testing.assert_array_equal(O.indexer_scores_row(wl4, t), -base.astype(np.float32))
+    # scaling w by 3 scales the score by 3 (within one fp32 rounding)
+    wl5 = small(ctx=[100]); wl5.w *= 3
+    np.testing.assert_allclose(O.indexer_scores_row(wl5, t), 3 * base, rtol=1e-6, atol=1e-6)
+
+
+def test_indexer_page_table_invariance():
+    """Shuffled physical pages give the same logical scores as contiguous ones."""
+    a = small("decode_b64", ctx=None, ctx_range=(150, 400), B=3, K=16)
+    b = small("decode_b64", ctx=None, ctx_range=(150, 400), B=3, K=16)
+    # rebuild b with an identity page table: move every page to its logical slot
+    P = a.page_size
+    order = []
+    for bb in range(a.B):
+        npg = (a.seq_lens[bb] + P - 1) // P
+        order += list(a.block_table[bb, :npg])
+    rows = np.concatenate([np.arange(p * P, p * P + P) for p in order])
+    b.k_i = a.k_i[rows]; b.k_i_scale = a.k_i_scale[rows]; b.kv = a.kv[rows]
+    off = 0
+    for bb in range(a.B):
+        npg = (a.seq_lens[bb] + P - 1) // P
+        b.block_table[bb, :npg] = np.arange(off, off + npg)
+        off += npg
+    assert not np.array_equal(a.block_table, b.block_table)
+    np.testing.assert_array_equal(O.indexer_scores(a), O.indexer_scores(b))
+    idx = O.topk(O.indexer_scores(a), a.q_pos, a.K)
+    oa, la = O.sparse_mla_attn(a, idx)
+    ob, lb = O.sparse_mla_attn(b, idx)
+    np.testing.assert_array_equal(oa, ob); np.testing.assert_array_equal(la, lb)
+
+
+def test_indexer_causal_extent():
+    wl = small("tiny_fp32")
+    s = O.indexer_scores(wl)
+    for t in range(wl.T):
+        n = wl.q_pos[t] + 1
+        assert np.all(np.isfinite(s[t, :n])) and np.all(np.isneginf(s[t, n:]))
+    # the query's own position is part of its history
+    assert wl.q_pos[-1] + 1 == wl.max_ctx
+
+
+# --------------------------------------------------------------------------- top-k
+
+def brute_topk(vals, n, K):
+    """Repeatedly take the largest remaining value, lowest index first."""
+    remaining = list(range(n))
+    chosen = []
+    for _ in range(min(K, n)):
+        best = remaining[0]
+        for j in remaining[1:]:
+            if vals[j] > vals[best]:
+                best = j
+        chosen.append(best)
+        remaining.remove(best)
+    return sorted(chosen)
+
+
+def as_set(row):
+    return sorted(int(x) for x in row if x >= 0)
+
+
+@pytest.mark.parametrize("seed", range(5))
+def test_topk_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    n = int(rng.integers(1, 120))
+    K = int(rng.integers(1, 40))
+    vals = rng.integers(-5, 6, size=n).astype(np.float32)   # many ties
+    got = O.topk_row(vals, n, K)
+    assert as_set(got) == brute_topk(vals, n, K)
+    assert np.all(got[min(K, n):] == -1)
+
+
+def test_topk_special_cases():
+    n, K = 50, 10
+    assert as_set(O.topk_row(np.zeros(n, np.float32), n, K)) == list(range(K))
+    inc = np.arange(n, dtype=np.float32)
+    assert as_set(O.topk_row(inc, n, K)) == list(range(n - K, n))
+    assert as_set(O.topk_row(inc[::-1].copy(), n, K)) == list(range(K))
+    assert as_set(O.topk_row(inc, n, 80)) == list(range(n))
+    # ties straddling the K-th value go to the lower indices
+    v = np.array([5, 3, 3, 3, 1], np.float32)
+    assert as_set(O.topk_row(v, 5, 2)) == [0, 1]
+    assert as_set(O.topk_row(v, 5, 3)) == [0, 1, 2]
+    # -0.0 and +0.0 are equal values
+    z = np.array([1.0, -0.0, 0.0, -1.0], np.float32)
+    assert as_set(O.topk_row(z, 4, 2)) == [0, 1]
+    # only the causal prefix counts
+    big = np.array([0, 0, 0, 9, 9], np.float32)
+    assert as_set(O.topk_row(big, 3, 2)) == [0, 1]
+
+
+# --------------------------------------------------------------------------- attention
+
+def sdpa_dense(wl, t):
+    """Dense causal attention of query t with torch's SDPA (float64), MQA form."""
+    b = wl.q_seq[t]
+    n = int(wl.q_pos[t]) + 1
+    rows = np.array([int(wl.block_table[b, s // wl.page_size]) * wl.page_size + s % wl.page_size
+                     for s in range(n)])
+    if wl.mla_dtype == "bf16":
+        kv = torch.from_numpy(wl.kv[rows].view(np.int16)).view(torch.bfloat16).double()
+        q = torch.from_numpy(wl.q[t].view(np.int16)).view(torch.bfloat16).double()
+    elif wl.mla_dtype == "f32":
+        kv = torch.from_numpy(wl.kv[rows]).double(); q = torch.from_numpy(wl.q[t]).double()
+    else:
+        raw = wl.kv[rows]
+        sc = torch.from_numpy(raw[:, 512:516].copy().view("<f4")).double()
+        lat = torch.from_numpy(raw[:, :512].copy()).view(torch.float8_e4m3fn).double() * sc
+        rope = torch.from_numpy(raw[:, 528:].copy()).view(torch.bfloat16).double()
+        kv = torch.cat([lat, rope], 1)
+        q = torch.from_numpy(wl.q[t].view(np.int16)).view(torch.bfloat16).double()
+    H = wl.H
+    qq = q.view(1, H, 1, -1)
+    kk = kv.view(1, 1, n, -1).expand(1, H, n, -1)
+    vv = kv[:, :wl.d_v].reshape(1, 1, n, -1).expand(1, H, n, -1)
+    out = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, scale=wl.softmax_scale)
+    logits = (q @ kv.T) * wl.softmax_scale
+    return out.view(H, -1).numpy(), torch.logsumexp(logits, dim=1).numpy()
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "decode_b1", "decode_b4_long"])
+def test_attention_k_ge_ctx_equals_dense(name):
+    """Top-K with K >= context selects everything: sparse == dense causal attention."""
+    over = dict(ctx=[90], K=128)
+    if name == "tiny_fp32":
+        over = {}
+        wl = W.make(name, K=256)
+    else:
+        wl = small(name, **over)
+    _, idx, out, lse = O.decode_step(wl)
+    for t in range(wl.T):
+        assert as_set(idx[t]) == list(range(wl.q_pos[t] + 1))
+        ro, rl = sdpa_dense(wl, t)
+        np.testing.assert_allclose(out[t], ro, rtol=1e-10, atol=1e-12)
+        np.testing.assert_allclose(lse[t], rl, rtol=1e-12, atol=1e-12)
+
+
+def test_attention_closed_forms():
+    from scipy.special import logsumexp
+    wl = small(ctx=[128], K=32)
+    rows_all = O.latent_rows(wl, np.arange(128))
+    q = O.mla_query(wl, 0)
+    # one selected row: out = its value part, lse = its logit
+    idx = np.full(32, -1, np.int32); idx[0] = 17
+    out, lse = O.sparse_mla_attn_row(wl, 0, idx)
+    np.testing.assert_array_equal(out, np.broadcast_to(rows_all[17, :wl.d_v], out.shape))
+    np.testing.assert_allclose(lse, wl.softmax_scale * q @ rows_all[17], rtol=1e-12)
+    # q = 0: uniform weights -> mean of the selected value rows, lse = log m
+    sel = np.array([3, 9, 10, 64, 100], np.int32)
+    idx = np.full(32, -1, np.int32); idx[:5] = sel
+    wl0 = small(ctx=[128], K=32); wl0.q[:] = 0
+    out, lse = O.sparse_mla_attn_row(wl0, 0, idx)
+    np.testing.assert_allclose(out, np.broadcast_to(rows_all[sel, :wl.d_v].mean(0), out.shape), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(lse, math.log(5))
+    # lse against scipy's logsumexp; -1 entries anywhere are skipped
+    idx = np.array([5, -1, 40, 7, -1, 90] + [-1] * 26, np.int32)
+    out, lse = O.sparse_mla_attn_row(wl, 0, idx)
+    logits = wl.softmax_scale * q @ rows_all[[5, 40, 7, 90]].T
+    np.testing.assert_allclose(lse, logsumexp(logits, axis=1), rtol=1e-12)
+    out2, _ = O.sparse_mla_attn_row(wl, 0, np.array([5, 40, 7, 90], np.int32))
+    np.testing.assert_allclose(out, out2, rtol=1e-13, atol=1e-15)
+    # softmax weights sum to 1: out of all-equal value rows equals that row
+    wl1 = small(ctx=[128], K=32); wl1.idx_dtype = wl.idx_dtype
+    wl1.kv[:, :wl.d_v] = wl1.kv[0, :wl.d_v]
+    out, _ = O.sparse_mla_attn_row(wl1, 0, np.arange(32, dtype=np.int32))
+    np.testing.assert_allclose(out, np.broadcast_to(O.latent_rows(wl1, [0])[0, :wl.d_v], out.shape), rtol=1e-12)
+    # empty selection
+    out, lse = O.sparse_mla_attn_row(wl, 0, np.full(32, -1, np.int32))
+    assert np.all(out == 0) and np.all(np.isneginf(lse))
+
+
+def test_decode_step_composition_and_order():
+    wl = small("decode_b64", ctx=None, ctx_range=(100, 300), B=3, K=40)
+    scores, idx, out, lse = O.decode_step(wl)
+    for t in range(wl.T):
+        n = wl.q_pos[t] + 1
+        s = idx[t][idx[t] >= 0]
+        assert len(s) == min(40, n) and np.all(np.diff(s) > 0)
+        kth = np.sort(scores[t, :n])[::-1][min(40, n) - 1]
+        assert np.all(scores[t, s] >= kth)
+    # the subset of queries path equals the full path
+    s2, i2, o2, l2 = O.decode_step(wl, ts=[2, 0])
+    np.testing.assert_array_equal(i2, idx[[2, 0]])
+    np.testing.assert_array_equal(o2, out[[2, 0]])
+
+
+def test_workload_recipes_small():
+    """Shapes and storage of each named recipe (scaled down)."""
+    wl = W.make("tiny_fp32")
+    assert (wl.T, wl.K, wl.H_I, wl.D_I, wl.H, wl.d_qk, wl.d_v) == (8, 32, 4, 32, 4, 80, 64)
+    assert list(wl.q_pos) == list(range(248, 256))
+    wl = small("decode_b64", ctx=None, ctx_range=(2048, 2100), B=5, K=16)
+    assert np.all((wl.seq_lens >= 2048) & (wl.seq_lens <= 2100))
+    used = np.sort(wl.block_table[wl.block_table >= 0])
+    assert np.array_equal(used, np.arange(wl.cache_rows // 64))
+    wl = small("decode_b4_long", ctx=[100, 64], B=2, K=8)
+    assert wl.kv.shape == (wl.cache_rows, 656) and wl.row_bytes == 656
+    assert np.all(wl.kv[:, 516:528] == 0)
+
+
+def test_hand_worked_golden_example():
+    from tests.fixtures import hand_example
+    wl, exp = hand_example()
+    scores, idx, out, lse = O.decode_step(wl)
+    np.testing.assert_array_equal(scores[0], np.array(exp["scores"], np.float32))
+    assert as_set(idx[0]) == exp["topk_set"]
+    # ln 3 is stored as an fp32 cache value (relative rounding <= 2^-24), so the
+    # closed form holds to ~1e-7 relative
+    np.testing.assert_allclose(out[0, 0], exp["out"], rtol=1e-7)
+    np.testing.assert_allclose(lse[0, 0], exp["lse"], rtol=1e-7)
