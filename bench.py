@@ -1,0 +1,426 @@
+"""Benchmark of the DSA decode/prefill step on one GB300.
+
+  python bench.py [--steps K] [--warmup W] [--workload decode_b1|decode_b64|decode_b4_long|prefill_16k]
+  python bench.py --impl reference      # the CPU oracle as the reference arm
+
+One step = one pass of the whole path (indexer scores -> Top-K -> sparse MLA
+attention) over one batch of seeded synthetic input through the C ABI
+(dsa_decode_step).  Inputs are resident in HBM; R independent copies are rotated
+so that the bytes touched between two uses of a copy exceed twice the L2 cache.
+The timed steps are replayed from a CUDA graph of R captured steps and timed with
+CUDA events on the launching stream.  Prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "DSA layer decode tok/s & prefill tok/s on 1 GB300; % of HBM / tensor roofline"
+L2_BYTES = 129 * 1024 * 1024
+DESCRIPTIONS = {
+    "decode_b1": "decode batch 1: 1 query, ctx 32768, indexer 64x128 e4m3 + per-token fp32 scale, "
+                 "top-k 2048, MLA 128 heads, bf16 latent 512+64, contiguous 64-token pages",
+    "decode_b64": "decode batch 64: 1 query/seq, ctx ~ U{2048..8192}, shuffled 64-token pages, "
+                  "indexer 64x128 e4m3, top-k 2048, MLA 128 heads, bf16 512+64",
+    "decode_b4_long": "decode batch 4: ctx 131072 each, FP8 e4m3 latent (656-byte rows, per-token scale, "
+                      "bf16 rope), indexer 64x128 e4m3, top-k 2048, MLA 128 heads",
+    "prefill_16k": "prefill: 16384 causal tokens, indexer 64x128 e4m3, top-k 2048, MLA 128 heads, "
+                   "bf16 512+64, inputs N(0,1) + rank-8 component",
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": p["hbm_gbs"], "bf16_tflops": p["bf16_tflops"],
+                "bf16_tflops_sustained": p.get("bf16_tflops_sustained", p["bf16_tflops"]), "src": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "src": "fallback"}
+
+
+# ----------------------------------------------------------------------------- bytes / flops
+
+def algorithmic(wl):
+    """What each stage must move (bytes) or compute (flops) for this workload."""
+    import numpy as np
+    n = wl.q_pos.astype(np.int64) + 1
+    m = np.minimum(n, wl.K)
+    # keys shared by the queries of a sequence are read once
+    per_seq = {}
+    for b, nn in zip(wl.q_seq, n):
+        per_seq[int(b)] = max(per_seq.get(int(b), 0), int(nn))
+    key_bytes = sum(per_seq.values()) * (wl.D_I + 4)
+    qi_bytes = wl.T * wl.H_I * (wl.D_I + 8)
+    score_bytes = int(n.sum()) * 4
+    gather = int(m.sum()) * (656 if wl.mla_dtype == "e4m3" else wl.d_qk * 2)
+    q_bytes = wl.T * wl.H * wl.d_qk * 2
+    out_bytes = wl.T * wl.H * (wl.d_v * 2 + 4)
+    idx_bytes = wl.T * wl.K * 4
+    causal_pairs = int(n.sum())
+    return {
+        "indexer": {"bytes": key_bytes + qi_bytes + score_bytes,
+                    "flops": causal_pairs * wl.H_I * wl.D_I * 2},
+        "topk": {"bytes": score_bytes + idx_bytes},
+        "attn": {"bytes": gather + q_bytes + out_bytes + idx_bytes,
+                 "flops": int(m.sum()) * wl.H * (wl.d_qk + wl.d_v) * 2},
+        # the step: keys + indexer queries + gathered rows + MLA queries + outputs
+        "step_bytes": key_bytes + qi_bytes + gather + q_bytes + out_bytes,
+    }
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc = index, None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.15)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        sm.sort()
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def kernel_count(plan: str) -> int:
+    return sum(plan.count(k) for k in ("indexer_tc", "indexer_generic", "topk_radix", "attn_tc",
+                                       "attn_generic", "attn_combine"))
+
+
+def traffic_from_profiles(kernel_file: str, workload: str):
+    """DRAM bytes per launch recorded in profiles/ for this workload, if the
+    kernel source is unchanged since the capture (sha256 prefix)."""
+    src = os.path.join(ROOT, "dsa_indexed_sparse_gb300", "csrc", kernel_file)
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        for line in open(os.path.join(pdir, f)):
+            mt = re.match(r"traffic_per_launch:\s*workload=(\S+)\s+kernel_src=(\S+)\s+sha=(\w+)\s+bytes=(\d+)", line)
+            if mt and mt.group(1) == workload and mt.group(2) == kernel_file and mt.group(3) == sha:
+                return int(mt.group(4))
+    return None
+
+
+def time_graph(torch, graph, replays, stream):
+    """Replays on `stream` (the stream the events are recorded on)."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(replays):
+            graph.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / 1e3  # seconds
+
+
+def capture(torch, fn, copies, stream):
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for c in copies:
+            fn(c)  # warm: attribute setup happens outside capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for c in copies:
+                fn(c)
+    return g
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+
+def oracle_rate(wl, budget_s: float):
+    """The CPU oracle as it stands on a bounded sample of the workload: whole
+    decode steps (all queries) for decode workloads; a subset of query rows for
+    prefill.  Returns (tokens/s, sample description)."""
+    from oracle import dsa_oracle as O
+    t0 = time.perf_counter()
+    if wl.name.startswith("prefill"):
+        import numpy as np
+        rows = list(np.linspace(0, wl.T - 1, 8).astype(int))
+        done = 0
+        while True:
+            O.decode_step(wl, ts=rows)
+            done += len(rows)
+            if time.perf_counter() - t0 > budget_s:
+                break
+        el = time.perf_counter() - t0
+        return done / el, f"{done} query rows of the prefill (rows spread over positions 0..{wl.T - 1}) in {el:.1f} s"
+    steps = 0
+    while True:
+        O.decode_step(wl)
+        steps += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    el = time.perf_counter() - t0
+    return steps * wl.T / el, f"{steps} full decode steps ({steps * wl.T} query tokens) in {el:.1f} s"
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode_b1", choices=sorted(DESCRIPTIONS))
+    ap.add_argument("--oracle-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    import dsa_workloads as W
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        wl = W.make(args.workload, seed=0)
+        steps = args.steps or 3
+        warm = max(args.warmup, 0)
+        for _ in range(min(warm, 1)):
+            oracle_rate(wl, 0.0)
+        budget = max(1.0, args.oracle_seconds * steps / 3)
+        rate, sample = oracle_rate(wl, budget)
+        unit = "tok/s"
+        line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": unit, "n_gpus": 1,
+                "steps": steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.T / rate,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}"},
+                "cpu_baseline": {"value": rate, "unit": unit, "cores": host_cores(), "kind": "oracle",
+                                 "sample": sample},
+                "e2e": {"value": rate, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return 0
+
+    if world > 1 or args.gpus != 1:
+        print(json.dumps({"error": "single-GPU path: the benchmark runs on one GPU (replicas only)"}))
+        return 2
+
+    import numpy as np
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import dsa_indexed_sparse_gb300 as dsa
+
+    peaks = load_peaks()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    wl = W.make(args.workload, seed=0)
+    alg = algorithmic(wl)
+    copies_n = max(1, min(64, math.ceil(2 * L2_BYTES / max(alg["step_bytes"], 1)) + 1))
+    default_steps = {"decode_b1": 20000, "decode_b64": 2000, "decode_b4_long": 5000, "prefill_16k": 10}
+    steps = args.steps or default_steps[args.workload]
+    warmup = max(3, args.warmup)
+
+    tens = W.device_tensors(wl, dev, copies=copies_n) if copies_n > 1 else [W.device_tensors(wl, dev)]
+    runs = []
+    for d in tens:
+        seq, idxr, mla = dsa.Seq(**d["seq"]), dsa.Indexer(**d["indexer"]), dsa.Mla(**d["mla"])
+        out = torch.empty((wl.T, wl.H, wl.d_v), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+        runs.append(dict(seq=seq, idxr=idxr, mla=mla, out=out, lse=lse))
+    ws_bytes = dsa.decode_workspace_size(runs[0]["seq"], runs[0]["idxr"], runs[0]["mla"], wl.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ld = (wl.max_ctx + 3) // 4 * 4
+    scores = torch.empty((wl.T, ld), dtype=torch.float32, device=dev)
+    sel = torch.empty((wl.T, wl.K), dtype=torch.int32, device=dev)
+    attn_ws = torch.empty(max(16, dsa.sparse_mla_attn_workspace_size(runs[0]["seq"], runs[0]["mla"], wl.K)),
+                          dtype=torch.uint8, device=dev)
+    stream = torch.cuda.Stream()
+
+    def step(r):
+        dsa.decode_step(r["seq"], r["idxr"], r["mla"], wl.K, r["out"], ws, lse=r["lse"], stream=stream)
+
+    def st_indexer(r):
+        dsa.indexer_scores(r["seq"], r["idxr"], scores, stream=stream)
+
+    def st_topk(r):
+        dsa.topk(r["seq"], scores, wl.K, sel, stream=stream)
+
+    def st_attn(r):
+        dsa.sparse_mla_attn(r["seq"], r["mla"], sel, wl.K, r["out"], lse=r["lse"], workspace=attn_ws, stream=stream)
+
+    # correctness of the configuration before timing
+    with torch.cuda.stream(stream):
+        step(runs[0])
+    plan = dsa.last_plan()
+    dsa.check_status(stream)
+
+    g_step = capture(torch, step, runs, stream)
+    per_replay = len(runs)
+    replays = max(1, math.ceil(steps / per_replay))
+    steps = replays * per_replay
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / per_replay))):
+            g_step.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        t_step = time_graph(torch, g_step, replays, stream)
+    dsa.check_status(stream)
+    clocks = clk.summary()
+    ms_per_step = 1e3 * t_step / steps
+    value = wl.T * steps / t_step
+
+    # per-stage timing (same rotation, stage alone) for the roofline of the dominant kernel
+    stage_t = {}
+    stage_plan = {}
+    for name, fn in (("indexer", st_indexer), ("topk", st_topk), ("attn", st_attn)):
+        with torch.cuda.stream(stream):
+            fn(runs[0])
+        stage_plan[name] = dsa.last_plan()
+        g = capture(torch, fn, runs, stream)
+        rp = max(1, min(replays, math.ceil(200 / per_replay)))
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        stage_t[name] = time_graph(torch, g, rp, stream) / (rp * per_replay)
+        dsa.check_status(stream)
+    dom = max(stage_t, key=stage_t.get)
+    if dom == "attn" and wl.name.startswith("prefill"):
+        achieved = alg["attn"]["flops"] / stage_t["attn"] / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    elif dom == "indexer" and wl.name.startswith("prefill"):
+        achieved = alg["indexer"]["flops"] / stage_t["indexer"] / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": 2 * peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        achieved = alg[dom]["bytes"] / stage_t[dom] / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    kfile = {"indexer": "indexer.cu", "topk": "topk.cu", "attn": "attn.cu"}[dom]
+    roof["traffic"] = traffic_from_profiles(kfile, args.workload)
+    roof["kernel"] = stage_plan[dom]
+    roof["peak_src"] = peaks["src"]
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    # per-step inputs (indexer query + scales + head weights, MLA query, positions) travel
+    # host -> device in one packed pinned buffer; out + lse come back in another
+    r0 = runs[0]
+    parts = [r0["idxr"].q, r0["idxr"].q_scale, r0["idxr"].w, r0["mla"].q, r0["seq"].q_pos, r0["seq"].q_seq]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs = np.cumsum([0] + [(s + 255) // 256 * 256 for s in sizes])
+    h_pack = torch.empty(int(offs[-1]), dtype=torch.uint8).pin_memory()
+    d_pack = torch.empty(int(offs[-1]), dtype=torch.uint8, device=dev)
+    views = []
+    for t, o, n in zip(parts, offs[:-1], sizes):
+        h_pack[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+        views.append(d_pack[o:o + n].view(t.dtype).view(t.shape))
+    e_seq = dsa.Seq(q_seq=views[5], q_pos=views[4], block_table=r0["seq"].block_table, max_ctx=r0["seq"].max_ctx,
+                    cache_rows=r0["seq"].cache_rows, page_size=r0["seq"].page_size, q_per_seq=r0["seq"].q_per_seq)
+    e_idx = dsa.Indexer(q=views[0], w=views[2], k_cache=r0["idxr"].k_cache, q_scale=views[1],
+                        k_scale=r0["idxr"].k_scale)
+    e_mla = dsa.Mla(q=views[3], kv_cache=r0["mla"].kv_cache, d_latent=wl.d_latent, d_rope=wl.d_rope,
+                    softmax_scale=wl.softmax_scale, dtype=r0["mla"].dtype)
+    out_bytes = r0["out"].numel() * 2
+    d_res = torch.empty(out_bytes + r0["lse"].numel() * 4, dtype=torch.uint8, device=dev)
+    e_out = d_res[:out_bytes].view(torch.bfloat16).view(r0["out"].shape)
+    e_lse = d_res[out_bytes:].view(torch.float32).view(r0["lse"].shape)
+    h_res = torch.empty(d_res.numel(), dtype=torch.uint8).pin_memory()
+    h2d = int(sum(sizes))
+    d2h = int(d_res.numel())
+    e2e_steps = max(3, min(steps, 2000))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            d_pack.copy_(h_pack, non_blocking=True)
+            dsa.decode_step(e_seq, e_idx, e_mla, wl.K, e_out, ws, lse=e_lse, stream=stream)
+            h_res.copy_(d_res, non_blocking=True)
+
+    for _ in range(warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    t_e2e = ev0.elapsed_time(ev1) / 1e3
+    e2e = {"value": wl.T * e2e_steps / t_e2e, "unit": "tok/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+    dsa.check_status(stream)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": 1, "steps": steps, "warmup": warmup,
+        "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3+bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {DESCRIPTIONS[args.workload]}",
+                   "l2": f"{len(runs)} rotated input copies, {alg['step_bytes'] / 1e6:.1f} MB touched per step "
+                         f"(inputs larger than L2 between reuses)",
+                   "cuda_graph": f"{per_replay} steps per graph replay", "plan": plan,
+                   "step_algorithmic_bytes": alg["step_bytes"],
+                   "step_hbm_frac": alg["step_bytes"] / (ms_per_step / 1e3) / 1e9 / peaks["hbm_gbs"],
+                   "stage_us": {k: v * 1e6 for k, v in stage_t.items()}},
+        "roofline": roof,
+        "e2e": e2e,
+        "gpu_launches": kernel_count(plan) * steps,
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline:
+        rate, sample = oracle_rate(wl, args.oracle_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": host_cores(), "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line))
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,715 @@
+// Sparse MLA attention over the selected latent rows (step 3 of the DSA path).
+//
+// "Large Language Model Inference Acceleration in Practice", section 1.2 (SFA)
+// and section 3.1: using the indices produced by the lightning indexer, the
+// kernel reads only the selected positions' rows from the paged KV cache and runs
+// flash attention over them.  MQA form over the MLA latent cache: each cache row
+// holds a 576-d key (512 latent + 64 rope) whose first 512 values are also the
+// value; all heads of a query share the rows.  For query t, head h and selected
+// set S:
+//     logit_s = scale * q[t,h] . row_s[0:576],  out = sum_s softmax(logit)_s row_s[0:512],
+//     lse = log sum_s exp(logit_s).
+//
+// Kernels:
+//  * attn_tc_kernel<kFp8> -- tensor-core path for H = 128, 512 + 64 dims, bf16 rows or
+//    656-byte FP8 rows.  FP8 codes are widened to bf16 exactly (no scale applied)
+//    while gathering; the per-row scale is applied to the latent part of the logit
+//    (S_latent and S_rope accumulate in separate TMEM columns) and folded into P
+//    for P V, so the FP8 path rounds nothing the bf16 path does not.  One CTA handles one
+//    query, one half of the value dims (256 of 512) and one contiguous slice of the
+//    selected rows.  The CTA pair covering both value halves computes the same
+//    logits: O[128 x 512] fp32 would fill all of TMEM, so each CTA keeps a
+//    [128 x 256] accumulator plus double-buffered logits.
+//      warps 0-3: gather 32 selected rows per tile with 16-byte cp.async through
+//                 the page table into a 128-byte-swizzled K-major tile (two
+//                 producer groups own one ring stage each);
+//      warp 8   : issues S = Q K^T (M=128 heads, N=32 rows, K=576) and
+//                 O += P V (M=128, N=256, K=32) with tcgen05.mma, accumulators in TMEM;
+//      warps 4-7: online softmax, one thread per head (its TMEM lane), P written
+//                 as bf16 to shared memory, the denominator summed from the fp32
+//                 weights; the running max is only moved (and O rescaled in
+//                 TMEM) when it grows by more than 2^8.
+//  * attn_combine_kernel -- merges per-slice partial results by their LSE.
+//  * attn_generic_kernel -- CUDA cores, any head count / dims / row format.
+#include <algorithm>
+#include <cmath>
+#include <cstdio>
+#include <mutex>
+
+#include "dsa_device.cuh"
+#include "dsa_internal.h"
+
+DSA_DEFINE_STATUS_WORD(attn)
+
+namespace dsa {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// =============================================================== generic kernel
+constexpr int kGenThreads = 128;
+
+__device__ __forceinline__ float load_elem(MlaKind kind, const uint8_t* row, int d) {
+  switch (kind) {
+    case MlaKind::kF32:
+      return reinterpret_cast<const float*>(row)[d];
+    case MlaKind::kBF16:
+      return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[d]);
+    default: {  // 656-byte FP8 row
+      if (d < 512) return e4m3_to_float(row[d]) * *reinterpret_cast<const float*>(row + 512);
+      return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row + 528)[d - 512]);
+    }
+  }
+}
+
+__device__ __forceinline__ float block_reduce_max(float v, float* buf) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  float r = buf[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, buf[w]);
+  return r;
+}
+__device__ __forceinline__ float block_reduce_sum(float v, float* buf) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) buf[warp] = v;
+  __syncthreads();
+  float r = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += buf[w];
+  return r;
+}
+
+__global__ void __launch_bounds__(kGenThreads)
+    attn_generic_kernel(SeqArgs seq, MlaArgs a) {
+  extern __shared__ float sm_gen[];
+  const int dqk = a.d_latent + a.d_rope, dv = a.d_latent, K = a.K;
+  float* qs = sm_gen;                                            // [dqk]
+  float* ps = qs + dqk;                                          // [K] logits then weights
+  int32_t* rows = reinterpret_cast<int32_t*>(ps + K);            // [K] physical rows
+  __shared__ float red[kGenThreads / 32];
+  const int h = blockIdx.x, t = blockIdx.y;
+  const int qp = __ldg(seq.q_pos + t);
+  const int b = __ldg(seq.q_seq + t);
+  const bool q_ok = qp >= 0 && qp < seq.max_ctx && b >= 0 && b < seq.B;
+  if (!q_ok && threadIdx.x == 0 && h == 0) atomicOr(&g_status_attn, kDevBadPos);
+  const int64_t qoff = (static_cast<int64_t>(t) * a.H + h) * dqk;
+  for (int d = threadIdx.x; d < dqk; d += blockDim.x) {
+    qs[d] = (a.kind == MlaKind::kF32) ? static_cast<const float*>(a.q)[qoff + d]
+                                      : bf16_bits_to_float(static_cast<const uint16_t*>(a.q)[qoff + d]);
+  }
+  __syncthreads();
+  const uint8_t* kv = static_cast<const uint8_t*>(a.kv);
+  const int32_t* bt = seq.block_table + static_cast<int64_t>(q_ok ? b : 0) * seq.bt_stride;
+  float mloc = -INFINITY;
+  for (int r = threadIdx.x; r < K; r += blockDim.x) {
+    const int pos = __ldg(a.idx + static_cast<int64_t>(t) * K + r);
+    int64_t prow = -1;
+    if (q_ok && pos >= 0) {
+      if (pos > qp) {
+        atomicOr(&g_status_attn, kDevBadIndex);
+      } else {
+        prow = phys_row(bt, pos, seq.page_size, seq.n_pages, &g_status_attn);
+      }
+    }
+    rows[r] = static_cast<int32_t>(prow);
+    float logit = -INFINITY;
+    if (prow >= 0) {
+      const uint8_t* rp = kv + prow * a.row_bytes;
+      float acc = 0.f;
+      for (int d = 0; d < dqk; ++d) acc = fmaf(qs[d], load_elem(a.kind, rp, d), acc);
+      logit = acc * a.softmax_scale;
+    }
+    ps[r] = logit;
+    mloc = fmaxf(mloc, logit);
+  }
+  const float m = block_reduce_max(mloc, red);
+  float lsum = 0.f;
+  for (int r = threadIdx.x; r < K; r += blockDim.x) {
+    const float p = (m == -INFINITY || ps[r] == -INFINITY) ? 0.f : __expf(ps[r] - m);
+    ps[r] = p;
+    lsum += p;
+  }
+  const float l = block_reduce_sum(lsum, red);  // includes a __syncthreads
+  const float inv = l > 0.f ? 1.f / l : 0.f;
+  const int64_t ooff = (static_cast<int64_t>(t) * a.H + h) * dv;
+  for (int d = threadIdx.x; d < dv; d += blockDim.x) {
+    float acc = 0.f;
+    for (int r = 0; r < K; ++r) {
+      if (rows[r] >= 0) acc = fmaf(ps[r], load_elem(a.kind, kv + static_cast<int64_t>(rows[r]) * a.row_bytes, d), acc);
+    }
+    acc *= inv;
+    if (a.kind == MlaKind::kF32)
+      static_cast<float*>(a.out)[ooff + d] = acc;
+    else
+      static_cast<__nv_bfloat16*>(a.out)[ooff + d] = __float2bfloat16_rn(acc);
+  }
+  if (threadIdx.x == 0 && a.lse)
+    a.lse[static_cast<int64_t>(t) * a.H + h] = l > 0.f ? m + logf(l) : -INFINITY;
+}
+
+// =============================================================== tcgen05 kernel
+constexpr int kH = 128;          // heads = UMMA M
+constexpr int kDqk = 576;
+constexpr int kDv = 512;
+constexpr int kDvHalf = 256;     // value dims per CTA = UMMA N of P V
+constexpr int kBR = 32;          // rows per tile = UMMA N of Q K^T
+constexpr int kQBytes = kH * kDqk * 2;             // 147456
+constexpr int kTileBytes = kBR * kDqk * 2;         // 36864
+constexpr int kPBytes = kH * kBR * 2;              // 8192
+constexpr int kOffQ = 0;
+constexpr int kOffKV = kOffQ + kQBytes;
+constexpr int kOffP = kOffKV + 2 * kTileBytes;
+constexpr int kOffMask = kOffP + kPBytes;          // uint16 [2 stages][2 warps]
+constexpr int kOffScale = kOffMask + 16;           // float [2 stages][32] FP8 row scales
+constexpr int kOffBar = kOffScale + 2 * kBR * 4;
+// barriers: full[2], empty[2], sfull[2], pfull, pvdone, ofull
+constexpr int kNumBars = 9;
+constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
+constexpr int kThreads = 288;                      // 4 producer, 4 softmax, 1 MMA warp
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kColS = 0;                      // S buffers: [0,32), [32,64)
+constexpr uint32_t kColSr = 64;                    // FP8 rows: rope part of S, [64,96), [96,128)
+constexpr uint32_t kColO = 256;                    // O: [256, 512)
+constexpr uint32_t kIdescS = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR);
+constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, kFmtBF16, false, true, kH, kDvHalf);
+constexpr float kRescaleThreshold = 8.0f;          // log2 units
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct TcAttnParams {
+  SeqArgs seq;
+  MlaArgs a;
+  int32_t n_split;       // row slices per query
+  int32_t rows_per_split;
+  float* ws_o;           // [n_split, T, H, 512] fp32 partials (n_split > 1)
+  float* ws_lse;         // [n_split, T, H]
+};
+
+// Byte offset of 16-byte chunk `ch` (of 72) of tile row `r` in a 128B-swizzled
+// K-major tile of `rows` rows: atom (64 values) major, then row, then swizzled chunk.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
+  return static_cast<uint32_t>((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
+}
+
+template <bool kFp8>
+__global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint64_t* full = bars;         // [2] producer group g -> stage g
+  uint64_t* empty = bars + 2;    // [2]
+  uint64_t* sfull = bars + 4;    // [2]
+  uint64_t* pfull = bars + 6;
+  uint64_t* pvdone = bars + 7;
+  uint64_t* ofull = bars + 8;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + kOffMask);
+  volatile float* row_scale = reinterpret_cast<volatile float*>(sm + kOffScale);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x & 1;                     // value half
+  const int rest = blockIdx.x >> 1;
+  const int split = rest % p.n_split;
+  const int t = rest / p.n_split;
+  const int K = p.a.K;
+  const int r0 = split * p.rows_per_split;
+  const int r1 = min(K, r0 + p.rows_per_split);
+  const int ntiles = (r1 - r0 + kBR - 1) / kBR;     // >= 1 (host guarantees r0 < K)
+
+  int qp = __ldg(p.seq.q_pos + t);
+  int b = __ldg(p.seq.q_seq + t);
+  if (qp < 0 || qp >= p.seq.max_ctx || b < 0 || b >= p.seq.B) {
+    if (threadIdx.x == 0) atomicOr(&g_status_attn, kDevBadPos);
+    qp = -1;  // every row masked
+    b = 0;
+  }
+
+  // ---- setup: barriers, TMEM, Q tile --------------------------------------
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&full[i], 64);
+      mbar_init(&empty[i], 1);
+      mbar_init(&sfull[i], 1);
+    }
+    mbar_init(pfull, 128);
+    mbar_init(pvdone, 1);
+    mbar_init(ofull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(misc, kTmemCols);
+    tmem_relinquish();
+  }
+  {
+    const uint16_t* qg = static_cast<const uint16_t*>(p.a.q) + static_cast<int64_t>(t) * kH * kDqk;
+    const uint32_t qbase = smem_u32(sm + kOffQ);
+    for (int i = threadIdx.x; i < kH * (kDqk / 8); i += kThreads) {
+      const int h = i / (kDqk / 8), ch = i % (kDqk / 8);
+      cp_async16(qbase + sw128_offset(h, ch, kH), qg + h * kDqk + ch * 8);
+    }
+    cp_async_commit();
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  if (warp < 4) {
+    // ------------------------------------------------ producers (2 groups)
+    const int pg = warp >> 1, wi = warp & 1;
+    const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);
+    const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride;
+    const int32_t* idx = p.a.idx + static_cast<int64_t>(t) * K;
+    const uint32_t stage = smem_u32(sm + kOffKV + pg * kTileBytes);
+    for (int j = pg; j < ntiles; j += 2) {
+      // Resolve the warp's 16 rows in parallel (lane r: index -> page -> cache row)
+      // before waiting for the stage, so the dependent loads overlap the wait.
+      int64_t my_row = -1;
+      float my_scale = 0.f;
+      if (lane < 16) {
+        const int gi = r0 + j * kBR + wi * 16 + lane;  // entry of the index list
+        if (gi < r1) {
+          const int pos = __ldg(idx + gi);
+          if (pos >= 0) {
+            if (pos > qp)
+              atomicOr(&g_status_attn, kDevBadIndex);
+            else
+              my_row = phys_row(bt, pos, p.seq.page_size, p.seq.n_pages, &g_status_attn);
+          }
+        }
+        if (kFp8 && my_row >= 0)
+          my_scale = __ldg(reinterpret_cast<const float*>(kv + my_row * p.a.row_bytes + 512));
+      }
+      if (j >= 2) {
+        const bool ok = mbar_wait(&empty[pg], ((j >> 1) - 1) & 1, &g_status_attn, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      if (kFp8 && lane < 16) row_scale[pg * kBR + wi * 16 + lane] = my_scale;
+      const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFFFFu;
+      if (!kFp8) {
+#pragma unroll 1
+        for (int rr = 0; rr < 16; ++rr) {
+          const int rl = wi * 16 + rr;
+          const int64_t prow = __shfl_sync(0xffffffffu, my_row, rr);
+          if (prow >= 0) {
+            const uint8_t* src = kv + prow * p.a.row_bytes;
+            for (int ch = lane; ch < kDqk / 8; ch += 32)
+              cp_async16(stage + sw128_offset(rl, ch, kBR), src + ch * 16);
+          } else {
+            for (int ch = lane; ch < kDqk / 8; ch += 32)
+              st_shared_v4(stage + sw128_offset(rl, ch, kBR), 0u, 0u, 0u, 0u);
+          }
+        }
+      } else {
+        // latent: 16 e4m3 codes per lane and row, all 16 rows' loads in flight
+        // before any conversion; widened to bf16 exactly (two 16-byte chunks)
+        uint4 raw[16];
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          const int64_t prow = __shfl_sync(0xffffffffu, my_row, rr);
+          raw[rr] = prow >= 0 ? ld_global_nc_v4(kv + prow * p.a.row_bytes + lane * 16) : make_uint4(0, 0, 0, 0);
+          if (prow >= 0 && lane < 8)
+            cp_async16(stage + sw128_offset(wi * 16 + rr, 64 + lane, kBR), kv + prow * p.a.row_bytes + 528 + lane * 16);
+          else if (lane < 8)
+            st_shared_v4(stage + sw128_offset(wi * 16 + rr, 64 + lane, kBR), 0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 16; ++rr) {
+          const int rl = wi * 16 + rr;
+          const uint32_t w[4] = {raw[rr].x, raw[rr].y, raw[rr].z, raw[rr].w};
+          uint32_t o[8];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+            const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w[k] >> 16));
+            o[2 * k] = pack_bf16x2(lo.x, lo.y);
+            o[2 * k + 1] = pack_bf16x2(hi.x, hi.y);
+          }
+          st_shared_v4(stage + sw128_offset(rl, 2 * lane, kBR), o[0], o[1], o[2], o[3]);
+          st_shared_v4(stage + sw128_offset(rl, 2 * lane + 1, kBR), o[4], o[5], o[6], o[7]);
+        }
+      }
+      if (lane == 0) mask16[pg * 2 + wi] = static_cast<uint16_t>(bits);
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      mbar_arrive(&full[pg]);
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t qbase = smem_u32(sm + kOffQ);
+      const uint32_t pbase = smem_u32(sm + kOffP);
+      auto issue_pv = [&](int j) {
+        const uint32_t vbase = smem_u32(sm + kOffKV + (j & 1) * kTileBytes) + c * 4 * kBR * 128;
+#pragma unroll
+        for (int kk = 0; kk < kBR / 16; ++kk) {
+          const uint64_t da = make_sdesc(pbase + kk * 256, 128, 512, kLayoutNone);
+          const uint64_t db = make_sdesc(vbase + kk * 16 * 128, kBR * 128, 1024, kLayoutSw128);
+          umma_f16(tmem + kColO, da, db, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(pvdone);
+        umma_commit(&empty[j & 1]);
+      };
+      // Issue S_j as soon as tile j has landed (and its S buffer is free, i.e.
+      // P_{j-2} was consumed) and P V_j as soon as P_j is written, in whichever
+      // order they become ready, so neither kind of MMA waits on the other's inputs.
+      int next_s = 0, next_pv = 0;
+      uint32_t spins = 0;
+      uint64_t stall_t0 = 0;
+      while (next_pv < ntiles) {
+        bool progress = false;
+        if (next_s < ntiles && next_s <= next_pv + 1 &&
+            mbar_try_wait(smem_u32(&full[next_s & 1]), (next_s >> 1) & 1)) {
+          tc_fence_after();
+          const int j = next_s;
+          const uint32_t kbase = smem_u32(sm + kOffKV + (j & 1) * kTileBytes);
+#pragma unroll 4
+          for (int kk = 0; kk < kDqk / 16; ++kk) {
+            const int atom = kk >> 2, sub = kk & 3;
+            const uint64_t da = make_sdesc(qbase + atom * kH * 128 + sub * 32, 16, 1024, kLayoutSw128);
+            const uint64_t db = make_sdesc(kbase + atom * kBR * 128 + sub * 32, 16, 1024, kLayoutSw128);
+            // FP8 rows: latent (k < 512) and rope (k >= 512) logits in separate columns
+            const bool rope = kFp8 && kk >= kDv / 16;
+            const uint32_t col = (rope ? kColSr : kColS) + (j & 1) * kBR;
+            const bool first = kk == 0 || (kFp8 && kk == kDv / 16);
+            umma_f16(tmem + col, da, db, kIdescS, first ? 0u : 1u);
+          }
+          umma_commit(&sfull[j & 1]);
+          ++next_s;
+          progress = true;
+        }
+        if (next_pv < next_s && mbar_try_wait(smem_u32(pfull), next_pv & 1)) {
+          tc_fence_after();
+          issue_pv(next_pv);
+          if (next_pv == ntiles - 1) umma_commit(ofull);
+          ++next_pv;
+          progress = true;
+        }
+        if (progress) {
+          stall_t0 = 0;
+        } else if ((++spins & 63u) == 0u) {
+          if (*abort_flag) break;
+          const uint64_t now = globaltimer_ns();
+          if (stall_t0 == 0) {
+            stall_t0 = now;
+          } else if (now - stall_t0 > kWaitLimitNs) {
+            atomicOr(&g_status_attn, kDevTimeout);
+            *abort_flag = 1;
+            break;
+          }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax + epilogue (warps 4-7)
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.a.softmax_scale * kLog2e;
+    const uint32_t prow_addr = smem_u32(sm + kOffP) + (h >> 3) * 512 + (h & 7) * 16;
+    // l: sum of the bf16 weights actually multiplied into O (normalising by it
+    // makes the output an exact convex combination of the rows); l32: the same
+    // weights in fp32, for the log-sum-exp.
+    float m = -INFINITY, l = 0.f, l32 = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      ok = mbar_wait(&sfull[j & 1], (j >> 1) & 1, &g_status_attn, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // The producers' mask bytes are ordered by their release on full[]: that
+      // phase is still the current one here (the stage is only refilled after
+      // this tile's P V, which needs this thread's arrival on pfull).
+      ok = mbar_wait(&full[j & 1], (j >> 1) & 1, &g_status_attn, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32(tmem + lane_off + kColS + (j & 1) * kBR, r);
+      const uint32_t vmask = static_cast<uint32_t>(mask16[(j & 1) * 2]) |
+                             (static_cast<uint32_t>(mask16[(j & 1) * 2 + 1]) << 16);
+      float x[32];
+      float mloc = -INFINITY;
+      if (kFp8) {
+        uint32_t rr[32];
+        tmem_ld32(tmem + lane_off + kColSr + (j & 1) * kBR, rr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float lg = fmaf(row_scale[(j & 1) * kBR + i], __uint_as_float(r[i]), __uint_as_float(rr[i]));
+          x[i] = ((vmask >> i) & 1u) ? lg * sl2 : -INFINITY;
+          mloc = fmaxf(mloc, x[i]);
+        }
+      } else {
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          x[i] = ((vmask >> i) & 1u) ? __uint_as_float(r[i]) * sl2 : -INFINITY;
+          mloc = fmaxf(mloc, x[i]);
+        }
+      }
+      if (j >= 1) {
+        ok = mbar_wait(pvdone, (j - 1) & 1, &g_status_attn, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const float m_new = fmaxf(m, mloc);
+      const bool need = m_new > m + kRescaleThreshold;
+      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+        const float f = need ? exp2f(m - m_new) : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          tmem_st32(tmem + lane_off + kColO + cc * 32, o);
+        }
+        tmem_st_wait();
+      }
+      if (need) {
+        const float f = exp2f(m - m_new);
+        l *= f;
+        l32 *= f;
+        m = m_new;
+      }
+      const float msub = (m == -INFINITY) ? 0.f : m;
+      float psum = 0.f, psum32 = 0.f;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float p0 = exp2f(x[2 * i] - msub), p1 = exp2f(x[2 * i + 1] - msub);
+        psum32 += p0 + p1;
+        if (kFp8) {
+          // P V runs on the unscaled codes: fold the row scale into P; the
+          // denominator takes the rounded weights divided back by the scale
+          const float s0 = row_scale[(j & 1) * kBR + 2 * i], s1 = row_scale[(j & 1) * kBR + 2 * i + 1];
+          __nv_bfloat162 v = __floats2bfloat162_rn(p0 * s0, p1 * s1);
+          pk[i] = *reinterpret_cast<uint32_t*>(&v);
+          const float2 back = __bfloat1622float2(v);
+          psum += (s0 > 0.f ? back.x / s0 : 0.f) + (s1 > 0.f ? back.y / s1 : 0.f);
+        } else {
+          __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+          pk[i] = *reinterpret_cast<uint32_t*>(&v);
+          const float2 back = __bfloat1622float2(v);
+          psum += back.x + back.y;
+        }
+      }
+      l += psum;
+      l32 += psum32;
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc)
+        st_shared_v4(prow_addr + cc * 128, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(pfull);
+    }
+    if (ok) {
+      ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse = l32 > 0.f ? (m + log2f(l32)) * kLn2 : -INFINITY;
+      const int64_t th = static_cast<int64_t>(t) * kH + h;
+      if (p.n_split == 1) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + th * kDv + c * kDvHalf;
+#pragma unroll 1
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
+          uint4* dst = reinterpret_cast<uint4*>(out + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+        }
+        if (c == 0 && p.a.lse) p.a.lse[th] = lse;
+      } else {
+        const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
+        float* out = p.ws_o + sth * kDv + c * kDvHalf;
+#pragma unroll 1
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_ld_wait();
+          float4* dst = reinterpret_cast<float4*>(out + cc * 32);
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
+                                 __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+        }
+        if (c == 0) p.ws_lse[sth] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Merges row slices: out[t,h,:] = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max_s lse_s);
+// lse = max + log sum_s w_s.  One CTA per (query, group of 8 heads); a warp per head.
+constexpr int kCombineHeads = 8;
+__global__ void __launch_bounds__(256)
+    attn_combine_kernel(const float* ws_o, const float* ws_lse, int n_split, int T, int H, int dv,
+                        __nv_bfloat16* out, float* lse_out) {
+  extern __shared__ float wts[];  // [kCombineHeads][n_split]
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kCombineHeads + warp;
+  float* w = wts + warp * n_split;
+  float m = -INFINITY;
+  for (int s = lane; s < n_split; s += 32) m = fmaxf(m, ws_lse[(static_cast<int64_t>(s) * T + t) * H + h]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+  for (int s = lane; s < n_split; s += 32) {
+    const float l = ws_lse[(static_cast<int64_t>(s) * T + t) * H + h];
+    const float wv = (m == -INFINITY) ? 0.f : __expf(l - m);
+    w[s] = wv;
+    sum += wv;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  __syncwarp();
+  if (lane == 0 && lse_out) lse_out[static_cast<int64_t>(t) * H + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
+  const float inv = sum > 0.f ? 1.f / sum : 0.f;
+  const int64_t th = static_cast<int64_t>(t) * H + h;
+  for (int i = lane; i < dv / 4; i += 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n_split; ++s) {
+      const float ww = w[s];
+      if (ww == 0.f) continue;
+      const float4 v = reinterpret_cast<const float4*>(ws_o + (static_cast<int64_t>(s) * T * H + th) * dv)[i];
+      acc.x = fmaf(ww, v.x, acc.x);
+      acc.y = fmaf(ww, v.y, acc.y);
+      acc.z = fmaf(ww, v.z, acc.z);
+      acc.w = fmaf(ww, v.w, acc.w);
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    reinterpret_cast<uint2*>(out + th * dv)[i] =
+        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+  }
+}
+
+bool tc_supported(const SeqArgs& seq, const MlaArgs& a) {
+  if (a.H != kH || a.d_latent != kDv || a.d_rope != kDqk - kDv) return false;
+  if (a.kind == MlaKind::kF32) return false;
+  if (a.kind == MlaKind::kBF16 && a.row_bytes % 16 != 0) return false;
+  if (a.kind == MlaKind::kFP8Row && a.row_bytes % 16 != 0) return false;
+  if (reinterpret_cast<uintptr_t>(a.kv) % 16 || reinterpret_cast<uintptr_t>(a.q) % 16 ||
+      reinterpret_cast<uintptr_t>(a.out) % 16)
+    return false;
+  (void)seq;
+  return true;
+}
+
+// Row slices per query: fill the GPU with (query, half, slice) CTAs, at least
+// 4 tiles (128 rows) per slice, at most 64 slices.
+int choose_split(const SeqArgs& seq, const MlaArgs& a, int num_sms) {
+  const int max_split = std::min(64, std::max(1, (a.K + 4 * kBR - 1) / (4 * kBR)));
+  const int64_t ctas = 2ll * seq.T;
+  int split = 1;
+  while (split < max_split && ctas * split * 2 <= num_sms) split *= 2;
+  return std::min(split, max_split);
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(const SeqArgs& seq, const MlaArgs& a, int num_sms) {
+  if (!tc_supported(seq, a) || seq.T == 0) return 0;
+  const int split = choose_split(seq, a, num_sms);
+  if (split <= 1) return 0;
+  const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(float);
+  const size_t l = static_cast<size_t>(split) * seq.T * kH * sizeof(float);
+  return ((o + 255) / 256) * 256 + ((l + 255) / 256) * 256;
+}
+
+cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, size_t ws_bytes,
+                        const LaunchEnv& env, std::string* plan, bool* unsupported,
+                        std::string* why) {
+  *unsupported = false;
+  if (seq.T == 0) {
+    *plan += "attn[empty]";
+    return cudaSuccess;
+  }
+  if (tc_supported(seq, a)) {
+    int split = choose_split(seq, a, env.num_sms);
+    if (split > 1 && (workspace == nullptr || ws_bytes < attn_workspace_bytes(seq, a, env.num_sms)))
+      split = 1;  // no room for partials: one slice per query
+    const int rps = ((a.K + split - 1) / split + kBR - 1) / kBR * kBR;
+    split = (a.K + rps - 1) / rps;  // every slice non-empty
+    TcAttnParams p{seq, a, split, rps, nullptr, nullptr};
+    if (split > 1) {
+      const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(float);
+      p.ws_o = static_cast<float*>(workspace);
+      p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o + 255) / 256) * 256);
+    }
+    const bool fp8 = a.kind == MlaKind::kFP8Row;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+      attr_err = cudaFuncSetAttribute(attn_tc_kernel<false>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int grid = seq.T * split * 2;
+    if (fp8)
+      attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, env.stream>>>(p);
+    else
+      attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, env.stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    char buf[128];
+    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8" : "bf16", split, grid);
+    *plan += buf;
+    if (split > 1) {
+      const size_t smem = static_cast<size_t>(split) * kCombineHeads * sizeof(float);
+      attn_combine_kernel<<<dim3(seq.T, kH / kCombineHeads), 256, smem, env.stream>>>(
+          p.ws_o, p.ws_lse, split, seq.T, kH, kDv, static_cast<__nv_bfloat16*>(a.out), a.lse);
+      *plan += "+attn_combine";
+      e = cudaGetLastError();
+    }
+    return e;
+  }
+  const int dqk = a.d_latent + a.d_rope;
+  const size_t smem = static_cast<size_t>(dqk) * 4 + static_cast<size_t>(a.K) * 8;
+  if (smem > 200 * 1024) {
+    *unsupported = true;
+    *why = "attn: K or head dim too large for the generic kernel";
+    return cudaSuccess;
+  }
+  if (smem > 48 * 1024)
+    cudaFuncSetAttribute(attn_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+  dim3 grid(a.H, seq.T);
+  attn_generic_kernel<<<grid, kGenThreads, smem, env.stream>>>(seq, a);
+  *plan += "attn_generic";
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

@@ -1,0 +1,85 @@
+// Host-side interface between the C-ABI facade (api.cu) and the kernel
+// translation units.  Plain structs passed by value to the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include <string>
+
+namespace dsa {
+
+struct SeqArgs {
+  int32_t B, T, max_ctx, q_per_seq;
+  const int32_t* q_seq;
+  const int32_t* q_pos;
+  const int32_t* block_table;
+  int32_t bt_stride, page_size;
+  int64_t cache_rows;
+  int64_t n_pages;  // cache_rows / page_size
+};
+
+struct IndexerArgs {
+  int32_t H_I, D_I;
+  bool e4m3;  // else fp32
+  const void* q;
+  const float* q_scale;  // may be null
+  const float* w;
+  const void* k;
+  const float* k_scale;  // may be null
+  float* scores;
+  int64_t ld;
+};
+
+enum class MlaKind { kF32 = 0, kBF16 = 1, kFP8Row = 2 };
+
+struct MlaArgs {
+  int32_t H, d_latent, d_rope;
+  MlaKind kind;
+  const void* q;
+  const void* kv;
+  int64_t row_bytes;
+  float softmax_scale;
+  const int32_t* idx;
+  int32_t K;
+  void* out;
+  float* lse;  // may be null
+};
+
+struct LaunchEnv {
+  cudaStream_t stream;
+  int num_sms;
+  int device;
+};
+
+// Each launcher validates kernel-specific limits, enqueues its kernels and
+// appends a short description of what it launched to *plan.  Returns
+// cudaSuccess or the launch error; `unsupported` is set (and nothing launched)
+// when no kernel covers the arguments.
+
+// Lightning indexer.
+cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
+                           std::string* plan, bool* unsupported, std::string* why);
+
+// Top-K.
+cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int32_t K,
+                        int32_t* idx, const LaunchEnv& env, std::string* plan);
+
+// Sparse MLA attention.  workspace may be null (ws_bytes 0).
+size_t attn_workspace_bytes(const SeqArgs& seq, const MlaArgs& a, int num_sms);
+cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, size_t ws_bytes,
+                        const LaunchEnv& env, std::string* plan, bool* unsupported,
+                        std::string* why);
+
+// Tensor-map encoder (driver entry point, resolved once).
+bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
+                       uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
+                       std::string* why);
+
+}  // namespace dsa
+
+// Per-translation-unit device status words (read and clear; 0xFFFFFFFF on error).
+uint32_t dsa_status_read_clear_indexer();
+uint32_t dsa_status_read_clear_topk();
+uint32_t dsa_status_read_clear_attn();

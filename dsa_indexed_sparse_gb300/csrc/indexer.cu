@@ -1,0 +1,512 @@
+// Lightning-indexer scores (step 1 of the DSA path).
+//
+// "Day0 Inference Adaptation and Performance Optimization for Kimi K3.1 Pro",
+// section 3: relevance scores between each query and every historical position,
+// weighted by per-head weights, read from the paged key cache.  Per query t and
+// causal position s <= q_pos[t]:
+//     I[t, s] = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s])
+// with q_I = q_code * q_scale[t,h] and k_I = k_code * k_scale[s].  Because the
+// scales are positive, the kernels factor them out of the ReLU:
+//     I[t, s] = k_scale[s] * sum_h (w[t,h] * q_scale[t,h]) * ReLU(q_code . k_code)
+//
+// Two kernels:
+//  * indexer_tc_kernel<G> -- the tensor-core path (FP8 e4m3, H_I = 64, D_I = 128,
+//    64-token pages).  Swap-AB tcgen05 GEMM: the 128 keys of a tile are the M
+//    rows (TMEM lanes), the G queries x 64 heads of a query group are the N
+//    columns, K = 128.  Keys arrive page by page through TMA (128-byte swizzle),
+//    accumulators live in TMEM (double buffered) and 4 epilogue warps turn each
+//    key's row of G*64 dot products into G scores with an in-thread head sum.
+//    Persistent: every CTA takes an equal contiguous share of the (group, key
+//    tile) list, computed on the device from q_pos.
+//  * indexer_generic_kernel -- CUDA cores, any H_I/D_I, fp32 or e4m3.
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "dsa_device.cuh"
+#include "dsa_internal.h"
+
+DSA_DEFINE_STATUS_WORD(indexer)
+
+namespace dsa {
+namespace {
+
+// =============================================================== generic kernel
+constexpr int kGenThreads = 256;
+
+template <bool kE4M3>
+__global__ void __launch_bounds__(kGenThreads)
+    indexer_generic_kernel(SeqArgs seq, IndexerArgs a) {
+  extern __shared__ float sm_gen[];
+  float* qf = sm_gen;                   // [H_I * D_I] query codes (as float)
+  float* wq = sm_gen + a.H_I * a.D_I;  // [H_I] w * q_scale
+  const int t = blockIdx.y;
+  const int qpos = __ldg(seq.q_pos + t);
+  const int b = __ldg(seq.q_seq + t);
+  if (qpos < 0 || qpos >= seq.max_ctx || b < 0 || b >= seq.B) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(&g_status_indexer, kDevBadPos);
+    return;
+  }
+  const int HD = a.H_I * a.D_I;
+  for (int i = threadIdx.x; i < HD; i += blockDim.x) {
+    if (kE4M3)
+      qf[i] = e4m3_to_float(static_cast<const uint8_t*>(a.q)[static_cast<int64_t>(t) * HD + i]);
+    else
+      qf[i] = static_cast<const float*>(a.q)[static_cast<int64_t>(t) * HD + i];
+  }
+  for (int h = threadIdx.x; h < a.H_I; h += blockDim.x) {
+    const float sq = a.q_scale ? __ldg(a.q_scale + static_cast<int64_t>(t) * a.H_I + h) : 1.f;
+    wq[h] = __ldg(a.w + static_cast<int64_t>(t) * a.H_I + h) * sq;
+  }
+  __syncthreads();
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s > qpos) return;
+  const int64_t row = phys_row(seq.block_table + static_cast<int64_t>(b) * seq.bt_stride, s,
+                               seq.page_size, seq.n_pages, &g_status_indexer);
+  if (row < 0) return;
+  float acc = 0.f;
+  for (int h = 0; h < a.H_I; ++h) {
+    float d = 0.f;
+    if (kE4M3) {
+      const uint8_t* kr = static_cast<const uint8_t*>(a.k) + row * a.D_I;
+      for (int i = 0; i < a.D_I; ++i) d = fmaf(qf[h * a.D_I + i], e4m3_to_float(kr[i]), d);
+    } else {
+      const float* kr = static_cast<const float*>(a.k) + row * a.D_I;
+      for (int i = 0; i < a.D_I; ++i) d = fmaf(qf[h * a.D_I + i], kr[i], d);
+    }
+    acc = fmaf(wq[h], fmaxf(d, 0.f), acc);
+  }
+  const float sk = a.k_scale ? __ldg(a.k_scale + row) : 1.f;
+  a.scores[static_cast<int64_t>(t) * a.ld + s] = acc * sk;
+}
+
+// =============================================================== tcgen05 kernel
+constexpr int kTcHeads = 64;       // H_I
+constexpr int kTcDim = 128;        // D_I (bytes per key row)
+constexpr int kTcKeys = 128;       // keys per tile = UMMA M
+constexpr int kTcPage = 64;        // tokens per page
+constexpr int kTcStages = 6;       // key-tile ring depth (16 KB each)
+constexpr int kTcThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
+constexpr int kTcEpiThreads = 128;
+
+template <int G>
+struct TcCfg {
+  static constexpr int N = kTcHeads * G;                 // UMMA N
+  static constexpr int kStageBytes = kTcKeys * kTcDim;   // 16384
+  static constexpr int kQBytes = N * kTcDim;             // one query-group buffer
+  static constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128u : ((2 * N <= 256) ? 256u : 512u);
+  static constexpr int kOffStages = 0;
+  static constexpr int kOffQ = kOffStages + kTcStages * kStageBytes;
+  static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [2][G*64]
+  static constexpr int kOffBar = kOffWq + 2 * N * 4;
+  // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2]
+  static constexpr int kNumBars = 2 * kTcStages + 8;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, sched[4]
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr uint32_t kIdesc = make_idesc(kFmtE4M3, kFmtE4M3, false, false, kTcKeys, N);
+};
+
+struct TcParams {
+  SeqArgs seq;
+  IndexerArgs a;
+  int32_t n_groups;
+};
+
+// Number of 128-key tiles of query group g (its longest causal history), with
+// q_pos validation.  Also returns the group's history length.
+template <int G>
+__device__ __forceinline__ int group_tiles(const TcParams& p, int g, int* n_hist) {
+  int n = 0;
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    const int t = g * G + j;
+    if (t < p.seq.T) {
+      const int qp = __ldg(p.seq.q_pos + t);
+      if (qp < 0 || qp >= p.seq.max_ctx) {
+        atomicOr(&g_status_indexer, kDevBadPos);
+      } else {
+        n = max(n, qp + 1);
+      }
+    }
+  }
+  *n_hist = n;
+  return (n + kTcKeys - 1) / kTcKeys;
+}
+
+// Walks the (group, key tile) list from a starting point.
+template <int G>
+struct TileWalker {
+  int g, kt, ntiles, nhist;
+  __device__ void init(const TcParams& p, int g0, int kt0) {
+    g = g0;
+    kt = kt0;
+    ntiles = group_tiles<G>(p, g, &nhist);
+  }
+  __device__ void advance(const TcParams& p) {
+    ++kt;
+    while (kt >= ntiles && g + 1 < p.n_groups) {
+      ++g;
+      kt = 0;
+      ntiles = group_tiles<G>(p, g, &nhist);
+    }
+  }
+};
+
+__device__ __forceinline__ int block_sum_192(int v, int* red) {
+  // 6 warps
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  int tot = 0;
+#pragma unroll
+  for (int w = 0; w < kTcThreads / 32; ++w) tot += red[w];
+  return tot;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap qmap, TcParams p) {
+  using C = TcCfg<G>;
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kTcStages;
+  uint64_t* qfull = bars + 2 * kTcStages;
+  uint64_t* qempty = qfull + 2;
+  uint64_t* accfull = qfull + 4;
+  uint64_t* accempty = qfull + 6;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  int* sched = reinterpret_cast<int*>(misc + 2);   // g0, kt0
+  int* red = reinterpret_cast<int*>(misc + 4);     // 6 ints
+  float* wq_s = reinterpret_cast<float*>(sm + C::kOffWq);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // ---- work split: equal share of the global tile list -----------------
+  int total = 0;
+  for (int g0 = 0; g0 < p.n_groups; g0 += kTcThreads) {
+    const int g = g0 + threadIdx.x;
+    int nh;
+    const int c = (g < p.n_groups) ? group_tiles<G>(p, g, &nh) : 0;
+    total += block_sum_192(c, red);
+  }
+  const int64_t begin = static_cast<int64_t>(blockIdx.x) * total / gridDim.x;
+  const int64_t end = static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x;
+  if (begin >= end) return;  // block-uniform
+  {
+    int run = 0;
+    for (int g0 = 0; g0 < p.n_groups; g0 += kTcThreads) {
+      const int g = g0 + threadIdx.x;
+      int nh;
+      const int c = (g < p.n_groups) ? group_tiles<G>(p, g, &nh) : 0;
+      // inclusive scan within the block (6 warps)
+      int v = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+      }
+      __syncthreads();
+      if (lane == 31) red[warp] = v;
+      __syncthreads();
+      int before = 0, chunk = 0;
+      for (int w = 0; w < kTcThreads / 32; ++w) {
+        if (w < warp) before += red[w];
+        chunk += red[w];
+      }
+      const int excl = run + before + v - c;
+      if (c > 0 && begin >= excl && begin < excl + c) {
+        sched[0] = g;
+        sched[1] = static_cast<int>(begin - excl);
+      }
+      run += chunk;
+    }
+  }
+
+  // ---- barriers and TMEM -------------------------------------------------
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kTcStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], kTcEpiThreads);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&qmap);
+  }
+  if (warp == 1) {
+    tmem_alloc(misc, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  const int g_start = sched[0], kt_start = sched[1];
+  const int64_t ntiles = end - begin;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      TileWalker<G> w;
+      w.init(p, g_start, kt_start);
+      int cur_g = -1, qcount = 0;
+      for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+        if (w.g != cur_g) {
+          const int qb = qcount & 1;
+          if (qcount >= 2 &&
+              !mbar_wait(&qempty[qb], ((qcount >> 1) - 1) & 1, &g_status_indexer, abort_flag))
+            break;
+          mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+          tma_load_2d(sm + C::kOffQ + qb * C::kQBytes, &qmap, &qfull[qb], 0,
+                      w.g * G * kTcHeads);
+          cur_g = w.g;
+          ++qcount;
+        }
+        const int st = static_cast<int>(it % kTcStages);
+        if (it >= kTcStages &&
+            !mbar_wait(&empty[st], ((it / kTcStages) - 1) & 1, &g_status_indexer, abort_flag))
+          break;
+        const int b = __ldg(p.seq.q_seq + w.g * G);
+        const bool b_ok = (b >= 0 && b < p.seq.B);
+        const int npg = (w.nhist + kTcPage - 1) / kTcPage;
+        const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b_ok ? b : 0) * p.seq.bt_stride;
+        int32_t pid[2];
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int lp = 2 * w.kt + h;
+          pid[h] = (b_ok && lp < npg) ? __ldg(bt + lp) : -1;
+          if (lp < npg && (pid[h] < 0 || pid[h] >= p.seq.n_pages || !b_ok)) {
+            atomicOr(&g_status_indexer, kDevBadIndex);
+            pid[h] = -1;
+          }
+          if (pid[h] >= 0) bytes += C::kStageBytes / 2;
+        }
+        mbar_arrive_expect_tx(&full[st], bytes);
+        uint8_t* dst = sm + C::kOffStages + st * C::kStageBytes;
+        if (pid[0] >= 0) tma_load_2d(dst, &kmap, &full[st], 0, pid[0] * kTcPage);
+        if (pid[1] >= 0) tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid[1] * kTcPage);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      TileWalker<G> w;
+      w.init(p, g_start, kt_start);
+      int cur_g = -1, qcount = 0, qb = 0;
+      for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+        if (w.g != cur_g) {
+          if (qcount > 0) umma_commit(&qempty[qb]);  // previous group's MMAs release its Q
+          qb = qcount & 1;
+          if (!mbar_wait(&qfull[qb], (qcount >> 1) & 1, &g_status_indexer, abort_flag)) break;
+          cur_g = w.g;
+          ++qcount;
+        }
+        const int st = static_cast<int>(it % kTcStages);
+        if (!mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag)) break;
+        const int ab = static_cast<int>(it & 1);
+        if (it >= 2 &&
+            !mbar_wait(&accempty[ab], ((it >> 1) - 1) & 1, &g_status_indexer, abort_flag))
+          break;
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(sm + C::kOffStages + st * C::kStageBytes);
+        const uint32_t b_base = smem_u32(sm + C::kOffQ + qb * C::kQBytes);
+#pragma unroll
+        for (int k = 0; k < kTcDim / 32; ++k) {
+          umma_f8(tmem + ab * C::N, make_sdesc(a_base + 32 * k, 16, 1024, kLayoutSw128),
+                  make_sdesc(b_base + 32 * k, 16, 1024, kLayoutSw128), C::kIdesc, k > 0 ? 1u : 0u);
+        }
+        umma_commit(&empty[st]);
+        umma_commit(&accfull[ab]);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;
+    const int row = quarter * 32 + lane;          // key within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int etid = threadIdx.x - 64;
+    TileWalker<G> w;
+    w.init(p, g_start, kt_start);
+    int cur_g = -1, gcount = 0;
+    int tq[G], qp[G];
+    int b = 0;
+    // After a failed wait a warp stops computing but keeps walking the tile list,
+    // so that every epilogue warp reaches the same named barriers.
+    bool dead = false;
+    for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+      if (w.g != cur_g) {
+        const int wb = gcount & 1;
+        b = __ldg(p.seq.q_seq + w.g * G);
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          tq[j] = w.g * G + j;
+          qp[j] = -1;
+          if (tq[j] < p.seq.T) {
+            qp[j] = __ldg(p.seq.q_pos + tq[j]);
+            if (qp[j] >= p.seq.max_ctx) qp[j] = -1;
+            if (__ldg(p.seq.q_seq + tq[j]) != b) {
+              if (etid == 0) atomicOr(&g_status_indexer, kDevBadGroup);
+            }
+          }
+        }
+        if (b < 0 || b >= p.seq.B) {
+          if (etid == 0) atomicOr(&g_status_indexer, kDevBadIndex);
+#pragma unroll
+          for (int j = 0; j < G; ++j) qp[j] = -1;
+          b = 0;
+        }
+        for (int i = etid; i < C::N; i += kTcEpiThreads) {
+          const int j = i / kTcHeads, h = i % kTcHeads;
+          float v = 0.f;
+          if (tq[j] < p.seq.T) {
+            const int64_t o = static_cast<int64_t>(tq[j]) * kTcHeads + h;
+            v = __ldg(p.a.w + o) * (p.a.q_scale ? __ldg(p.a.q_scale + o) : 1.f);
+          }
+          wq_s[wb * C::N + i] = v;
+        }
+        named_bar_sync(1, kTcEpiThreads);
+        cur_g = w.g;
+        ++gcount;
+      }
+      if (dead) continue;
+      const float* wq = wq_s + ((gcount - 1) & 1) * C::N;
+      const int ab = static_cast<int>(it & 1);
+      const bool ok = mbar_wait(&accfull[ab], (it >> 1) & 1, &g_status_indexer, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        dead = true;
+        continue;
+      }
+      tc_fence_after();
+      const int s = w.kt * kTcKeys + row;
+      float sk = 0.f;
+      bool key_ok = false;
+      if (s < w.nhist) {
+        const int64_t r = phys_row(p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride,
+                                   s, kTcPage, p.seq.n_pages, &g_status_indexer);
+        if (r >= 0) {
+          key_ok = true;
+          sk = p.a.k_scale ? __ldg(p.a.k_scale + r) : 1.f;
+        }
+      }
+#pragma unroll 1
+      for (int j = 0; j < G; ++j) {
+        uint32_t v0[32], v1[32];
+        const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
+        tmem_ld32(col, v0);
+        tmem_ld32(col + 32, v1);
+        tmem_ld_wait();
+        float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          acc0 = fmaf(wq[j * kTcHeads + i], fmaxf(__uint_as_float(v0[i]), 0.f), acc0);
+          acc1 = fmaf(wq[j * kTcHeads + i + 1], fmaxf(__uint_as_float(v0[i + 1]), 0.f), acc1);
+        }
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          acc0 = fmaf(wq[j * kTcHeads + 32 + i], fmaxf(__uint_as_float(v1[i]), 0.f), acc0);
+          acc1 = fmaf(wq[j * kTcHeads + 33 + i], fmaxf(__uint_as_float(v1[i + 1]), 0.f), acc1);
+        }
+        if (key_ok && s <= qp[j]) p.a.scores[static_cast<int64_t>(tq[j]) * p.a.ld + s] = (acc0 + acc1) * sk;
+      }
+      tc_fence_before();
+      mbar_arrive(&accempty[ab]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+template <int G>
+cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
+                      std::string* plan, bool* unsupported, std::string* why) {
+  using C = TcCfg<G>;
+  alignas(64) CUtensorMap kmap, qmap;
+  if (!encode_tmap_2d_u8(&kmap, a.k, kTcDim, static_cast<uint64_t>(seq.cache_rows), kTcDim,
+                         kTcDim, kTcPage, why) ||
+      !encode_tmap_2d_u8(&qmap, a.q, kTcDim, static_cast<uint64_t>(seq.T) * kTcHeads, kTcDim,
+                         kTcDim, C::N, why)) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  TcParams p{seq, a, (seq.T + G - 1) / G};
+  const int64_t tiles_ub =
+      static_cast<int64_t>(p.n_groups) * ((seq.max_ctx + kTcKeys - 1) / kTcKeys);
+  const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles_ub, env.num_sms)));
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(indexer_tc_kernel<G>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  indexer_tc_kernel<G><<<grid, kTcThreads, C::kSmemBytes, env.stream>>>(kmap, qmap, p);
+  char buf[160];
+  snprintf(buf, sizeof(buf), "indexer_tc<G=%d>[grid=%d,tiles<=%lld]", G, grid,
+           static_cast<long long>(tiles_ub));
+  *plan += buf;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
+                           std::string* plan, bool* unsupported, std::string* why) {
+  *unsupported = false;
+  if (seq.T == 0) {
+    *plan += "indexer[empty]";
+    return cudaSuccess;
+  }
+  const bool tc_ok = a.e4m3 && a.H_I == kTcHeads && a.D_I == kTcDim && seq.page_size == kTcPage &&
+                     (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(a.q) % 16 == 0);
+  if (tc_ok) {
+    const int qps = seq.q_per_seq;
+    if (qps > 0 && qps % 4 == 0) return launch_tc<4>(seq, a, env, plan, unsupported, why);
+    if (qps > 0 && qps % 2 == 0) return launch_tc<2>(seq, a, env, plan, unsupported, why);
+    return launch_tc<1>(seq, a, env, plan, unsupported, why);
+  }
+  const size_t smem = (static_cast<size_t>(a.H_I) * a.D_I + a.H_I) * sizeof(float);
+  if (smem > 200 * 1024) {
+    *unsupported = true;
+    *why = "indexer: H_I * D_I too large for the generic kernel";
+    return cudaSuccess;
+  }
+  dim3 grid((seq.max_ctx + kGenThreads - 1) / kGenThreads, seq.T);
+  if (a.e4m3) {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(indexer_generic_kernel<true>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    indexer_generic_kernel<true><<<grid, kGenThreads, smem, env.stream>>>(seq, a);
+  } else {
+    if (smem > 48 * 1024)
+      cudaFuncSetAttribute(indexer_generic_kernel<false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    indexer_generic_kernel<false><<<grid, kGenThreads, smem, env.stream>>>(seq, a);
+  }
+  *plan += a.e4m3 ? "indexer_generic<e4m3>" : "indexer_generic<f32>";
+  return cudaGetLastError();
+}
+
+}  // namespace dsa

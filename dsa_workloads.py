@@ -105,7 +105,12 @@ class Spec:
     ctx_range: Optional[tuple] = None   # (lo, hi) inclusive integer-uniform draw
     B: int = 1
     low_rank: int = 0            # rank of the structured component (0 = none)
-    low_rank_amp: float = 2.0
+    # per-element std of the structured component (the N(0,1) part has std 1):
+    # large enough that it shapes the indexer scores (structured : noise ~ 1 : 1
+    # in a 128-d dot product) and the attention logits (~2 : 1 over 576 dims),
+    # small enough that the inputs stay close to N(0, 1) and the bf16 outputs stay
+    # in the range where a bf16 result can meet the stated 2e-2 max-abs tolerance
+    low_rank_amp: float = 0.5
 
 
 def spec(name: str, **over) -> Spec:
@@ -259,3 +264,38 @@ def make(name_or_spec, seed: int = 0, **over) -> Workload:
 
 
 NAMES = ("tiny_fp32", "decode_b1", "decode_b64", "prefill_16k", "decode_b4_long")
+
+
+def device_tensors(wl: Workload, device, copies: int = 1) -> dict:
+    """Copies a workload's arrays to ``device`` as torch tensors, grouped under the
+    field names of the binding's Seq / Indexer / Mla records (plus ``K``).
+    ``copies > 1`` returns a list of independent copies of the cache-side and
+    query-side tensors (used to rotate inputs past the L2 cache)."""
+    def t(a, dtype=None):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        if dtype is not None:
+            x = x.view(dtype)
+        return x.to(device)
+
+    def one():
+        seq = dict(q_seq=t(wl.q_seq), q_pos=t(wl.q_pos), block_table=t(wl.block_table),
+                   max_ctx=wl.max_ctx, cache_rows=wl.cache_rows, page_size=wl.page_size,
+                   q_per_seq=wl.q_per_seq)
+        idx = dict(q=t(wl.q_i), w=t(wl.w), k_cache=t(wl.k_i), q_scale=t(wl.q_i_scale),
+                   k_scale=t(wl.k_i_scale))
+        if wl.mla_dtype == "bf16":
+            q, kv = t(wl.q.view(np.int16), torch.bfloat16), t(wl.kv.view(np.int16), torch.bfloat16)
+            dt = None
+        elif wl.mla_dtype == "e4m3":
+            q, kv = t(wl.q.view(np.int16), torch.bfloat16), t(wl.kv)
+            dt = 2  # FP8 row format
+        else:
+            q, kv = t(wl.q), t(wl.kv)
+            dt = None
+        mla = dict(q=q, kv_cache=kv, d_latent=wl.d_latent, d_rope=wl.d_rope,
+                   softmax_scale=wl.softmax_scale, dtype=dt)
+        return dict(seq=seq, indexer=idx, mla=mla, K=wl.K)
+
+    if copies == 1:
+        return one()
+    return [one() for _ in range(copies)]

@@ -1,0 +1,182 @@
+/*
+ * dsa.h -- C ABI of libdsa, the GB300 (sm_103a) DSA sparse-attention hot path:
+ * lightning-indexer scores -> per-query Top-K -> sparse MLA attention over the
+ * selected latent-cache rows.
+ *
+ * Sources of each operation (page title, section):
+ *  - "Day0 Inference Adaptation and Performance Optimization for Kimi K3.1 Pro",
+ *    section 3: the indexer computes relevance scores between queries and
+ *    historical positions, applies head-weight weighting and selects the Top-K
+ *    positions, reading a paged cache; sparse flash attention then reads the KV
+ *    rows of the selected positions.
+ *  - "Large Language Model Inference Acceleration in Practice", section 1.2
+ *    (DSA = MLA + LI + SFA; complexity O(N*K)) and section 3.1 (fused LI + SFA:
+ *    indices feed SFA without a global round trip; rows read from the paged KV
+ *    cache).
+ *  - The score formula I[t,s] = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]) with FP8
+ *    keys and per-token scales, ties to the lower index, and the MQA form of the
+ *    latent attention (576-d keys = 512 latent + 64 rope, 512-d values) follow
+ *    the method's statement of the DSA path.
+ *
+ * Conventions for every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library
+ *    never allocates or frees device memory; calls that need scratch take a
+ *    caller-provided workspace (256-byte aligned) and report its size through
+ *    the matching *_workspace_size() query.
+ *  - Every call validates its arguments on the host, then enqueues its kernels
+ *    on `stream` (a cudaStream_t; NULL = legacy default stream) and returns
+ *    without synchronising.  Nothing is launched when validation fails.
+ *  - Errors found on the device (out-of-range page ids or indices, q_pos beyond
+ *    max_ctx, a wrong q_per_seq hint, a pipeline wait that timed out) never trap:
+ *    the offending element is skipped and a sticky device status word is set;
+ *    dsa_check_status() reads and clears it.
+ *  - Calls are thread-safe; dsa_last_error()/dsa_last_plan() are per thread.
+ *  - Base pointers must be 16-byte aligned.  Row-major, densely packed layouts
+ *    unless a stride is given.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad shape or stride      */
+  DSA_ERR_UNSUPPORTED = 2,   /* no kernel for this dtype/dimension/K combination  */
+  DSA_ERR_WORKSPACE = 3,     /* workspace missing or too small                    */
+  DSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed              */
+  DSA_ERR_TIMEOUT = 5,       /* dsa_check_status: a device-side wait gave up      */
+  DSA_ERR_DEVICE_CHECK = 6   /* dsa_check_status: a device-side bounds check hit  */
+} dsa_status_t;
+
+typedef enum dsa_dtype {
+  DSA_F32 = 0,
+  DSA_BF16 = 1,
+  DSA_E4M3 = 2               /* OCP FP8 E4M3 codes (bias 7, max 448, no inf)      */
+} dsa_dtype_t;
+
+typedef void* dsa_stream_t;  /* cudaStream_t */
+
+/* Queries, sequences and the paged cache they read.
+ * Query t belongs to sequence q_seq[t] and sits at position q_pos[t]; its causal
+ * history is the positions s in [0, q_pos[t]] (its own key already cached).
+ * Logical position s of sequence b lives in cache row
+ *     block_table[b * bt_stride + s / page_size] * page_size + s % page_size.
+ * The indexer-key pool and the latent pool share this page table. */
+typedef struct dsa_seq_desc {
+  int32_t B;                 /* sequences                                          */
+  int32_t T;                 /* query tokens (T >= 0)                              */
+  int32_t max_ctx;           /* host bound: q_pos[t] + 1 <= max_ctx for every t;   */
+                             /* sizes grids and score rows                          */
+  int32_t q_per_seq;         /* > 0: sequence b owns queries [b*q_per_seq,          */
+                             /* (b+1)*q_per_seq) (T == B*q_per_seq); 0: no layout   */
+                             /* promise (each query handled on its own)             */
+  const int32_t* q_seq;      /* device int32 [T]                                   */
+  const int32_t* q_pos;      /* device int32 [T]                                   */
+  const int32_t* block_table;/* device int32 [B, bt_stride] physical page ids      */
+  int32_t bt_stride;         /* >= ceil(max_ctx / page_size)                       */
+  int32_t page_size;         /* tokens per page (64 on the tensor-core paths)      */
+  int64_t cache_rows;        /* rows in each pool; page ids must be < cache_rows / */
+                             /* page_size                                          */
+} dsa_seq_desc_t;
+
+/* Lightning indexer inputs (dequantised value = code * scale). */
+typedef struct dsa_indexer_desc {
+  int32_t H_I;               /* indexer heads                                      */
+  int32_t D_I;               /* indexer head dim                                   */
+  dsa_dtype_t dtype;         /* DSA_E4M3 or DSA_F32, for both q and k_cache        */
+  const void* q;             /* device [T, H_I, D_I]                               */
+  const float* q_scale;      /* device fp32 [T, H_I], or NULL for all-ones         */
+  const float* w;            /* device fp32 [T, H_I] head weights                  */
+  const void* k_cache;       /* device [cache_rows, D_I]                           */
+  const float* k_scale;      /* device fp32 [cache_rows] per-token, or NULL        */
+} dsa_indexer_desc_t;
+
+/* MLA latent attention inputs (MQA form: one latent row per position, shared by
+ * all H heads; keys are the first d_latent + d_rope values of a row, values the
+ * first d_latent). */
+typedef struct dsa_mla_desc {
+  int32_t H;                 /* attention heads                                    */
+  int32_t d_latent;          /* value dim (512 on the tensor-core path)            */
+  int32_t d_rope;            /* extra key dims (64 on the tensor-core path)        */
+  dsa_dtype_t dtype;         /* cache format:                                      */
+                             /*  DSA_BF16: row = d_latent+d_rope bf16 values       */
+                             /*  DSA_E4M3: 656-byte row (d_latent 512, d_rope 64): */
+                             /*   [0,512) e4m3 latent codes, [512,516) fp32 scale, */
+                             /*   [516,528) reserved, [528,656) 64 bf16 rope       */
+                             /*  DSA_F32 : row = d_latent+d_rope fp32 values       */
+  const void* q;             /* device [T, H, d_latent+d_rope]: bf16, or fp32 when */
+                             /* dtype == DSA_F32                                   */
+  const void* kv_cache;      /* device [cache_rows, row_bytes]                     */
+  int64_t row_bytes;         /* bytes per cache row (multiple of 16)               */
+  float softmax_scale;       /* logit = softmax_scale * q . key                    */
+} dsa_mla_desc_t;
+
+int dsa_abi_version(void);
+const char* dsa_status_string(dsa_status_t status);
+/* Detail of the last failure on the calling thread ("" if none). */
+const char* dsa_last_error(void);
+/* Kernels chosen by the last successful compute call on the calling thread. */
+const char* dsa_last_plan(void);
+
+/* Step 1 -- lightning-indexer scores.
+ * scores[t * ld + s] = sum_h w[t,h] * ReLU(q_I[t,h] . k_I[s]) for s <= q_pos[t],
+ * accumulated in fp32 from the dequantised FP8 (or fp32) values.  Entries with
+ * s > q_pos[t] are not written.  scores: device fp32 [T, ld], ld >= max_ctx,
+ * ld % 4 == 0. */
+dsa_status_t dsa_indexer_scores(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
+                                 float* scores, int64_t ld, dsa_stream_t stream);
+
+/* Step 2 -- per-query Top-K.
+ * idx[t * K + j]: the min(K, q_pos[t]+1) positions s <= q_pos[t] with the largest
+ * scores[t * ld + s] (compared as fp32 values, -0 == +0), ties to the lower s,
+ * written in ascending position order, then -1 padding up to K.
+ * K >= 1; scores: device fp32 [T, ld], ld >= max_ctx, ld % 4 == 0;
+ * idx: device int32 [T, K]. */
+dsa_status_t dsa_topk(const dsa_seq_desc_t* seq, const float* scores, int64_t ld, int32_t K,
+                      int32_t* idx, dsa_stream_t stream);
+
+/* Step 3 -- sparse MLA attention over the selected rows.
+ * For query t and head h, over S = { idx[t*K + j] : idx >= 0 }:
+ *   logit_s = softmax_scale * q[t,h,:] . row_s[0 : d_latent+d_rope]
+ *   out[t,h,:] = sum_s softmax(logit)_s * row_s[0 : d_latent]
+ *   lse[t,h]   = log sum_s exp(logit_s)      (natural log; -inf if S is empty)
+ * Entries -1 are skipped wherever they appear; an entry > q_pos[t] is skipped and
+ * flagged.  1 <= K <= 16384.  out: device [T, H, d_latent], bf16 (fp32 when dtype == DSA_F32);
+ * lse: device fp32 [T, H] or NULL.  workspace may be NULL when
+ * dsa_sparse_mla_attn_workspace_size() returns 0; a larger workspace lets the
+ * call split each query's rows across more CTAs. */
+size_t dsa_sparse_mla_attn_workspace_size(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla,
+                                          int32_t K);
+dsa_status_t dsa_sparse_mla_attn(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla,
+                                 const int32_t* idx, int32_t K, void* out, float* lse,
+                                 void* workspace, size_t workspace_bytes, dsa_stream_t stream);
+
+/* Steps 1-3 chained for one decode (or prefill) step: scores stay in the
+ * workspace (L2-resident at decode sizes) and feed Top-K, whose indices feed
+ * the attention directly.  idx_out (device int32 [T, K]) receives the selected
+ * positions when non-NULL.  workspace: >= dsa_decode_workspace_size() bytes. */
+size_t dsa_decode_workspace_size(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
+                                 const dsa_mla_desc_t* mla, int32_t K);
+dsa_status_t dsa_decode_step(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
+                             const dsa_mla_desc_t* mla, int32_t K, void* out, float* lse,
+                             int32_t* idx_out, void* workspace, size_t workspace_bytes,
+                             dsa_stream_t stream);
+
+/* Synchronises `stream`, then returns and clears the device status word:
+ * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK (dsa_last_error() names the
+ * flags), or DSA_ERR_CUDA if the stream itself reports an error. */
+dsa_status_t dsa_check_status(dsa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -12,6 +12,12 @@ def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
 
 
+def pytest_sessionstart(session):
+    # the binding loads libdsa.so at import time; (re)build it once per session
+    import __graft_entry__
+    __graft_entry__._build_module().build()
+
+
 @pytest.fixture(scope="session")
 def dev():
     import torch

@@ -1,0 +1,79 @@
+"""The C-ABI library loads and exports every symbol include/dsa.h declares; host
+validation rejects bad arguments before anything reaches the GPU (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dsa_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def dsa():
+    import __graft_entry__
+    __graft_entry__.build()
+    import dsa_indexed_sparse_gb300 as m
+    return m
+
+
+def test_every_declared_function_is_exported(dsa):
+    names = header_functions()
+    assert len(names) >= 11
+    lib = ctypes.CDLL(dsa.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(dsa.EXPORTED) == names
+
+
+def test_version_and_status_strings(dsa):
+    assert dsa.abi_version() == 1
+    for code, name in dsa.STATUS_NAMES.items():
+        assert dsa._lib.dsa_status_string(code).decode() == name
+
+
+def test_host_validation_rejects_bad_arguments(dsa):
+    lib = dsa._lib
+    # NULL descriptors
+    assert lib.dsa_indexer_scores(None, None, None, 0, None) == 1
+    assert lib.dsa_topk(None, None, 0, 1, None, None) == 1
+    assert "NULL" in dsa.last_error()
+    # T = B * q_per_seq violated
+    s = dsa.SeqDesc(B=2, T=3, max_ctx=128, q_per_seq=1, q_seq=16, q_pos=16, block_table=16,
+                    bt_stride=2, page_size=64, cache_rows=256)
+    assert lib.dsa_topk(ctypes.byref(s), 16, 128, 8, 16, None) == 1
+    assert "q_per_seq" in dsa.last_error()
+    # page table too narrow for max_ctx
+    s = dsa.SeqDesc(B=1, T=1, max_ctx=1000, q_per_seq=1, q_seq=16, q_pos=16, block_table=16,
+                    bt_stride=2, page_size=64, cache_rows=4096)
+    assert lib.dsa_topk(ctypes.byref(s), 16, 1024, 8, 16, None) == 1
+    assert "bt_stride" in dsa.last_error()
+    # K = 0
+    s.bt_stride = 16
+    assert lib.dsa_topk(ctypes.byref(s), 16, 1024, 0, 16, None) == 1
+    # FP8 latent rows only for 512 + 64 dims
+    m = dsa.MlaDesc(H=4, d_latent=64, d_rope=16, dtype=dsa.DSA_E4M3, q=16, kv_cache=16, row_bytes=656,
+                    softmax_scale=0.1)
+    assert lib.dsa_sparse_mla_attn_workspace_size(ctypes.byref(s), ctypes.byref(m), 32) == 0
+    assert lib.dsa_sparse_mla_attn(ctypes.byref(s), ctypes.byref(m), 16, 32, 16, None, None, 0, None) == 2
+    # misaligned score buffer for the indexer
+    x = dsa.IndexerDesc(H_I=4, D_I=32, dtype=dsa.DSA_F32, q=16, q_scale=None, w=16, k_cache=16, k_scale=None)
+    assert lib.dsa_indexer_scores(ctypes.byref(s), ctypes.byref(x), 20, 1024, None) == 1
+    # decode step without a workspace
+    assert lib.dsa_decode_step(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), 32, 16, None, None,
+                               None, 0, None) == 3
+
+
+def test_product_package_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "dsa_indexed_sparse_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f
