@@ -9,7 +9,7 @@
 #include <mutex>
 #include <string>
 
-#include "../../include/dsa.h"
+#include "dsa.h"
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
 

@@ -20,15 +20,15 @@
 //    selected rows.  The CTA pair covering both value halves computes the same
 //    logits: O[128 x 512] fp32 would fill all of TMEM, so each CTA keeps a
 //    [128 x 256] accumulator plus double-buffered logits.
-//      warps 0-3: gather 32 selected rows per tile with 16-byte cp.async through
-//                 the page table into a 128-byte-swizzled K-major tile (two
-//                 producer groups own one ring stage each);
-//      warp 8   : issues S = Q K^T (M=128 heads, N=32 rows, K=576) and
-//                 O += P V (M=128, N=256, K=32) with tcgen05.mma, accumulators in TMEM;
+//      warps 0-3: gather 32 selected rows per tile (lane = row: index -> page ->
+//                 cache row) with 16-byte cp.async into a 128-byte-swizzled
+//                 K-major tile; 4 tiles in flight (3 for FP8 rows);
+//      warp 8   : issues S = Q K^T (M=128 heads, N=32 rows, K=576; the first 256
+//                 query dims are read from TMEM, the rest from shared memory) and
+//                 O += P V (M=128, N=256, K=32; P read from TMEM) with tcgen05.mma;
 //      warps 4-7: online softmax, one thread per head (its TMEM lane), P written
-//                 as bf16 to shared memory, the denominator summed from the fp32
-//                 weights; the running max is only moved (and O rescaled in
-//                 TMEM) when it grows by more than 2^8.
+//                 as bf16 into TMEM; the running max is only moved (and O
+//                 rescaled in TMEM) when it grows by more than 2^8.
 //  * attn_combine_kernel -- merges per-slice partial results by their LSE.
 //  * attn_generic_kernel -- CUDA cores, any head count / dims / row format.
 #include <algorithm>
@@ -160,28 +160,42 @@ constexpr int kDqk = 576;
 constexpr int kDv = 512;
 constexpr int kDvHalf = 256;     // value dims per CTA = UMMA N of P V
 constexpr int kBR = 32;          // rows per tile = UMMA N of Q K^T
-constexpr int kQBytes = kH * kDqk * 2;             // 147456
 constexpr int kTileBytes = kBR * kDqk * 2;         // 36864
-constexpr int kPBytes = kH * kBR * 2;              // 8192
-constexpr int kOffQ = 0;
-constexpr int kOffKV = kOffQ + kQBytes;
-constexpr int kOffP = kOffKV + 2 * kTileBytes;
-constexpr int kOffMask = kOffP + kPBytes;          // uint16 [2 stages][2 warps]
-constexpr int kOffScale = kOffMask + 16;           // float [2 stages][32] FP8 row scales
-constexpr int kOffBar = kOffScale + 2 * kBR * 4;
-// barriers: full[2], empty[2], sfull[2], pfull, pvdone, ofull
-constexpr int kNumBars = 9;
-constexpr int kOffMisc = kOffBar + kNumBars * 8;   // tmem base, abort
-constexpr int kSmemBytes = kOffMisc + 16 + 1024;   // + alignment slack
 constexpr int kThreads = 288;                      // 4 producer, 4 softmax, 1 MMA warp
+constexpr int kProducerWarps = 4;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS = 0;                      // S buffers: [0,32), [32,64)
-constexpr uint32_t kColSr = 64;                    // FP8 rows: rope part of S, [64,96), [96,128)
-constexpr uint32_t kColO = 256;                    // O: [256, 512)
 constexpr uint32_t kIdescS = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR);
 constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, kFmtBF16, false, true, kH, kDvHalf);
 constexpr float kRescaleThreshold = 8.0f;          // log2 units
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// Shared memory and TMEM plan.  The first kQTmemDims query dims live in TMEM
+// (A operand of Q K^T read from tensor memory), the rest in shared memory, and P
+// lives in TMEM too, which leaves room for kStages gathered tiles.
+//   TMEM columns: S [0,64) (two buffers), FP8 rope logits [64,128), P (16),
+//   Q (kQTmemDims / 2), O [256, 512).
+template <bool kFp8>
+struct AttnCfg {
+  static constexpr int kQTmemDims = kFp8 ? 192 : 256;
+  static constexpr int kQTmemSteps = kQTmemDims / 16;
+  static constexpr int kQSmemAtoms = (kDqk - kQTmemDims) / 64;
+  static constexpr int kStages = kFp8 ? 3 : 4;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kQSmemAtoms * kH * 128;
+  static constexpr int kOffMask = kOffKV + kStages * kTileBytes;   // uint32 [stages]
+  static constexpr int kOffScale = kOffMask + 16;                  // float [stages][32]
+  static constexpr int kOffBar = kOffScale + kStages * kBR * 4;
+  // barriers: full[S], empty[S], sfull[2], pfull, pvdone, ofull
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;          // tmem base, abort
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + alignment slack
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColSr = 64;
+  static constexpr uint32_t kColP = kFp8 ? 128 : 64;
+  static constexpr uint32_t kColQ = kFp8 ? 160 : 128;
+  static constexpr uint32_t kColO = 256;
+  static_assert(kColQ + kQTmemDims / 2 <= kColO, "TMEM plan");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
 
 struct TcAttnParams {
   SeqArgs seq;
@@ -192,28 +206,30 @@ struct TcAttnParams {
   float* ws_lse;         // [n_split, T, H]
 };
 
-// Byte offset of 16-byte chunk `ch` (of 72) of tile row `r` in a 128B-swizzled
-// K-major tile of `rows` rows: atom (64 values) major, then row, then swizzled chunk.
+// Byte offset of 16-byte chunk `ch` of tile row `r` in a 128B-swizzled K-major
+// tile of `rows` rows: atom (64 values) major, then row, then swizzled chunk.
 __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
   return static_cast<uint32_t>((ch >> 3) * rows * 128 + r * 128 + (((ch & 7) ^ (r & 7)) << 4));
 }
 
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
+  using C = AttnCfg<kFp8>;
+  constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kOffBar);
-  uint64_t* full = bars;         // [2] producer group g -> stage g
-  uint64_t* empty = bars + 2;    // [2]
-  uint64_t* sfull = bars + 4;    // [2]
-  uint64_t* pfull = bars + 6;
-  uint64_t* pvdone = bars + 7;
-  uint64_t* ofull = bars + 8;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kOffMisc);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
+  uint64_t* full = bars;          // [S] tile landed (32 producer lanes)
+  uint64_t* empty = bars + S;     // [S] tile consumed by P V (MMA commit)
+  uint64_t* sfull = bars + 2 * S; // [2] logits ready
+  uint64_t* pfull = bars + 2 * S + 2;
+  uint64_t* pvdone = bars + 2 * S + 3;
+  uint64_t* ofull = bars + 2 * S + 4;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + kOffMask);
-  volatile float* row_scale = reinterpret_cast<volatile float*>(sm + kOffScale);
+  volatile uint32_t* mask_s = reinterpret_cast<volatile uint32_t*>(sm + C::kOffMask);
+  volatile float* row_scale = reinterpret_cast<volatile float*>(sm + C::kOffScale);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x & 1;                     // value half
@@ -232,14 +248,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
     qp = -1;  // every row masked
     b = 0;
   }
+  const uint16_t* qg = static_cast<const uint16_t*>(p.a.q) + static_cast<int64_t>(t) * kH * kDqk;
 
-  // ---- setup: barriers, TMEM, Q tile --------------------------------------
+  // ---- setup: barriers, TMEM, Q (shared-memory part via cp.async) -----------
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&full[i], 64);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&full[i], 32);
       mbar_init(&empty[i], 1);
-      mbar_init(&sfull[i], 1);
     }
+    for (int i = 0; i < 2; ++i) mbar_init(&sfull[i], 1);
     mbar_init(pfull, 128);
     mbar_init(pvdone, 1);
     mbar_init(ofull, 1);
@@ -251,165 +268,204 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
     tmem_relinquish();
   }
   {
-    const uint16_t* qg = static_cast<const uint16_t*>(p.a.q) + static_cast<int64_t>(t) * kH * kDqk;
-    const uint32_t qbase = smem_u32(sm + kOffQ);
-    for (int i = threadIdx.x; i < kH * (kDqk / 8); i += kThreads) {
-      const int h = i / (kDqk / 8), ch = i % (kDqk / 8);
-      cp_async16(qbase + sw128_offset(h, ch, kH), qg + h * kDqk + ch * 8);
+    const uint32_t qbase = smem_u32(sm + C::kOffQ);
+    constexpr int kChunks = (kDqk - C::kQTmemDims) / 8;  // 16-byte chunks per row in smem
+    for (int i = threadIdx.x; i < kH * kChunks; i += kThreads) {
+      const int h = i / kChunks, ch = i % kChunks;
+      cp_async16(qbase + sw128_offset(h, ch, kH), qg + h * kDqk + C::kQTmemDims + ch * 8);
     }
     cp_async_commit();
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  if (warp >= 4 && warp < 8) {
+    // Q dims [0, kQTmemDims) of head h -> TMEM lane h (two bf16 per column)
+    const int h = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
+#pragma unroll 1
+    for (int blk = 0; blk < C::kQTmemDims / 64; ++blk) {
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(qrow + blk * 8 + i);
+        r[4 * i] = v.x;
+        r[4 * i + 1] = v.y;
+        r[4 * i + 2] = v.z;
+        r[4 * i + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_off + C::kColQ + blk * 32, r);
+    }
+    tmem_st_wait();
+  }
+  cp_async_wait<0>();
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
 
-  if (warp < 4) {
-    // ------------------------------------------------ producers (2 groups)
-    const int pg = warp >> 1, wi = warp & 1;
+  if (warp < kProducerWarps) {
+    // ------------------------------------------------ producers: warp w owns tiles j = w mod 4
     const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);
     const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride;
     const int32_t* idx = p.a.idx + static_cast<int64_t>(t) * K;
-    const uint32_t stage = smem_u32(sm + kOffKV + pg * kTileBytes);
-    for (int j = pg; j < ntiles; j += 2) {
-      // Resolve the warp's 16 rows in parallel (lane r: index -> page -> cache row)
-      // before waiting for the stage, so the dependent loads overlap the wait.
+    for (int j = warp; j < ntiles; j += kProducerWarps) {
+      const int st = j % S;
+      // lane r resolves tile row r (index -> page -> cache row) before the wait
       int64_t my_row = -1;
       float my_scale = 0.f;
-      if (lane < 16) {
-        const int gi = r0 + j * kBR + wi * 16 + lane;  // entry of the index list
-        if (gi < r1) {
-          const int pos = __ldg(idx + gi);
-          if (pos >= 0) {
-            if (pos > qp)
-              atomicOr(&g_status_attn, kDevBadIndex);
-            else
-              my_row = phys_row(bt, pos, p.seq.page_size, p.seq.n_pages, &g_status_attn);
-          }
+      const int gi = r0 + j * kBR + lane;
+      if (gi < r1) {
+        const int pos = __ldg(idx + gi);
+        if (pos >= 0) {
+          if (pos > qp)
+            atomicOr(&g_status_attn, kDevBadIndex);
+          else
+            my_row = phys_row(bt, pos, p.seq.page_size, p.seq.n_pages, &g_status_attn);
         }
-        if (kFp8 && my_row >= 0)
-          my_scale = __ldg(reinterpret_cast<const float*>(kv + my_row * p.a.row_bytes + 512));
       }
-      if (j >= 2) {
-        const bool ok = mbar_wait(&empty[pg], ((j >> 1) - 1) & 1, &g_status_attn, abort_flag);
+      if (kFp8 && my_row >= 0)
+        my_scale = __ldg(reinterpret_cast<const float*>(kv + my_row * p.a.row_bytes + 512));
+      if (j >= S) {
+        const bool ok = mbar_wait(&empty[st], ((j / S) - 1) & 1, &g_status_attn, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
-      if (kFp8 && lane < 16) row_scale[pg * kBR + wi * 16 + lane] = my_scale;
-      const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFFFFu;
+      const uint32_t stage = smem_u32(sm + C::kOffKV + st * kTileBytes);
+      const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0);
+      if (kFp8) row_scale[st * kBR + lane] = my_scale;
+      if (lane == 0) mask_s[st] = bits;
       if (!kFp8) {
-#pragma unroll 1
-        for (int rr = 0; rr < 16; ++rr) {
-          const int rl = wi * 16 + rr;
+        // 72 16-byte chunks per row; consecutive lanes take consecutive chunks
+#pragma unroll 4
+        for (int i = lane; i < kBR * (kDqk / 8); i += 32) {
+          const int rr = i / (kDqk / 8), ch = i % (kDqk / 8);
           const int64_t prow = __shfl_sync(0xffffffffu, my_row, rr);
-          if (prow >= 0) {
-            const uint8_t* src = kv + prow * p.a.row_bytes;
-            for (int ch = lane; ch < kDqk / 8; ch += 32)
-              cp_async16(stage + sw128_offset(rl, ch, kBR), src + ch * 16);
-          } else {
-            for (int ch = lane; ch < kDqk / 8; ch += 32)
-              st_shared_v4(stage + sw128_offset(rl, ch, kBR), 0u, 0u, 0u, 0u);
-          }
+          if (prow >= 0)
+            cp_async16(stage + sw128_offset(rr, ch, kBR), kv + prow * p.a.row_bytes + ch * 16);
+          else
+            st_shared_v4(stage + sw128_offset(rr, ch, kBR), 0u, 0u, 0u, 0u);
         }
       } else {
-        // latent: 16 e4m3 codes per lane and row, all 16 rows' loads in flight
-        // before any conversion; widened to bf16 exactly (two 16-byte chunks)
-        uint4 raw[16];
+        // latent: 16 e4m3 codes per lane and row, 8 rows' loads in flight before
+        // any conversion; widened to bf16 exactly (two 16-byte chunks); rope by cp.async
+#pragma unroll 1
+        for (int r8 = 0; r8 < kBR; r8 += 8) {
+          uint4 raw[8];
 #pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          const int64_t prow = __shfl_sync(0xffffffffu, my_row, rr);
-          raw[rr] = prow >= 0 ? ld_global_nc_v4(kv + prow * p.a.row_bytes + lane * 16) : make_uint4(0, 0, 0, 0);
-          if (prow >= 0 && lane < 8)
-            cp_async16(stage + sw128_offset(wi * 16 + rr, 64 + lane, kBR), kv + prow * p.a.row_bytes + 528 + lane * 16);
-          else if (lane < 8)
-            st_shared_v4(stage + sw128_offset(wi * 16 + rr, 64 + lane, kBR), 0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int rr = 0; rr < 16; ++rr) {
-          const int rl = wi * 16 + rr;
-          const uint32_t w[4] = {raw[rr].x, raw[rr].y, raw[rr].z, raw[rr].w};
-          uint32_t o[8];
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[k] & 0xFFFFu));
-            const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w[k] >> 16));
-            o[2 * k] = pack_bf16x2(lo.x, lo.y);
-            o[2 * k + 1] = pack_bf16x2(hi.x, hi.y);
+          for (int q = 0; q < 8; ++q) {
+            const int64_t prow = __shfl_sync(0xffffffffu, my_row, r8 + q);
+            raw[q] = prow >= 0 ? ld_global_nc_v4(kv + prow * p.a.row_bytes + lane * 16) : make_uint4(0, 0, 0, 0);
+            if (lane < 8) {
+              if (prow >= 0)
+                cp_async16(stage + sw128_offset(r8 + q, 64 + lane, kBR), kv + prow * p.a.row_bytes + 528 + lane * 16);
+              else
+                st_shared_v4(stage + sw128_offset(r8 + q, 64 + lane, kBR), 0u, 0u, 0u, 0u);
+            }
           }
-          st_shared_v4(stage + sw128_offset(rl, 2 * lane, kBR), o[0], o[1], o[2], o[3]);
-          st_shared_v4(stage + sw128_offset(rl, 2 * lane + 1, kBR), o[4], o[5], o[6], o[7]);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const uint32_t w[4] = {raw[q].x, raw[q].y, raw[q].z, raw[q].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[k] & 0xFFFFu));
+              const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w[k] >> 16));
+              o[2 * k] = pack_bf16x2(lo.x, lo.y);
+              o[2 * k + 1] = pack_bf16x2(hi.x, hi.y);
+            }
+            st_shared_v4(stage + sw128_offset(r8 + q, 2 * lane, kBR), o[0], o[1], o[2], o[3]);
+            st_shared_v4(stage + sw128_offset(r8 + q, 2 * lane + 1, kBR), o[4], o[5], o[6], o[7]);
+          }
         }
       }
-      if (lane == 0) mask16[pg * 2 + wi] = static_cast<uint16_t>(bits);
       cp_async_commit();
       cp_async_wait<0>();
       fence_proxy_async_smem();
-      mbar_arrive(&full[pg]);
+      mbar_arrive(&full[st]);
     }
   } else if (warp == 8) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      const uint32_t qbase = smem_u32(sm + kOffQ);
-      const uint32_t pbase = smem_u32(sm + kOffP);
-      auto issue_pv = [&](int j) {
-        const uint32_t vbase = smem_u32(sm + kOffKV + (j & 1) * kTileBytes) + c * 4 * kBR * 128;
+    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
+    // Descriptors are built once; the unrolled issue loops only add constant byte
+    // offsets (>> 4) to the start-address field, and one elected lane issues a
+    // whole block of MMAs (this keeps the issue cost near 30-40 cycles per MMA).
+    const uint64_t dq0 = make_sdesc(smem_u32(sm + C::kOffQ), 16, 1024, kLayoutSw128);
+    const uint64_t dk0 = make_sdesc(smem_u32(sm + C::kOffKV), 16, 1024, kLayoutSw128);
+    const uint64_t dv0 = make_sdesc(smem_u32(sm + C::kOffKV) + c * 4 * kBR * 128, kBR * 128, 1024, kLayoutSw128);
+    auto issue_pv = [&](int j) {
+      const uint64_t dv = dv0 + static_cast<uint64_t>(((j % S) * kTileBytes) >> 4);
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < kBR / 16; ++kk) {
-          const uint64_t da = make_sdesc(pbase + kk * 256, 128, 512, kLayoutNone);
-          const uint64_t db = make_sdesc(vbase + kk * 16 * 128, kBR * 128, 1024, kLayoutSw128);
-          umma_f16(tmem + kColO, da, db, kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBR / 16; ++kk)
+          umma_f16_tmem_a(tmem + C::kColO, tmem + C::kColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                          kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
         umma_commit(pvdone);
-        umma_commit(&empty[j & 1]);
-      };
-      // Issue S_j as soon as tile j has landed (and its S buffer is free, i.e.
-      // P_{j-2} was consumed) and P V_j as soon as P_j is written, in whichever
-      // order they become ready, so neither kind of MMA waits on the other's inputs.
-      int next_s = 0, next_pv = 0;
-      uint32_t spins = 0;
-      uint64_t stall_t0 = 0;
-      while (next_pv < ntiles) {
-        bool progress = false;
-        if (next_s < ntiles && next_s <= next_pv + 1 &&
-            mbar_try_wait(smem_u32(&full[next_s & 1]), (next_s >> 1) & 1)) {
-          tc_fence_after();
-          const int j = next_s;
-          const uint32_t kbase = smem_u32(sm + kOffKV + (j & 1) * kTileBytes);
-#pragma unroll 4
+        umma_commit(&empty[j % S]);
+      }
+      __syncwarp();
+    };
+    // Issue S_j as soon as tile j has landed (and its S buffer is free, i.e.
+    // P_{j-2} was consumed) and P V_j as soon as P_j is written, in whichever
+    // order they become ready, so neither kind of MMA waits on the other's inputs.
+    int next_s = 0, next_pv = 0;
+    uint32_t spins = 0;
+    uint64_t stall_t0 = 0;
+    while (next_pv < ntiles) {
+      bool progress = false;
+      const bool s_ready = next_s < ntiles && next_s <= next_pv + 1 &&
+                           mbar_test_wait(smem_u32(&full[next_s % S]), (next_s / S) & 1);
+      if (__shfl_sync(0xffffffffu, s_ready, 0)) {
+        tc_fence_after();
+        const int j = next_s;
+        const uint64_t dk = dk0 + static_cast<uint64_t>(((j % S) * kTileBytes) >> 4);
+        const uint32_t col_s = tmem + C::kColS + (j & 1) * kBR;
+        const uint32_t col_r = tmem + C::kColSr + (j & 1) * kBR;
+        if (elect_one()) {
+#pragma unroll
           for (int kk = 0; kk < kDqk / 16; ++kk) {
-            const int atom = kk >> 2, sub = kk & 3;
-            const uint64_t da = make_sdesc(qbase + atom * kH * 128 + sub * 32, 16, 1024, kLayoutSw128);
-            const uint64_t db = make_sdesc(kbase + atom * kBR * 128 + sub * 32, 16, 1024, kLayoutSw128);
+            const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR * 128 + (kk & 3) * 32) >> 4);
             // FP8 rows: latent (k < 512) and rope (k >= 512) logits in separate columns
             const bool rope = kFp8 && kk >= kDv / 16;
-            const uint32_t col = (rope ? kColSr : kColS) + (j & 1) * kBR;
-            const bool first = kk == 0 || (kFp8 && kk == kDv / 16);
-            umma_f16(tmem + col, da, db, kIdescS, first ? 0u : 1u);
+            const uint32_t acc = (kk == 0 || (kFp8 && kk == kDv / 16)) ? 0u : 1u;
+            if (kk < C::kQTmemSteps) {
+              umma_f16_tmem_a(rope ? col_r : col_s, tmem + C::kColQ + kk * 8, db, kIdescS, acc);
+            } else {
+              const int qk = kk - C::kQTmemSteps;
+              const uint64_t da = dq0 + static_cast<uint64_t>(((qk >> 2) * kH * 128 + (qk & 3) * 32) >> 4);
+              umma_f16(rope ? col_r : col_s, da, db, kIdescS, acc);
+            }
           }
           umma_commit(&sfull[j & 1]);
-          ++next_s;
-          progress = true;
         }
-        if (next_pv < next_s && mbar_try_wait(smem_u32(pfull), next_pv & 1)) {
-          tc_fence_after();
-          issue_pv(next_pv);
-          if (next_pv == ntiles - 1) umma_commit(ofull);
-          ++next_pv;
-          progress = true;
+        __syncwarp();
+        ++next_s;
+        progress = true;
+      }
+      const bool p_ready = next_pv < next_s && mbar_test_wait(smem_u32(pfull), next_pv & 1);
+      if (__shfl_sync(0xffffffffu, p_ready, 0)) {
+        tc_fence_after();
+        issue_pv(next_pv);
+        if (next_pv == ntiles - 1) {
+          if (elect_one()) umma_commit(ofull);
+          __syncwarp();
         }
-        if (progress) {
-          stall_t0 = 0;
-        } else if ((++spins & 63u) == 0u) {
-          if (*abort_flag) break;
-          const uint64_t now = globaltimer_ns();
-          if (stall_t0 == 0) {
-            stall_t0 = now;
-          } else if (now - stall_t0 > kWaitLimitNs) {
+        ++next_pv;
+        progress = true;
+      }
+      if (progress) {
+        stall_t0 = 0;
+      } else if ((++spins & 63u) == 0u) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+        if (stall_t0 == 0) {
+          stall_t0 = now;
+        } else if (now - stall_t0 > kWaitLimitNs) {
+          if (lane == 0) {
             atomicOr(&g_status_attn, kDevTimeout);
             *abort_flag = 1;
-            break;
           }
+          break;
         }
       }
     }
@@ -419,34 +475,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
     const int h = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.a.softmax_scale * kLog2e;
-    const uint32_t prow_addr = smem_u32(sm + kOffP) + (h >> 3) * 512 + (h & 7) * 16;
     // l: sum of the bf16 weights actually multiplied into O (normalising by it
     // makes the output an exact convex combination of the rows); l32: the same
     // weights in fp32, for the log-sum-exp.
     float m = -INFINITY, l = 0.f, l32 = 0.f;
     bool ok = true;
     for (int j = 0; j < ntiles; ++j) {
+      const int st = j % S;
       ok = mbar_wait(&sfull[j & 1], (j >> 1) & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      // The producers' mask bytes are ordered by their release on full[]: that
-      // phase is still the current one here (the stage is only refilled after
-      // this tile's P V, which needs this thread's arrival on pfull).
-      ok = mbar_wait(&full[j & 1], (j >> 1) & 1, &g_status_attn, abort_flag);
+      // The producer's mask and scales are ordered by its release on full[st]:
+      // that phase is still the current one here (the stage is only refilled
+      // after this tile's P V, which needs this thread's arrival on pfull).
+      ok = mbar_wait(&full[st], (j / S) & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       uint32_t r[32];
-      tmem_ld32(tmem + lane_off + kColS + (j & 1) * kBR, r);
-      const uint32_t vmask = static_cast<uint32_t>(mask16[(j & 1) * 2]) |
-                             (static_cast<uint32_t>(mask16[(j & 1) * 2 + 1]) << 16);
+      tmem_ld32(tmem + lane_off + C::kColS + (j & 1) * kBR, r);
+      const uint32_t vmask = mask_s[st];
       float x[32];
       float mloc = -INFINITY;
       if (kFp8) {
         uint32_t rr[32];
-        tmem_ld32(tmem + lane_off + kColSr + (j & 1) * kBR, rr);
+        tmem_ld32(tmem + lane_off + C::kColSr + (j & 1) * kBR, rr);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const float lg = fmaf(row_scale[(j & 1) * kBR + i], __uint_as_float(r[i]), __uint_as_float(rr[i]));
+          const float lg = fmaf(row_scale[st * kBR + i], __uint_as_float(r[i]), __uint_as_float(rr[i]));
           x[i] = ((vmask >> i) & 1u) ? lg * sl2 : -INFINITY;
           mloc = fmaxf(mloc, x[i]);
         }
@@ -459,6 +514,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
         }
       }
       if (j >= 1) {
+        // P V_{j-1} must have read P (TMEM) and written O before P and O change
         ok = mbar_wait(pvdone, (j - 1) & 1, &g_status_attn, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
@@ -470,13 +526,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 #pragma unroll 1
         for (int cc = 0; cc < kDvHalf / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_st32(tmem + lane_off + C::kColO + cc * 32, o);
         }
-        tmem_st_wait();
       }
       if (need) {
         const float f = exp2f(m - m_new);
@@ -494,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
         if (kFp8) {
           // P V runs on the unscaled codes: fold the row scale into P; the
           // denominator takes the rounded weights divided back by the scale
-          const float s0 = row_scale[(j & 1) * kBR + 2 * i], s1 = row_scale[(j & 1) * kBR + 2 * i + 1];
+          const float s0 = row_scale[st * kBR + 2 * i], s1 = row_scale[st * kBR + 2 * i + 1];
           __nv_bfloat162 v = __floats2bfloat162_rn(p0 * s0, p1 * s1);
           pk[i] = *reinterpret_cast<uint32_t*>(&v);
           const float2 back = __bfloat1622float2(v);
@@ -508,10 +563,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
       }
       l += psum;
       l32 += psum32;
-#pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        st_shared_v4(prow_addr + cc * 128, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-      fence_proxy_async_smem();
+      tmem_st16(tmem + lane_off + C::kColP, pk);
+      tmem_st_wait();
       tc_fence_before();
       mbar_arrive(pfull);
     }
@@ -529,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 #pragma unroll 1
         for (int cc = 0; cc < kDvHalf / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
           tmem_ld_wait();
           uint32_t pk[16];
 #pragma unroll
@@ -546,7 +599,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 #pragma unroll 1
         for (int cc = 0; cc < kDvHalf / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kColO + cc * 32, o);
+          tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
           tmem_ld_wait();
           float4* dst = reinterpret_cast<float4*>(out + cc * 32);
 #pragma unroll
@@ -670,18 +723,18 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(attn_tc_kernel<false>,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+      attr_err = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      AttnCfg<false>::kSmemBytes);
       if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        AttnCfg<true>::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = seq.T * split * 2;
     if (fp8)
-      attn_tc_kernel<true><<<grid, kThreads, kSmemBytes, env.stream>>>(p);
+      attn_tc_kernel<true><<<grid, kThreads, AttnCfg<true>::kSmemBytes, env.stream>>>(p);
     else
-      attn_tc_kernel<false><<<grid, kThreads, kSmemBytes, env.stream>>>(p);
+      attn_tc_kernel<false><<<grid, kThreads, AttnCfg<false>::kSmemBytes, env.stream>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     char buf[128];

@@ -98,7 +98,9 @@ struct TcCfg {
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kOffStages + kTcStages * kStageBytes;
   static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [2][G*64]
-  static constexpr int kOffBar = kOffWq + 2 * N * 4;
+  static constexpr int kOffScale = kOffWq + 2 * N * 4;    // float [stages][128] key scales
+  static constexpr int kOffValid = kOffScale + kTcStages * kTcKeys * 4;  // uint32 [stages]
+  static constexpr int kOffBar = kOffValid + kTcStages * 4 + 8;
   // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2]
   static constexpr int kNumBars = 2 * kTcStages + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, sched[4]
@@ -234,7 +236,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+      // freed by the MMA (keys read) and by the epilogue (key scales read)
+      mbar_init(&empty[i], 1 + kTcEpiThreads);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
@@ -261,80 +264,113 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int64_t ntiles = end - begin;
 
   if (warp == 0) {
-    // ------------------------------------------------ TMA producer
-    if (lane == 0) {
-      TileWalker<G> w;
-      w.init(p, g_start, kt_start);
-      int cur_g = -1, qcount = 0;
-      for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
-        if (w.g != cur_g) {
-          const int qb = qcount & 1;
-          if (qcount >= 2 &&
-              !mbar_wait(&qempty[qb], ((qcount >> 1) - 1) & 1, &g_status_indexer, abort_flag))
-            break;
+    // ------------------------------------------------ TMA producer (warp 0)
+    // The warp keeps the page ids of a window of 32 logical pages in registers
+    // (one per lane, loaded in parallel); lane 0 issues, per 128-key tile, the TMA
+    // tile loads of its two pages and the bulk copies of their per-key scales.
+    TileWalker<G> w;
+    w.init(p, g_start, kt_start);
+    int cur_g = -1, qcount = 0;
+    int win = -1;           // first logical page held in the window
+    int32_t my_page = -1;   // page id of logical page win + lane
+    const int32_t* bt = p.seq.block_table;
+    bool b_ok = false;
+    uint32_t* valid_s = reinterpret_cast<uint32_t*>(sm + C::kOffValid);
+    float* scale_s = reinterpret_cast<float*>(sm + C::kOffScale);
+    for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+      if (w.g != cur_g) {
+        const int qb = qcount & 1;
+        if (qcount >= 2) {
+          const bool ok = mbar_wait(&qempty[qb], ((qcount >> 1) - 1) & 1, &g_status_indexer, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) break;
+        }
+        if (lane == 0) {
           mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
-          tma_load_2d(sm + C::kOffQ + qb * C::kQBytes, &qmap, &qfull[qb], 0,
-                      w.g * G * kTcHeads);
-          cur_g = w.g;
-          ++qcount;
+          tma_load_2d(sm + C::kOffQ + qb * C::kQBytes, &qmap, &qfull[qb], 0, w.g * G * kTcHeads);
         }
-        const int st = static_cast<int>(it % kTcStages);
-        if (it >= kTcStages &&
-            !mbar_wait(&empty[st], ((it / kTcStages) - 1) & 1, &g_status_indexer, abort_flag))
-          break;
         const int b = __ldg(p.seq.q_seq + w.g * G);
-        const bool b_ok = (b >= 0 && b < p.seq.B);
-        const int npg = (w.nhist + kTcPage - 1) / kTcPage;
-        const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b_ok ? b : 0) * p.seq.bt_stride;
-        int32_t pid[2];
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int lp = 2 * w.kt + h;
-          pid[h] = (b_ok && lp < npg) ? __ldg(bt + lp) : -1;
-          if (lp < npg && (pid[h] < 0 || pid[h] >= p.seq.n_pages || !b_ok)) {
-            atomicOr(&g_status_indexer, kDevBadIndex);
-            pid[h] = -1;
-          }
-          if (pid[h] >= 0) bytes += C::kStageBytes / 2;
+        b_ok = (b >= 0 && b < p.seq.B);
+        bt = p.seq.block_table + static_cast<int64_t>(b_ok ? b : 0) * p.seq.bt_stride;
+        win = -1;
+        cur_g = w.g;
+        ++qcount;
+      }
+      const int npg = (w.nhist + kTcPage - 1) / kTcPage;
+      const int lp0 = 2 * w.kt;
+      if (win < 0 || lp0 + 1 >= win + 32) {
+        win = lp0;
+        const int lp = win + lane;
+        my_page = (b_ok && lp < npg) ? __ldg(bt + lp) : -1;
+        if (lp < npg && (my_page < 0 || my_page >= p.seq.n_pages || !b_ok)) {
+          atomicOr(&g_status_indexer, kDevBadIndex);
+          my_page = -1;
         }
-        mbar_arrive_expect_tx(&full[st], bytes);
+      }
+      const int32_t pid0 = __shfl_sync(0xffffffffu, my_page, lp0 - win);
+      int32_t pid1 = __shfl_sync(0xffffffffu, my_page, min(lp0 + 1 - win, 31));
+      if (lp0 + 1 >= npg) pid1 = -1;
+      const int st = static_cast<int>(it % kTcStages);
+      if (it >= kTcStages) {
+        const bool ok = mbar_wait(&empty[st], ((it / kTcStages) - 1) & 1, &g_status_indexer, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      if (lane == 0) {
+        const bool scaled = p.a.k_scale != nullptr;
+        const uint32_t per_page = C::kStageBytes / 2 + (scaled ? kTcPage * 4 : 0);
+        valid_s[st] = (pid0 >= 0 ? 1u : 0u) | (pid1 >= 0 ? 2u : 0u);
+        mbar_arrive_expect_tx(&full[st], (pid0 >= 0 ? per_page : 0u) + (pid1 >= 0 ? per_page : 0u));
         uint8_t* dst = sm + C::kOffStages + st * C::kStageBytes;
-        if (pid[0] >= 0) tma_load_2d(dst, &kmap, &full[st], 0, pid[0] * kTcPage);
-        if (pid[1] >= 0) tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid[1] * kTcPage);
+        float* sdst = scale_s + st * kTcKeys;
+        if (pid0 >= 0) {
+          tma_load_2d(dst, &kmap, &full[st], 0, pid0 * kTcPage);
+          if (scaled) bulk_load(sdst, p.a.k_scale + static_cast<int64_t>(pid0) * kTcPage, kTcPage * 4, &full[st]);
+        }
+        if (pid1 >= 0) {
+          tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid1 * kTcPage);
+          if (scaled)
+            bulk_load(sdst + kTcPage, p.a.k_scale + static_cast<int64_t>(pid1) * kTcPage, kTcPage * 4, &full[st]);
+        }
       }
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      TileWalker<G> w;
-      w.init(p, g_start, kt_start);
-      int cur_g = -1, qcount = 0, qb = 0;
-      for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
-        if (w.g != cur_g) {
-          if (qcount > 0) umma_commit(&qempty[qb]);  // previous group's MMAs release its Q
-          qb = qcount & 1;
-          if (!mbar_wait(&qfull[qb], (qcount >> 1) & 1, &g_status_indexer, abort_flag)) break;
-          cur_g = w.g;
-          ++qcount;
+    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
+    TileWalker<G> w;
+    w.init(p, g_start, kt_start);
+    int cur_g = -1, qcount = 0, qb = 0;
+    for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+      if (w.g != cur_g) {
+        if (qcount > 0) {
+          if (elect_one()) umma_commit(&qempty[qb]);  // previous group's MMAs release its Q
+          __syncwarp();
         }
-        const int st = static_cast<int>(it % kTcStages);
-        if (!mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag)) break;
-        const int ab = static_cast<int>(it & 1);
-        if (it >= 2 &&
-            !mbar_wait(&accempty[ab], ((it >> 1) - 1) & 1, &g_status_indexer, abort_flag))
-          break;
-        tc_fence_after();
-        const uint32_t a_base = smem_u32(sm + C::kOffStages + st * C::kStageBytes);
-        const uint32_t b_base = smem_u32(sm + C::kOffQ + qb * C::kQBytes);
+        qb = qcount & 1;
+        const bool ok = mbar_wait(&qfull[qb], (qcount >> 1) & 1, &g_status_indexer, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+        cur_g = w.g;
+        ++qcount;
+      }
+      const int st = static_cast<int>(it % kTcStages);
+      bool ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int ab = static_cast<int>(it & 1);
+      if (it >= 2) {
+        ok = mbar_wait(&accempty[ab], ((it >> 1) - 1) & 1, &g_status_indexer, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      tc_fence_after();
+      // descriptors built once per tile; the unrolled K loop adds 32-byte steps to
+      // the start-address field; one elected lane issues the block
+      const uint64_t da = make_sdesc(smem_u32(sm + C::kOffStages + st * C::kStageBytes), 16, 1024, kLayoutSw128);
+      const uint64_t db = make_sdesc(smem_u32(sm + C::kOffQ + qb * C::kQBytes), 16, 1024, kLayoutSw128);
+      const uint32_t dcol = tmem + ab * C::N;
+      if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < kTcDim / 32; ++k) {
-          umma_f8(tmem + ab * C::N, make_sdesc(a_base + 32 * k, 16, 1024, kLayoutSw128),
-                  make_sdesc(b_base + 32 * k, 16, 1024, kLayoutSw128), C::kIdesc, k > 0 ? 1u : 0u);
-        }
+        for (int k = 0; k < kTcDim / 32; ++k)
+          umma_f8(dcol, da + static_cast<uint64_t>(2 * k), db + static_cast<uint64_t>(2 * k), C::kIdesc, k > 0 ? 1u : 0u);
         umma_commit(&empty[st]);
         umma_commit(&accfull[ab]);
       }
+      __syncwarp();
     }
   } else {
     // ------------------------------------------------ epilogue (warps 2..5)
@@ -394,17 +430,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         continue;
       }
       tc_fence_after();
-      const int s = w.kt * kTcKeys + row;
-      float sk = 0.f;
-      bool key_ok = false;
-      if (s < w.nhist) {
-        const int64_t r = phys_row(p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride,
-                                   s, kTcPage, p.seq.n_pages, &g_status_indexer);
-        if (r >= 0) {
-          key_ok = true;
-          sk = p.a.k_scale ? __ldg(p.a.k_scale + r) : 1.f;
-        }
+      // the stage (keys, scales, page validity) is still this tile's: the
+      // producer refills it only after this thread's arrival on empty[st]
+      const int st = static_cast<int>(it % kTcStages);
+      const bool okf = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
+      if (!__all_sync(0xffffffffu, okf)) {
+        dead = true;
+        continue;
       }
+      const int s = w.kt * kTcKeys + row;
+      const uint32_t vmask = reinterpret_cast<const volatile uint32_t*>(sm + C::kOffValid)[st];
+      const bool key_ok = s < w.nhist && ((vmask >> (row >> 6)) & 1u);
+      const float sk = key_ok ? (p.a.k_scale ? reinterpret_cast<const float*>(sm + C::kOffScale)[st * kTcKeys + row] : 1.f)
+                              : 0.f;
+      mbar_arrive(&empty[st]);
 #pragma unroll 1
       for (int j = 0; j < G; ++j) {
         uint32_t v0[32], v1[32];

@@ -7,15 +7,21 @@
 // position, as an ascending list followed by -1 padding.
 //
 // Exact radix select, one CTA (1024 threads) per query:
-//  * scores -> order-preserving uint32 keys (-0.0 folded onto +0.0);
-//  * up to four 8-bit digit passes, each a shared-memory histogram of the keys
-//    that still match the selected prefix, narrow the K-th largest key; a pass
-//    stops early when the bucket holding the K-th key is taken whole;
-//  * an ordered compaction (contiguous per-thread chunks, two block scans) keeps
-//    every key above the threshold and the first `remaining` keys equal to it,
-//    which writes the output already sorted.
-// Keys are cached in shared memory when the history fits (<= 48K positions);
-// longer histories re-read the scores from global memory (L2) on every pass.
+//  * a query's history is split into contiguous slices over the CTAs of a
+//    thread-block cluster (1 to 8 CTAs of 512 threads), each slice's scores
+//    turned into order-preserving uint32 keys (-0.0 folded onto +0.0) and cached
+//    in that CTA's shared memory;
+//  * up to four 8-bit digit passes narrow the K-th largest key: every CTA builds
+//    the histogram of its slice (lanes that hit the same bucket combine their
+//    counts), the cluster's histograms are summed through distributed shared
+//    memory, and every CTA picks the same digit; a pass stops early when the
+//    bucket holding the K-th key is taken whole;
+//  * an ordered compaction keeps every key above the threshold and, in position
+//    order, the first `remaining` keys equal to it: cluster-wide prefix counts
+//    give each CTA its offsets, contiguous per-thread chunks (two block scans)
+//    give each thread its own, so the output comes out in ascending order.
+#include <cooperative_groups.h>
+
 #include <algorithm>
 #include <cstdio>
 #include <mutex>
@@ -28,9 +34,13 @@ DSA_DEFINE_STATUS_WORD(topk)
 namespace dsa {
 namespace {
 
-constexpr int kThreads = 1024;
+namespace cg = cooperative_groups;
+
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int kCacheKeys = 48 * 1024;  // 192 KB of shared memory
+constexpr int kMaxCluster = 8;
+constexpr int kSliceKeys = 4096;        // target history slice per CTA
+constexpr int kCacheKeys = 48 * 1024;   // shared-memory key cache per CTA (192 KB)
 
 __device__ __forceinline__ uint32_t order_key(float f) {
   uint32_t u = __float_as_uint(f);
@@ -45,34 +55,34 @@ struct TopkArgs {
   int32_t max_ctx;
   int32_t K;
   int32_t* idx;
-  int32_t cache_keys;  // keys cached in dynamic smem (0 = none)
+  int32_t cache_keys;  // keys cached per CTA in dynamic smem (0 = none)
 };
 
 // Exclusive scan of one value per warp; every thread gets (its warp's offset,
-// block total).  Uses `buf` [kWarps] and two __syncthreads.
+// block total).  Uses `buf` [kWarps + 1] and two __syncthreads.
 __device__ __forceinline__ void warp_offsets(uint32_t warp_count, uint32_t* buf, uint32_t* excl,
                                              uint32_t* total) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) buf[warp] = warp_count;
   __syncthreads();
   if (warp == 0) {
-    const uint32_t v = buf[lane];
+    const uint32_t v = lane < kWarps ? buf[lane] : 0u;
     uint32_t inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += u;
     }
-    buf[lane] = inc - v;                       // exclusive
-    if (lane == 31) buf[kWarps] = inc;         // total
+    if (lane < kWarps) buf[lane] = inc - v;   // exclusive
+    if (lane == 31) buf[kWarps] = inc;        // total
   }
   __syncthreads();
   *excl = buf[warp];
   *total = buf[kWarps];
 }
 
-// Exclusive block-wide scan of one value per thread (all kThreads threads).
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, uint32_t* total) {
+// Exclusive block-wide scan of one value per thread.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf) {
   const int lane = threadIdx.x & 31;
   uint32_t inc = v;
 #pragma unroll
@@ -82,37 +92,45 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf, u
   }
   uint32_t w_excl, tot;
   warp_offsets(__shfl_sync(0xffffffffu, inc, 31), buf, &w_excl, &tot);
-  *total = tot;
   return w_excl + inc - v;
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   extern __shared__ uint32_t keys_s[];
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[256];        // this CTA's slice
+  __shared__ uint32_t ghist[256];       // the cluster's sum
   __shared__ uint32_t scan_buf[kWarps + 1];
   __shared__ uint32_t s_digit, s_rem, s_bucket;
+  __shared__ uint32_t s_counts[2];      // this slice: keys == prefix, keys selected
 
-  const int t = blockIdx.x;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = static_cast<int>(cluster.num_blocks());
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int t = blockIdx.x / CL;
   const int tid = threadIdx.x, lane = tid & 31;
   int qp = __ldg(a.q_pos + t);
   if (qp < 0 || qp >= a.max_ctx) {
-    if (tid == 0) atomicOr(&g_status_topk, kDevBadPos);
+    if (tid == 0 && rank == 0) atomicOr(&g_status_topk, kDevBadPos);
     qp = -1;  // no valid history: all -1
   }
   const int n = qp + 1;
   const int K = a.K;
   int32_t* out = a.idx + static_cast<int64_t>(t) * K;
-  if (n <= K) {
-    for (int i = tid; i < K; i += kThreads) out[i] = (i < n) ? i : -1;
+  if (n <= K) {  // cluster-uniform
+    for (int i = rank * kThreads + tid; i < K; i += CL * kThreads) out[i] = (i < n) ? i : -1;
     return;
   }
-  const float* row = a.scores + static_cast<int64_t>(t) * a.ld;
-  const bool cached = n <= a.cache_keys;
+  // this CTA's slice [lo, hi) of the history (slice starts are multiples of 4)
+  const int slice = ((n + CL - 1) / CL + 3) & ~3;
+  const int lo = min(n, rank * slice), hi = min(n, lo + slice);
+  const int len = hi - lo;
+  const float* row = a.scores + static_cast<int64_t>(t) * a.ld + lo;
+  const bool cached = slice <= a.cache_keys;
   auto key_at = [&](int i) -> uint32_t { return cached ? keys_s[i] : order_key(__ldg(row + i)); };
 
   if (cached) {
     // scores -> keys in shared memory: 16-byte loads, several in flight per thread
-    const int n4 = n >> 2;
+    const int n4 = len >> 2;
     const float4* row4 = reinterpret_cast<const float4*>(row);
 #pragma unroll 4
     for (int i = tid; i < n4; i += kThreads) {
@@ -120,8 +138,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       reinterpret_cast<uint4*>(keys_s)[i] =
           make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
     }
-    for (int i = 4 * n4 + tid; i < n; i += kThreads) keys_s[i] = order_key(__ldg(row + i));
-    __syncthreads();
+    for (int i = 4 * n4 + tid; i < len; i += kThreads) keys_s[i] = order_key(__ldg(row + i));
   }
 
   uint32_t prefix = 0, pmask = 0;
@@ -130,13 +147,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     const int shift = 24 - 8 * pass;
     for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
     __syncthreads();
-    // Scores cluster in few top-digit buckets: lanes hitting the same bucket
-    // combine their counts (match_any) so each bucket takes one atomic per warp.
-    for (int base = 0; base < n; base += kThreads) {
+    for (int base = 0; base < len; base += kThreads) {
       const int i = base + tid;
       bool act = false;
       uint32_t k = 0;
-      if (i < n) {
+      if (i < len) {
         k = key_at(i);
         act = (k & pmask) == prefix;
       }
@@ -147,6 +162,12 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
       }
     }
+    cluster.sync();  // every slice's histogram complete
+    for (int i = tid; i < 256; i += kThreads) {
+      uint32_t v = 0;
+      for (int r = 0; r < CL; ++r) v += cluster.map_shared_rank(hist, r)[i];
+      ghist[i] = v;
+    }
     __syncthreads();
     if (tid < 32) {
       // lane l owns digits 255-8l .. 248-8l (descending); find the digit where
@@ -154,7 +175,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       uint32_t c[8], loc = 0;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = hist[255 - (8 * lane + j)];
+        c[j] = ghist[255 - (8 * lane + j)];
         loc += c[j];
       }
       uint32_t inc = loc;
@@ -176,31 +197,58 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         }
       }
     }
-    __syncthreads();
+    cluster.sync();  // peers are done reading `hist`; s_* visible in this CTA
     prefix |= s_digit << shift;
     pmask |= 255u << shift;
     rem = s_rem;
     const bool whole = (s_bucket == rem);
     __syncthreads();  // s_* are rewritten next pass
-    if (whole) break;
+    if (whole) break;  // cluster-uniform (same histogram everywhere)
   }
 
-  // Ordered compaction.  Thread `tid` owns positions [tid*c, tid*c + c), c odd
-  // (so the shared-memory reads of a warp fall in distinct banks).  Keep every
-  // key above the threshold and, in position order, the first `rem` keys equal
-  // to it; the output comes out in ascending position order.
-  int c = (n + kThreads - 1) / kThreads;
+  // Ordered compaction.  Thread `tid` owns slice positions [tid*c, tid*c + c),
+  // c odd (the shared-memory reads of a warp fall in distinct banks).
+  int c = (len + kThreads - 1) / kThreads;
   c |= 1;
-  const int lo = min(n, tid * c), hi = min(n, lo + c);
-  uint32_t n_eq = 0;
-  for (int i = lo; i < hi; ++i) n_eq += (key_at(i) & pmask) == prefix;
-  uint32_t tot;
-  uint32_t eq_rank = block_excl_scan(n_eq, scan_buf, &tot);
+  const int tlo = min(len, tid * c), thi = min(len, tlo + c);
+  uint32_t n_eq = 0, n_gt = 0;
+  for (int i = tlo; i < thi; ++i) {
+    const uint32_t km = key_at(i) & pmask;
+    n_eq += km == prefix;
+    n_gt += km > prefix;
+  }
+  uint32_t eq_rank = block_excl_scan(n_eq, scan_buf);  // rank within this slice
+  const uint32_t slice_eq = scan_buf[kWarps];
   __syncthreads();
+  const uint32_t gt_total = [&] {
+    uint32_t v = n_gt;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+  }();
+  if (lane == 0) scan_buf[tid >> 5] = gt_total;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t g = 0;
+    for (int w = 0; w < kWarps; ++w) g += scan_buf[w];
+    s_counts[0] = slice_eq;
+    s_counts[1] = g;
+  }
+  cluster.sync();  // every slice's counts visible cluster-wide
+  // Earlier slices: their keys equal to the threshold (for this slice's ranks)
+  // and how many of their keys are selected (for this slice's output offset).
+  uint32_t eq_before = 0, sel_before = 0;
+  for (int r = 0; r < rank; ++r) {
+    const uint32_t* pc = cluster.map_shared_rank(s_counts, r);
+    const uint32_t e = pc[0], g = pc[1];
+    sel_before += g + (eq_before >= rem ? 0u : min(e, rem - eq_before));
+    eq_before += e;
+  }
+  eq_rank += eq_before;
   uint32_t n_sel = 0;
   {
     uint32_t r = eq_rank;
-    for (int i = lo; i < hi; ++i) {
+    for (int i = tlo; i < thi; ++i) {
       const uint32_t km = key_at(i) & pmask;
       if (km > prefix) {
         ++n_sel;
@@ -210,8 +258,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       }
     }
   }
-  uint32_t pos = block_excl_scan(n_sel, scan_buf, &tot);
-  for (int i = lo; i < hi && n_sel > 0; ++i) {
+  __syncthreads();
+  uint32_t pos = sel_before + block_excl_scan(n_sel, scan_buf);
+  for (int i = tlo; i < thi && n_sel > 0; ++i) {
     const uint32_t km = key_at(i) & pmask;
     bool sel = km > prefix;
     if (km == prefix) {
@@ -219,10 +268,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       ++eq_rank;
     }
     if (sel) {
-      out[pos++] = i;
+      out[pos++] = lo + i;
       --n_sel;
     }
   }
+  cluster.sync();  // peers may still read s_counts
 }
 
 }  // namespace
@@ -233,8 +283,10 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
     *plan += "topk[empty]";
     return cudaSuccess;
   }
-  const int cache = std::min(seq.max_ctx, kCacheKeys);
-  const size_t smem = (seq.max_ctx <= kCacheKeys) ? static_cast<size_t>(cache) * 4 : 0;
+  const int cl = std::max(1, std::min(kMaxCluster, (seq.max_ctx + kSliceKeys - 1) / kSliceKeys));
+  const int slice = ((seq.max_ctx + cl - 1) / cl + 3) & ~3;
+  const bool cached = slice <= kCacheKeys;
+  const size_t smem = cached ? static_cast<size_t>(slice) * 4 : 0;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
@@ -242,12 +294,24 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
                                     kCacheKeys * 4);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, smem ? cache : 0};
-  topk_kernel<<<seq.T, kThreads, smem, env.stream>>>(a);
+  TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, cached ? slice : 0};
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(seq.T * cl);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = env.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, a);
   char buf[96];
-  snprintf(buf, sizeof(buf), "topk_radix[%s]", smem ? "smem" : "global");
+  snprintf(buf, sizeof(buf), "topk_radix[cluster=%d,%s]", cl, cached ? "smem" : "global");
   *plan += buf;
-  return cudaGetLastError();
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace dsa

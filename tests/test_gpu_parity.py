@@ -146,13 +146,18 @@ def test_topk_ties_and_boundaries(dev, K):
     _topk_run(dev, scores, q_pos, K)
 
 
-def test_topk_long_history_uncached(dev):
-    """Histories longer than the shared-memory key cache read scores from L2."""
+def test_topk_long_history_cluster_and_uncached(dev):
+    """Long histories are split over a cluster of CTAs; beyond the clusters'
+    shared-memory key cache the scores are re-read from L2."""
     rng = np.random.default_rng(5)
     L = 70000
     scores = np.stack([rng.standard_normal(L), rng.integers(0, 50, L).astype(np.float64)]).astype(np.float32)
     plan = _topk_run(dev, scores, [L - 1, 60001], 2048)
-    assert "global" in plan
+    assert "cluster=8,smem" in plan, plan
+    L = 400000
+    scores = np.stack([rng.standard_normal(L), rng.integers(0, 9, L).astype(np.float64)]).astype(np.float32)
+    plan = _topk_run(dev, scores, [L - 1, 390001], 2048)
+    assert "global" in plan, plan
 
 
 # --------------------------------------------------------------------------- attention edges
