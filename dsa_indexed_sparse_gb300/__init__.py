@@ -25,7 +25,8 @@ DSA_F32, DSA_BF16, DSA_E4M3 = 0, 1, 2
 EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_plan",
             "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn_workspace_size",
             "dsa_sparse_mla_attn", "dsa_decode_workspace_size", "dsa_decode_step",
-            "dsa_check_status")
+            "dsa_decode_step_static_ws", "dsa_check_status")
+STATIC_WORKSPACE_BYTES = 32 << 20   # DSA_STATIC_WORKSPACE_BYTES
 
 
 class SeqDesc(ctypes.Structure):
@@ -69,6 +70,7 @@ def _load() -> ctypes.CDLL:
         "dsa_sparse_mla_attn": (C, [P, P, P, ctypes.c_int32, P, P, P, ctypes.c_size_t, P]),
         "dsa_decode_workspace_size": (ctypes.c_size_t, [P, P, P, ctypes.c_int32]),
         "dsa_decode_step": (C, [P, P, P, ctypes.c_int32, P, P, P, P, ctypes.c_size_t, P]),
+        "dsa_decode_step_static_ws": (C, [P, P, P, ctypes.c_int32, P, P, P, P]),
         "dsa_check_status": (C, [P]),
     }
     for name, (res, args) in sig.items():
@@ -211,6 +213,18 @@ def decode_step(seq: Seq, idx: Indexer, mla: Mla, K: int, out: torch.Tensor, wor
     _check(_lib.dsa_decode_step(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), K, _ptr(out), _ptr(lse),
                                 _ptr(idx_out), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream)))
+    return out
+
+
+def decode_step_static_ws(seq: Seq, idx: Indexer, mla: Mla, K: int, out: torch.Tensor,
+                          lse: Optional[torch.Tensor] = None, idx_out: Optional[torch.Tensor] = None,
+                          stream=None) -> torch.Tensor:
+    """decode_step with the scratch in the library's own device array (no workspace
+    argument, nothing allocated) -- for callers that cannot allocate device memory.
+    Calls overlapping on the GPU race on that shared array."""
+    s, x, m = seq.desc(), idx.desc(), mla.desc()
+    _check(_lib.dsa_decode_step_static_ws(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), K, _ptr(out),
+                                          _ptr(lse), _ptr(idx_out), _stream(stream)))
     return out
 
 

@@ -143,6 +143,8 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 namespace dsa {
 
+void set_last_error(const std::string& msg) { g_last_error = msg; }
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,

@@ -72,6 +72,9 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
                         const LaunchEnv& env, std::string* plan, bool* unsupported,
                         std::string* why);
 
+// Sets the text dsa_last_error() returns on the calling thread.
+void set_last_error(const std::string& msg);
+
 // Tensor-map encoder (driver entry point, resolved once).
 bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,

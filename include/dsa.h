@@ -170,6 +170,28 @@ dsa_status_t dsa_decode_step(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t
                              int32_t* idx_out, void* workspace, size_t workspace_bytes,
                              dsa_stream_t stream);
 
+/* The decode step with its scratch memory in a device array the library owns,
+ * for callers that cannot allocate device memory (for example a plugin inside
+ * an engine that owns all device memory and offers plugins no allocator, or a
+ * caller whose memory pool is fixed at start-up).  The method itself has no
+ * counterpart to this call: it is the same computation as dsa_decode_step, with
+ * `workspace` replaced by the library's array.
+ *  - Inputs and outputs are the caller's, exactly as for dsa_decode_step.
+ *  - DSA_STATIC_WORKSPACE_BYTES of device memory stay reserved on every GPU that
+ *    loads the library until the process exits.
+ *  - The first call on a device looks up that device's address of the array;
+ *    make it before starting any stream capture on that device.
+ *  - A step needing more scratch than DSA_STATIC_WORKSPACE_BYTES (see
+ *    dsa_decode_workspace_size) fails with DSA_ERR_WORKSPACE.  The call never
+ *    allocates device memory.
+ *  - All calls share the array and it keeps the last call's contents (the step
+ *    needs none of it zeroed).  Calls that overlap on the GPU -- on two streams or
+ *    from two host threads -- race on the array: serialise them. */
+#define DSA_STATIC_WORKSPACE_BYTES (32ull << 20)
+dsa_status_t dsa_decode_step_static_ws(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
+                                       const dsa_mla_desc_t* mla, int32_t K, void* out, float* lse,
+                                       int32_t* idx_out, dsa_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK (dsa_last_error() names the
  * flags), or DSA_ERR_CUDA if the stream itself reports an error. */
