@@ -149,6 +149,11 @@ void set_last_error(const std::string& msg) { g_last_error = msg; }
 bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                        std::string* why) {
+  return encode_tmap_2d(tmap_out, base, 1, inner, rows, row_stride_bytes, box_inner, box_rows, why);
+}
+
+bool encode_tmap_2d(void* tmap_out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, std::string* why) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -170,7 +175,8 @@ bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_
   const cuuint64_t strides[1] = {row_stride_bytes};
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+  const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const CUresult r = fn(static_cast<CUtensorMap*>(tmap_out), dt, 2,
                         const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float p0 = exp2f(x[2 * i] - msub), p1 = exp2f(x[2 * i + 1] - msub);
+        const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
         psum32 += p0 + p1;
         if (kFp8) {
           // P V runs on the unscaled codes: fold the row scale into P; the
@@ -577,35 +577,437 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const float lse = l32 > 0.f ? (m + log2f(l32)) * kLn2 : -INFINITY;
       const int64_t th = static_cast<int64_t>(t) * kH + h;
+      // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB per warp
+      const uint32_t stg = smem_u32(sm + C::kOffKV) + quarter * 4096;
+      const int64_t th0 = static_cast<int64_t>(t) * kH + quarter * 32;   // this warp's first head
       if (p.n_split == 1) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.a.out) + th * kDv + c * kDvHalf;
+        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + c * kDvHalf);
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
+        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tmem + lane_off + C::kColO + cc * 64, o0);
+          tmem_ld32(tmem + lane_off + C::kColO + cc * 64 + 32, o1);
           tmem_ld_wait();
-          uint32_t pk[16];
+          uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv);
-          uint4* dst = reinterpret_cast<uint4*>(out + cc * 32);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) dst[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+          for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+            pk[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
+          }
+          warp_store_rows128(stg, pk, out + cc * 128, kDv * 2, lane);
         }
         if (c == 0 && p.a.lse) p.a.lse[th] = lse;
       } else {
         const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
-        float* out = p.ws_o + sth * kDv + c * kDvHalf;
+        uint8_t* out = reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<int64_t>(split) * p.seq.T * kH + th0) * kDv +
+                                                  c * kDvHalf);
 #pragma unroll 1
         for (int cc = 0; cc < kDvHalf / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
           tmem_ld_wait();
-          float4* dst = reinterpret_cast<float4*>(out + cc * 32);
 #pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv, __uint_as_float(o[4 * i + 1]) * inv,
-                                 __uint_as_float(o[4 * i + 2]) * inv, __uint_as_float(o[4 * i + 3]) * inv);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
+          warp_store_rows128(stg, o, out + cc * 128, kDv * 4, lane);
+        }
+        if (c == 0) p.ws_lse[sth] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// bf16 rows, 64-row tiles gathered by TMA.
+//
+// Two producer groups of four warps own one stage each and load alternate tiles
+// (16 rows per warp): lanes resolve the rows (index -> page -> cache row) while
+// the stage is still busy, then every lane copies its fixed 16-byte chunks of
+// each row with cp.async into the 128B-swizzled K-major tile (the row loop is
+// unrolled so the swizzle is a constant per row); rows that select nothing are
+// zeroed.
+// (A tile::gather4 TMA producer measured ~40 ns per 4 x 128-byte gather on this
+// GPU, several times slower than this.)  Q K^T runs with N = 64 rows
+// (the first 256 query dims read from TMEM), P V with N = 256 value dims and P
+// read from TMEM.  TMEM: S [0,64) (single buffer), P [64,96), Q [128,256),
+// O [256,512).  Two tiles of 72 KB are in flight.
+constexpr int kBR64 = 64;
+constexpr int kTile64Bytes = kBR64 * kDqk * 2;                 // 73728
+constexpr int kT64Stages = 2;
+constexpr int kT64QTmemDims = 256;
+constexpr int kT64QSmemAtoms = (kDqk - kT64QTmemDims) / 64;    // 5
+constexpr int kT64OffQ = 0;
+constexpr int kT64OffKV = kT64QSmemAtoms * kH * 128;           // 81920
+constexpr int kT64OffMask = kT64OffKV + kT64Stages * kTile64Bytes;  // uint64 [stages]
+constexpr int kT64OffBar = kT64OffMask + 16;
+// barriers: full[2], empty[2], sfull, sfree, pfull, pvdone, ofull
+constexpr int kT64NumBars = 2 * kT64Stages + 5;
+constexpr int kT64OffMisc = kT64OffBar + kT64NumBars * 8;
+constexpr int kT64SmemBytes = kT64OffMisc + 16 + 1024;
+constexpr int kT64Threads = 416;   // warps 0-7 producers (2 groups), warp 8 MMA, warps 9-12 softmax
+constexpr uint32_t kT64ColS = 0, kT64ColP = 64, kT64ColQ = 128, kT64ColO = 256;
+constexpr uint32_t kIdescS64 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR64);
+static_assert(kT64SmemBytes <= 232448, "shared memory budget");
+
+__global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams p) {
+  extern __shared__ __align__(1024) uint8_t sm_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kT64OffBar);
+  uint64_t* full = bars;            // [2] tile landed (one arrival per warp of the stage's group)
+  uint64_t* empty = bars + 2;       // [2] tile consumed by P V
+  uint64_t* sfull = bars + 4;       // logits ready
+  uint64_t* sfree = bars + 5;       // logits read by the softmax (S buffer reusable)
+  uint64_t* pfull = bars + 6;
+  uint64_t* pvdone = bars + 7;
+  uint64_t* ofull = bars + 8;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kT64OffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
+  volatile uint64_t* mask_s = reinterpret_cast<volatile uint64_t*>(sm + kT64OffMask);
+  volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + kT64OffMask);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x & 1;
+  const int rest = blockIdx.x >> 1;
+  const int split = rest % p.n_split;
+  const int t = rest / p.n_split;
+  const int K = p.a.K;
+  const int r0 = split * p.rows_per_split;
+  const int r1 = min(K, r0 + p.rows_per_split);
+  const int ntiles = (r1 - r0 + kBR64 - 1) / kBR64;
+
+  int qp = __ldg(p.seq.q_pos + t);
+  int b = __ldg(p.seq.q_seq + t);
+  if (qp < 0 || qp >= p.seq.max_ctx || b < 0 || b >= p.seq.B) {
+    if (threadIdx.x == 0) atomicOr(&g_status_attn, kDevBadPos);
+    qp = -1;
+    b = 0;
+  }
+  const uint16_t* qg = static_cast<const uint16_t*>(p.a.q) + static_cast<int64_t>(t) * kH * kDqk;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kT64Stages; ++i) {
+      mbar_init(&full[i], 4);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(sfull, 1);
+    mbar_init(sfree, 128);
+    mbar_init(pfull, 128);
+    mbar_init(pvdone, 1);
+    mbar_init(ofull, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 8) {
+    tmem_alloc(misc, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+  // The producers start gathering tiles at once; warps 8-12 stage the query
+  // meanwhile (dims [256, 576) in shared memory, [0, 256) in TMEM) and meet at
+  // named barrier 1 before the first MMA.
+  constexpr uint32_t kQBar = 1, kQBarThreads = 5 * 32;
+  if (warp >= 8) {
+    const uint32_t qbase = smem_u32(sm + kT64OffQ);
+    constexpr int kChunks = (kDqk - kT64QTmemDims) / 8;
+    for (int i = threadIdx.x - 8 * 32; i < kH * kChunks; i += kQBarThreads) {
+      const int h = i / kChunks, ch = i % kChunks;
+      cp_async16(qbase + sw128_offset(h, ch, kH), qg + h * kDqk + kT64QTmemDims + ch * 8);
+    }
+    cp_async_commit();
+  }
+  if (warp >= 9) {
+    const int h = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
+#pragma unroll 1
+    for (int blk = 0; blk < kT64QTmemDims / 64; ++blk) {
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(qrow + blk * 8 + i);
+        r[4 * i] = v.x;
+        r[4 * i + 1] = v.y;
+        r[4 * i + 2] = v.z;
+        r[4 * i + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_off + kT64ColQ + blk * 32, r);
+    }
+    tmem_st_wait();
+  }
+  if (warp >= 8) {
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(kQBar, kQBarThreads);
+    tc_fence_after();
+  }
+
+  if (warp < 8) {
+    // ------------------------------------------------ producers: group g = warp / 4 loads tiles
+    // j = g mod 2 into stage g; warp w = warp % 4 copies tile rows [16w, 16w+16)
+    const int grp = warp >> 2, pw = warp & 3;
+    const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);
+    const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride;
+    const int32_t* idx = p.a.idx + static_cast<int64_t>(t) * K;
+    // this lane's 16-byte chunks of a row: ch = lane, lane + 32, and lane + 64 for lanes < 8
+    const int nch = lane < 8 ? 3 : 2;
+    uint32_t dst_off[3], src_off[3];
+#pragma unroll
+    for (int k = 0; k < 3; ++k) {
+      const int ch = lane + 32 * k;
+      dst_off[k] = static_cast<uint32_t>((ch >> 3) * kBR64 * 128);   // atom block
+      src_off[k] = static_cast<uint32_t>(ch * 16);
+    }
+    const int st = grp;
+    const uint32_t stage = smem_u32(sm + kT64OffKV + st * kTile64Bytes);
+    for (int j = grp; j < ntiles; j += kT64Stages) {
+      int64_t my_row = -1;
+      if (lane < 16) {
+        const int gi = r0 + j * kBR64 + pw * 16 + lane;
+        if (gi < r1) {
+          const int pos = __ldg(idx + gi);
+          if (pos >= 0) {
+            if (pos > qp)
+              atomicOr(&g_status_attn, kDevBadIndex);
+            else
+              my_row = phys_row(bt, pos, p.seq.page_size, p.seq.n_pages, &g_status_attn);
+          }
+        }
+      }
+      const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFFFFu;
+      if (j >= kT64Stages) {
+        const bool ok = mbar_wait(&empty[st], ((j / kT64Stages) - 1) & 1, &g_status_attn, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      if (lane == 0) mask16[st * 4 + pw] = static_cast<uint16_t>(bits);
+#pragma unroll
+      for (int rr = 0; rr < 16; ++rr) {
+        const int r = pw * 16 + rr;                          // row within the tile
+        const int64_t prow = __shfl_sync(0xffffffffu, my_row, rr);
+        const uint32_t drow = stage + static_cast<uint32_t>(r * 128);
+        if (prow >= 0) {
+          const uint8_t* srow = kv + prow * p.a.row_bytes;
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            if (k < nch) {
+              const uint32_t sw = static_cast<uint32_t>((((lane + 32 * k) & 7) ^ (r & 7)) << 4);
+              cp_async16(drow + dst_off[k] + sw, srow + src_off[k]);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 3; ++k) {
+            if (k < nch) {
+              const uint32_t sw = static_cast<uint32_t>((((lane + 32 * k) & 7) ^ (r & 7)) << 4);
+              st_shared_v4(drow + dst_off[k] + sw, 0u, 0u, 0u, 0u);
+            }
+          }
+        }
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[st]);
+    }
+  } else if (warp == 8) {
+    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
+    const uint64_t dq0 = make_sdesc(smem_u32(sm + kT64OffQ), 16, 1024, kLayoutSw128);
+    const uint64_t dk0 = make_sdesc(smem_u32(sm + kT64OffKV), 16, 1024, kLayoutSw128);
+    const uint64_t dv0 = make_sdesc(smem_u32(sm + kT64OffKV) + c * 4 * kBR64 * 128, kBR64 * 128, 1024, kLayoutSw128);
+    int next_s = 0, next_pv = 0;
+    uint32_t spins = 0;
+    uint64_t stall_t0 = 0;
+    while (next_pv < ntiles) {
+      bool progress = false;
+      // S_j needs tile j and the S buffer read by the softmax of tile j-1
+      const bool s_ready = next_s < ntiles &&
+                           (next_s == 0 || mbar_test_wait(smem_u32(sfree), (next_s - 1) & 1)) &&
+                           mbar_test_wait(smem_u32(&full[next_s % kT64Stages]), (next_s / kT64Stages) & 1);
+      if (__shfl_sync(0xffffffffu, s_ready, 0)) {
+        tc_fence_after();
+        const int j = next_s;
+        const uint64_t dk = dk0 + static_cast<uint64_t>(((j % kT64Stages) * kTile64Bytes) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kDqk / 16; ++kk) {
+            const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR64 * 128 + (kk & 3) * 32) >> 4);
+            const uint32_t acc = kk == 0 ? 0u : 1u;
+            if (kk < kT64QTmemDims / 16) {
+              umma_f16_tmem_a(tmem + kT64ColS, tmem + kT64ColQ + kk * 8, db, kIdescS64, acc);
+            } else {
+              const int qk = kk - kT64QTmemDims / 16;
+              const uint64_t da = dq0 + static_cast<uint64_t>(((qk >> 2) * kH * 128 + (qk & 3) * 32) >> 4);
+              umma_f16(tmem + kT64ColS, da, db, kIdescS64, acc);
+            }
+          }
+          umma_commit(sfull);
+        }
+        __syncwarp();
+        ++next_s;
+        progress = true;
+      }
+      const bool p_ready = next_pv < next_s && mbar_test_wait(smem_u32(pfull), next_pv & 1);
+      if (__shfl_sync(0xffffffffu, p_ready, 0)) {
+        tc_fence_after();
+        const int j = next_pv;
+        const uint64_t dv = dv0 + static_cast<uint64_t>(((j % kT64Stages) * kTile64Bytes) >> 4);
+        if (elect_one()) {
+#pragma unroll
+          for (int kk = 0; kk < kBR64 / 16; ++kk)
+            umma_f16_tmem_a(tmem + kT64ColO, tmem + kT64ColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                            kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(pvdone);
+          umma_commit(&empty[j % kT64Stages]);
+          if (j == ntiles - 1) umma_commit(ofull);
+        }
+        __syncwarp();
+        ++next_pv;
+        progress = true;
+      }
+      if (progress) {
+        stall_t0 = 0;
+      } else if ((++spins & 63u) == 0u) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+        if (stall_t0 == 0) {
+          stall_t0 = now;
+        } else if (now - stall_t0 > kWaitLimitNs) {
+          if (lane == 0) {
+            atomicOr(&g_status_attn, kDevTimeout);
+            *abort_flag = 1;
+          }
+          break;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------ softmax + epilogue (warps 9-12)
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float sl2 = p.a.softmax_scale * kLog2e;
+    float m = -INFINITY, l = 0.f, l32 = 0.f;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kT64Stages;
+      ok = mbar_wait(sfull, j & 1, &g_status_attn, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      // the producer's row mask is ordered by its release on full[st] (still the
+      // current phase: the stage is refilled only after this tile's P V)
+      ok = mbar_wait(&full[st], (j / kT64Stages) & 1, &g_status_attn, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t r0v[32], r1v[32];
+      tmem_ld32(tmem + lane_off + kT64ColS, r0v);
+      tmem_ld32(tmem + lane_off + kT64ColS + 32, r1v);
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(sfree);
+      const uint64_t vmask = mask_s[st];
+      float x[64];
+      float mloc = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        x[i] = ((vmask >> i) & 1u) ? __uint_as_float(r0v[i]) * sl2 : -INFINITY;
+        x[32 + i] = ((vmask >> (32 + i)) & 1u) ? __uint_as_float(r1v[i]) * sl2 : -INFINITY;
+        mloc = fmaxf(mloc, fmaxf(x[i], x[32 + i]));
+      }
+      if (j >= 1) {
+        ok = mbar_wait(pvdone, (j - 1) & 1, &g_status_attn, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      const float m_new = fmaxf(m, mloc);
+      const bool need = m_new > m + kRescaleThreshold;
+      if (j >= 1 && __any_sync(0xffffffffu, need)) {
+        const float f = need ? exp2f(m - m_new) : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + kT64ColO + cc * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
+          tmem_st32(tmem + lane_off + kT64ColO + cc * 32, o);
+        }
+      }
+      if (need) {
+        const float f = exp2f(m - m_new);
+        l *= f;
+        l32 *= f;
+        m = m_new;
+      }
+      const float msub = (m == -INFINITY) ? 0.f : m;
+      float psum = 0.f, psum32 = 0.f;
+      uint32_t pk[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
+        psum32 += p0 + p1;
+        __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
+        pk[i] = *reinterpret_cast<uint32_t*>(&v);
+        const float2 back = __bfloat1622float2(v);
+        psum += back.x + back.y;
+      }
+      l += psum;
+      l32 += psum32;
+      tmem_st32(tmem + lane_off + kT64ColP, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(pfull);
+    }
+    if (ok) {
+      ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+    }
+    if (ok) {
+      tc_fence_after();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse = l32 > 0.f ? (m + log2f(l32)) * kLn2 : -INFINITY;
+      const int64_t th = static_cast<int64_t>(t) * kH + h;
+      // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB each
+      const uint32_t stg = smem_u32(sm + kT64OffKV) + quarter * 4096;
+      const int64_t th0 = static_cast<int64_t>(t) * kH + quarter * 32;   // this warp's first head
+      if (p.n_split == 1) {
+        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + c * kDvHalf);
+#pragma unroll 1
+        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+          uint32_t o0[32], o1[32];
+          tmem_ld32(tmem + lane_off + kT64ColO + cc * 64, o0);
+          tmem_ld32(tmem + lane_off + kT64ColO + cc * 64 + 32, o1);
+          tmem_ld_wait();
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            pk[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+            pk[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
+          }
+          warp_store_rows128(stg, pk, out + cc * 128, kDv * 2, lane);
+        }
+        if (c == 0 && p.a.lse) p.a.lse[th] = lse;
+      } else {
+        const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
+        uint8_t* out = reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<int64_t>(split) * p.seq.T * kH + th0) * kDv +
+                                                  c * kDvHalf);
+#pragma unroll 1
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tmem + lane_off + kT64ColO + cc * 32, o);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
+          warp_store_rows128(stg, o, out + cc * 128, kDv * 4, lane);
         }
         if (c == 0) p.ws_lse[sth] = lse;
       }
@@ -621,12 +1023,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 }
 
 // Merges row slices: out[t,h,:] = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max_s lse_s);
-// lse = max + log sum_s w_s.  One CTA per (query, group of 8 heads); a warp per head.
+// lse = max + log sum_s w_s.  One CTA per (query, group of 8 heads); a warp per
+// head, each lane owning 4 float4 columns; the slices' loads are issued four
+// slices at a time so that 16 loads per lane are in flight.
 constexpr int kCombineHeads = 8;
 __global__ void __launch_bounds__(256)
-    attn_combine_kernel(const float* ws_o, const float* ws_lse, int n_split, int T, int H, int dv,
+    attn_combine_kernel(const float* ws_o, const float* ws_lse, int n_split, int T,
                         __nv_bfloat16* out, float* lse_out) {
   extern __shared__ float wts[];  // [kCombineHeads][n_split]
+  constexpr int H = kH, kV4 = kDv / 4 / 32;   // float4 per lane
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * kCombineHeads + warp;
@@ -648,20 +1053,46 @@ __global__ void __launch_bounds__(256)
   if (lane == 0 && lse_out) lse_out[static_cast<int64_t>(t) * H + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const int64_t th = static_cast<int64_t>(t) * H + h;
-  for (int i = lane; i < dv / 4; i += 32) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int s = 0; s < n_split; ++s) {
-      const float ww = w[s];
-      if (ww == 0.f) continue;
-      const float4 v = reinterpret_cast<const float4*>(ws_o + (static_cast<int64_t>(s) * T * H + th) * dv)[i];
-      acc.x = fmaf(ww, v.x, acc.x);
-      acc.y = fmaf(ww, v.y, acc.y);
-      acc.z = fmaf(ww, v.z, acc.z);
-      acc.w = fmaf(ww, v.w, acc.w);
+  const int64_t slice_stride = static_cast<int64_t>(T) * H * (kDv / 4);   // in float4
+  const float4* src = reinterpret_cast<const float4*>(ws_o) + th * (kDv / 4) + lane;
+  float4 acc[kV4];
+#pragma unroll
+  for (int k = 0; k < kV4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  int s = 0;
+  for (; s + 4 <= n_split; s += 4) {
+    float4 v[4][kV4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int k = 0; k < kV4; ++k) v[u][k] = __ldcs(src + (s + u) * slice_stride + 32 * k);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float ww = w[s + u];
+#pragma unroll
+      for (int k = 0; k < kV4; ++k) {
+        acc[k].x = fmaf(ww, v[u][k].x, acc[k].x);
+        acc[k].y = fmaf(ww, v[u][k].y, acc[k].y);
+        acc[k].z = fmaf(ww, v[u][k].z, acc[k].z);
+        acc[k].w = fmaf(ww, v[u][k].w, acc[k].w);
+      }
     }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-    reinterpret_cast<uint2*>(out + th * dv)[i] =
+  }
+  for (; s < n_split; ++s) {
+    const float ww = w[s];
+#pragma unroll
+    for (int k = 0; k < kV4; ++k) {
+      const float4 v = __ldcs(src + s * slice_stride + 32 * k);
+      acc[k].x = fmaf(ww, v.x, acc[k].x);
+      acc[k].y = fmaf(ww, v.y, acc[k].y);
+      acc[k].z = fmaf(ww, v.z, acc[k].z);
+      acc[k].w = fmaf(ww, v.w, acc[k].w);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kV4; ++k) {
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
+    reinterpret_cast<uint2*>(out + th * kDv)[lane + 32 * k] =
         make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
   }
 }
@@ -708,10 +1139,12 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     return cudaSuccess;
   }
   if (tc_supported(seq, a)) {
+    const bool fp8 = a.kind == MlaKind::kFP8Row;
+    const int tile_rows = fp8 ? kBR : kBR64;
     int split = choose_split(seq, a, env.num_sms);
     if (split > 1 && (workspace == nullptr || ws_bytes < attn_workspace_bytes(seq, a, env.num_sms)))
       split = 1;  // no room for partials: one slice per query
-    const int rps = ((a.K + split - 1) / split + kBR - 1) / kBR * kBR;
+    const int rps = ((a.K + split - 1) / split + tile_rows - 1) / tile_rows * tile_rows;
     split = (a.K + rps - 1) / rps;  // every slice non-empty
     TcAttnParams p{seq, a, split, rps, nullptr, nullptr};
     if (split > 1) {
@@ -719,31 +1152,31 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
       p.ws_o = static_cast<float*>(workspace);
       p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o + 255) / 256) * 256);
     }
-    const bool fp8 = a.kind == MlaKind::kFP8Row;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      AttnCfg<false>::kSmemBytes);
+      attr_err = cudaFuncSetAttribute(attn_tc64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kT64SmemBytes);
       if (attr_err == cudaSuccess)
         attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         AttnCfg<true>::kSmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = seq.T * split * 2;
-    if (fp8)
+    if (fp8) {
       attn_tc_kernel<true><<<grid, kThreads, AttnCfg<true>::kSmemBytes, env.stream>>>(p);
-    else
-      attn_tc_kernel<false><<<grid, kThreads, AttnCfg<false>::kSmemBytes, env.stream>>>(p);
+    } else {
+      attn_tc64_kernel<<<grid, kT64Threads, kT64SmemBytes, env.stream>>>(p);
+    }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     char buf[128];
-    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8" : "bf16", split, grid);
+    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8" : "bf16x64", split, grid);
     *plan += buf;
     if (split > 1) {
       const size_t smem = static_cast<size_t>(split) * kCombineHeads * sizeof(float);
       attn_combine_kernel<<<dim3(seq.T, kH / kCombineHeads), 256, smem, env.stream>>>(
-          p.ws_o, p.ws_lse, split, seq.T, kH, kDv, static_cast<__nv_bfloat16*>(a.out), a.lse);
+          p.ws_o, p.ws_lse, split, seq.T, static_cast<__nv_bfloat16*>(a.out), a.lse);
       *plan += "+attn_combine";
       e = cudaGetLastError();
     }

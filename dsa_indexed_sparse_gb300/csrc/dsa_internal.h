@@ -79,6 +79,9 @@ void set_last_error(const std::string& msg);
 bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
                        uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows,
                        std::string* why);
+// Same for 1- or 2-byte elements (inner / box_inner counted in elements), 128-byte swizzle.
+bool encode_tmap_2d(void* tmap_out, const void* base, int elem_bytes, uint64_t inner, uint64_t rows,
+                    uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_rows, std::string* why);
 
 }  // namespace dsa
 
