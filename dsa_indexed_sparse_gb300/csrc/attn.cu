@@ -624,36 +624,98 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 rows, 64-row tiles gathered by TMA.
+// bf16 rows, 64-row tiles.
 //
-// Two producer groups of four warps own one stage each and load alternate tiles
-// (16 rows per warp): lanes resolve the rows (index -> page -> cache row) while
-// the stage is still busy, then every lane copies its fixed 16-byte chunks of
-// each row with cp.async into the 128B-swizzled K-major tile (the row loop is
-// unrolled so the swizzle is a constant per row); rows that select nothing are
-// zeroed.
-// (A tile::gather4 TMA producer measured ~40 ns per 4 x 128-byte gather on this
-// GPU, several times slower than this.)  Q K^T runs with N = 64 rows
-// (the first 256 query dims read from TMEM), P V with N = 256 value dims and P
-// read from TMEM.  TMEM: S [0,64) (single buffer), P [64,96), Q [128,256),
-// O [256,512).  Two tiles of 72 KB are in flight.
+// Producers (warps 0-7): two groups of four warps own one stage each and load
+// alternate tiles (16 rows per warp).  Lanes resolve the rows (index -> page ->
+// cache row) as soon as the group's previous tile has landed, about one
+// tile-time before the stage frees, and ask L2 to fetch those rows right away;
+// once the stage is free every lane copies its fixed 16-byte chunks of each row
+// with cp.async into the 128B-swizzled K-major tile (the row loop is unrolled
+// so the swizzle is a constant per row), now mostly from L2; rows that select
+// nothing are zeroed.  (On this GPU a tile::gather4 TMA producer reached ~12
+// GB/s per SM and cp.async gathers ~60 GB/s.)
+//
+// Softmax (warps 8-15): two warps per TMEM lane quarter; warp half hf takes
+// logit columns [32 hf, 32 hf + 32) and output columns [128 hf, 128 hf + 128),
+// and the pair agrees on the running max each tile through a shared-memory
+// value and a sequence flag (bounded spin).  One warp (the lead, warp 8) also
+// issues the MMAs, in the order P V_j then Q K^T_{j+1}, right after P_j is
+// complete: P V then never queues behind a whole Q K^T (it frees the stage
+// sooner), and the softmax never waits for the previous P V.
+//
+// Q K^T runs with N = 64 rows, P V with N = 256 value dims and P read from
+// TMEM.  An M=128 K=16 step whose A operand (the query) sits in shared memory
+// reads 6 KB of shared memory and takes ~53 clk, one with A in TMEM ~36 clk, so
+// the first 320 query dims live in TMEM.  TMEM: S [0,64), P [64,96), Q
+// [96,256), O [256,512).  Two tiles of 72 KB are in flight.
 constexpr int kBR64 = 64;
 constexpr int kTile64Bytes = kBR64 * kDqk * 2;                 // 73728
 constexpr int kT64Stages = 2;
-constexpr int kT64QTmemDims = 256;
-constexpr int kT64QSmemAtoms = (kDqk - kT64QTmemDims) / 64;    // 5
+constexpr int kT64QTmemDims = 320;
+constexpr int kT64QTmemSteps = kT64QTmemDims / 16;             // 20
+constexpr int kT64QSmemAtoms = (kDqk - kT64QTmemDims) / 64;    // 4
 constexpr int kT64OffQ = 0;
-constexpr int kT64OffKV = kT64QSmemAtoms * kH * 128;           // 81920
+constexpr int kT64OffKV = kT64QSmemAtoms * kH * 128;           // 65536
 constexpr int kT64OffMask = kT64OffKV + kT64Stages * kTile64Bytes;  // uint64 [stages]
-constexpr int kT64OffBar = kT64OffMask + 16;
-// barriers: full[2], empty[2], sfull, sfree, pfull, pvdone, ofull
-constexpr int kT64NumBars = 2 * kT64Stages + 5;
+constexpr int kT64OffRed = kT64OffMask + 16;                   // float [2 halves][128 heads]
+constexpr int kT64OffFlag = kT64OffRed + 2 * kH * 4;           // int [2 halves][4 quarters]
+constexpr int kT64OffBar = kT64OffFlag + 32;
+// barriers: full[2], empty[2], sfull, pfull, pvdone, ofull
+constexpr int kT64NumBars = 2 * kT64Stages + 4;
 constexpr int kT64OffMisc = kT64OffBar + kT64NumBars * 8;
 constexpr int kT64SmemBytes = kT64OffMisc + 16 + 1024;
-constexpr int kT64Threads = 416;   // warps 0-7 producers (2 groups), warp 8 MMA, warps 9-12 softmax
-constexpr uint32_t kT64ColS = 0, kT64ColP = 64, kT64ColQ = 128, kT64ColO = 256;
+// 16 warps: 4 per SM sub-partition, so 128 registers a thread
+constexpr int kT64Threads = 512;   // warps 0-7 producers, warps 8-15 softmax (warp 8 also issues MMAs)
+constexpr int kT64Lead = 8;
+constexpr int kT64Softmax = 256;
+constexpr uint32_t kT64ColS = 0, kT64ColP = 64, kT64ColQ = 96, kT64ColO = 256;
 constexpr uint32_t kIdescS64 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR64);
+static_assert(kT64ColQ + kT64QTmemDims / 2 <= kT64ColO, "TMEM plan");
 static_assert(kT64SmemBytes <= 232448, "shared memory budget");
+
+// Q K^T of one tile (elected lane of the lead warp).
+__device__ __forceinline__ void t64_issue_s(uint32_t tmem, uint64_t dq0, uint64_t dk) {
+#pragma unroll
+  for (int kk = 0; kk < kDqk / 16; ++kk) {
+    const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR64 * 128 + (kk & 3) * 32) >> 4);
+    const uint32_t acc = kk == 0 ? 0u : 1u;
+    if (kk < kT64QTmemSteps) {
+      umma_f16_tmem_a(tmem + kT64ColS, tmem + kT64ColQ + kk * 8, db, kIdescS64, acc);
+    } else {
+      const int qk = kk - kT64QTmemSteps;
+      const uint64_t da = dq0 + static_cast<uint64_t>(((qk >> 2) * kH * 128 + (qk & 3) * 32) >> 4);
+      umma_f16(tmem + kT64ColS, da, db, kIdescS64, acc);
+    }
+  }
+}
+
+// Exchanges one value per head with the partner warp of the pair: write own
+// value, publish sequence number `seq`, spin (bounded) on the partner's.
+__device__ __forceinline__ bool t64_pair_swap(volatile float* mine, volatile float* theirs, volatile int* my_flag,
+                                              volatile int* their_flag, int seq, float v, float* other, int lane,
+                                              volatile int* abort_flag) {
+  *mine = v;
+  __syncwarp();
+  if (lane == 0) {
+    __threadfence_block();
+    *my_flag = seq;
+  }
+  bool ok = true;
+  if (*their_flag < seq) {
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    while (*their_flag < seq) {
+      if ((++spins & 255u) == 0u && (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
+        ok = false;
+        break;
+      }
+    }
+  }
+  __threadfence_block();
+  *other = *theirs;
+  return __all_sync(0xffffffffu, ok);
+}
 
 __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams p) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
@@ -663,14 +725,15 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
   uint64_t* full = bars;            // [2] tile landed (one arrival per warp of the stage's group)
   uint64_t* empty = bars + 2;       // [2] tile consumed by P V
   uint64_t* sfull = bars + 4;       // logits ready
-  uint64_t* sfree = bars + 5;       // logits read by the softmax (S buffer reusable)
-  uint64_t* pfull = bars + 6;
-  uint64_t* pvdone = bars + 7;
-  uint64_t* ofull = bars + 8;
+  uint64_t* pfull = bars + 5;       // P written by all softmax threads
+  uint64_t* pvdone = bars + 6;
+  uint64_t* ofull = bars + 7;
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kT64OffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile uint64_t* mask_s = reinterpret_cast<volatile uint64_t*>(sm + kT64OffMask);
   volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + kT64OffMask);
+  volatile float* red = reinterpret_cast<volatile float*>(sm + kT64OffRed);
+  volatile int* flags = reinterpret_cast<volatile int*>(sm + kT64OffFlag);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x & 1;
@@ -697,14 +760,14 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       mbar_init(&empty[i], 1);
     }
     mbar_init(sfull, 1);
-    mbar_init(sfree, 128);
-    mbar_init(pfull, 128);
+    mbar_init(pfull, kT64Softmax);
     mbar_init(pvdone, 1);
     mbar_init(ofull, 1);
+    for (int i = 0; i < 8; ++i) flags[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 8) {
+  if (warp == kT64Lead) {
     tmem_alloc(misc, kTmemCols);
     tmem_relinquish();
   }
@@ -712,47 +775,8 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // The producers start gathering tiles at once; warps 8-12 stage the query
-  // meanwhile (dims [256, 576) in shared memory, [0, 256) in TMEM) and meet at
-  // named barrier 1 before the first MMA.
-  constexpr uint32_t kQBar = 1, kQBarThreads = 5 * 32;
-  if (warp >= 8) {
-    const uint32_t qbase = smem_u32(sm + kT64OffQ);
-    constexpr int kChunks = (kDqk - kT64QTmemDims) / 8;
-    for (int i = threadIdx.x - 8 * 32; i < kH * kChunks; i += kQBarThreads) {
-      const int h = i / kChunks, ch = i % kChunks;
-      cp_async16(qbase + sw128_offset(h, ch, kH), qg + h * kDqk + kT64QTmemDims + ch * 8);
-    }
-    cp_async_commit();
-  }
-  if (warp >= 9) {
-    const int h = (warp & 3) * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
-#pragma unroll 1
-    for (int blk = 0; blk < kT64QTmemDims / 64; ++blk) {
-      uint32_t r[32];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint4 v = __ldg(qrow + blk * 8 + i);
-        r[4 * i] = v.x;
-        r[4 * i + 1] = v.y;
-        r[4 * i + 2] = v.z;
-        r[4 * i + 3] = v.w;
-      }
-      tmem_st32(tmem + lane_off + kT64ColQ + blk * 32, r);
-    }
-    tmem_st_wait();
-  }
-  if (warp >= 8) {
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    tc_fence_before();
-    named_bar_sync(kQBar, kQBarThreads);
-    tc_fence_after();
-  }
 
-  if (warp < 8) {
+  if (warp < kT64Lead) {
     // ------------------------------------------------ producers: group g = warp / 4 loads tiles
     // j = g mod 2 into stage g; warp w = warp % 4 copies tile rows [16w, 16w+16)
     const int grp = warp >> 2, pw = warp & 3;
@@ -786,6 +810,13 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       }
       const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFFFFu;
       if (j >= kT64Stages) {
+        // the stage is still busy: have L2 fetch this warp's 16 rows (9 lines of 128 B each) meanwhile
+#pragma unroll
+        for (int k = 0; k < (16 * 9 + 31) / 32; ++k) {
+          const int i = lane + 32 * k;
+          const int64_t prow = __shfl_sync(0xffffffffu, my_row, min(i / 9, 15));
+          if (i < 16 * 9 && prow >= 0) prefetch_l2(kv + prow * p.a.row_bytes + (i % 9) * 128);
+        }
         const bool ok = mbar_wait(&empty[st], ((j / kT64Stages) - 1) & 1, &g_status_attn, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
@@ -820,126 +851,110 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
     }
-  } else if (warp == 8) {
-    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
-    const uint64_t dq0 = make_sdesc(smem_u32(sm + kT64OffQ), 16, 1024, kLayoutSw128);
-    const uint64_t dk0 = make_sdesc(smem_u32(sm + kT64OffKV), 16, 1024, kLayoutSw128);
-    const uint64_t dv0 = make_sdesc(smem_u32(sm + kT64OffKV) + c * 4 * kBR64 * 128, kBR64 * 128, 1024, kLayoutSw128);
-    int next_s = 0, next_pv = 0;
-    uint32_t spins = 0;
-    uint64_t stall_t0 = 0;
-    while (next_pv < ntiles) {
-      bool progress = false;
-      // S_j needs tile j and the S buffer read by the softmax of tile j-1
-      const bool s_ready = next_s < ntiles &&
-                           (next_s == 0 || mbar_test_wait(smem_u32(sfree), (next_s - 1) & 1)) &&
-                           mbar_test_wait(smem_u32(&full[next_s % kT64Stages]), (next_s / kT64Stages) & 1);
-      if (__shfl_sync(0xffffffffu, s_ready, 0)) {
-        tc_fence_after();
-        const int j = next_s;
-        const uint64_t dk = dk0 + static_cast<uint64_t>(((j % kT64Stages) * kTile64Bytes) >> 4);
-        if (elect_one()) {
+  } else {
+    // ------------------------------------------------ softmax + epilogue (warps 8-15)
+    // The query: dims [320, 576) into shared memory (all 256 threads), dims
+    // [0, 320) into TMEM lane h (the pair splits the five 64-dim blocks 3 + 2).
+    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
+    const int hf = warp >= kT64Lead + 4 ? 1 : 0;
+    const int h = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const bool lead = warp == kT64Lead;
+    {
+      const uint32_t qbase = smem_u32(sm + kT64OffQ);
+      constexpr int kChunks = (kDqk - kT64QTmemDims) / 8;
+      for (int i = threadIdx.x - kT64Lead * 32; i < kH * kChunks; i += kT64Softmax) {
+        const int hh = i / kChunks, ch = i % kChunks;
+        cp_async16(qbase + sw128_offset(hh, ch, kH), qg + hh * kDqk + kT64QTmemDims + ch * 8);
+      }
+      cp_async_commit();
+      const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
+#pragma unroll 1
+      for (int blk = hf * 3; blk < (hf ? kT64QTmemDims / 64 : 3); ++blk) {
+        uint32_t r[32];
 #pragma unroll
-          for (int kk = 0; kk < kDqk / 16; ++kk) {
-            const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR64 * 128 + (kk & 3) * 32) >> 4);
-            const uint32_t acc = kk == 0 ? 0u : 1u;
-            if (kk < kT64QTmemDims / 16) {
-              umma_f16_tmem_a(tmem + kT64ColS, tmem + kT64ColQ + kk * 8, db, kIdescS64, acc);
-            } else {
-              const int qk = kk - kT64QTmemDims / 16;
-              const uint64_t da = dq0 + static_cast<uint64_t>(((qk >> 2) * kH * 128 + (qk & 3) * 32) >> 4);
-              umma_f16(tmem + kT64ColS, da, db, kIdescS64, acc);
-            }
-          }
+        for (int i = 0; i < 8; ++i) {
+          const uint4 v = __ldg(qrow + blk * 8 + i);
+          r[4 * i] = v.x;
+          r[4 * i + 1] = v.y;
+          r[4 * i + 2] = v.z;
+          r[4 * i + 3] = v.w;
+        }
+        tmem_st32(tmem + lane_off + kT64ColQ + blk * 32, r);
+      }
+      tmem_st_wait();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, kT64Softmax);
+      tc_fence_after();
+    }
+    // MMA descriptors (lead warp only; rebuilt where used to keep registers free)
+    const uint32_t q_smem = smem_u32(sm + kT64OffQ), kv_smem = smem_u32(sm + kT64OffKV);
+    bool ok = true;
+    if (lead && ntiles > 0) {
+      ok = mbar_wait(&full[0], 0, &g_status_attn, abort_flag);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        if (elect_one()) {
+          t64_issue_s(tmem, make_sdesc(q_smem, 16, 1024, kLayoutSw128), make_sdesc(kv_smem, 16, 1024, kLayoutSw128));
           umma_commit(sfull);
         }
         __syncwarp();
-        ++next_s;
-        progress = true;
-      }
-      const bool p_ready = next_pv < next_s && mbar_test_wait(smem_u32(pfull), next_pv & 1);
-      if (__shfl_sync(0xffffffffu, p_ready, 0)) {
-        tc_fence_after();
-        const int j = next_pv;
-        const uint64_t dv = dv0 + static_cast<uint64_t>(((j % kT64Stages) * kTile64Bytes) >> 4);
-        if (elect_one()) {
-#pragma unroll
-          for (int kk = 0; kk < kBR64 / 16; ++kk)
-            umma_f16_tmem_a(tmem + kT64ColO, tmem + kT64ColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
-                            kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(pvdone);
-          umma_commit(&empty[j % kT64Stages]);
-          if (j == ntiles - 1) umma_commit(ofull);
-        }
-        __syncwarp();
-        ++next_pv;
-        progress = true;
-      }
-      if (progress) {
-        stall_t0 = 0;
-      } else if ((++spins & 63u) == 0u) {
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-        if (stall_t0 == 0) {
-          stall_t0 = now;
-        } else if (now - stall_t0 > kWaitLimitNs) {
-          if (lane == 0) {
-            atomicOr(&g_status_attn, kDevTimeout);
-            *abort_flag = 1;
-          }
-          break;
-        }
       }
     }
-  } else {
-    // ------------------------------------------------ softmax + epilogue (warps 9-12)
-    const int quarter = warp & 3;
-    const int h = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t col_o = kT64ColO + hf * (kDvHalf / 2);
+    volatile float* my_red = red + hf * kH + h;
+    volatile float* their_red = red + (1 - hf) * kH + h;
+    volatile int* my_flag = flags + hf * 4 + quarter;
+    volatile int* their_flag = flags + (1 - hf) * 4 + quarter;
     const float sl2 = p.a.softmax_scale * kLog2e;
     float m = -INFINITY, l = 0.f, l32 = 0.f;
-    bool ok = true;
-    for (int j = 0; j < ntiles; ++j) {
+    for (int j = 0; ok && j < ntiles; ++j) {
       const int st = j % kT64Stages;
       ok = mbar_wait(sfull, j & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-      // the producer's row mask is ordered by its release on full[st] (still the
+      // the producers' row mask is ordered by their release on full[st] (still the
       // current phase: the stage is refilled only after this tile's P V)
       ok = mbar_wait(&full[st], (j / kT64Stages) & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t r0v[32], r1v[32];
-      tmem_ld32(tmem + lane_off + kT64ColS, r0v);
-      tmem_ld32(tmem + lane_off + kT64ColS + 32, r1v);
+      uint32_t sv[32];
+      tmem_ld32(tmem + lane_off + kT64ColS + hf * 32, sv);
       tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(sfree);
-      const uint64_t vmask = mask_s[st];
-      float x[64];
+      const uint32_t vmask = static_cast<uint32_t>(mask_s[st] >> (32 * hf));
+      float x[32];
       float mloc = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        x[i] = ((vmask >> i) & 1u) ? __uint_as_float(r0v[i]) * sl2 : -INFINITY;
-        x[32 + i] = ((vmask >> (32 + i)) & 1u) ? __uint_as_float(r1v[i]) * sl2 : -INFINITY;
-        mloc = fmaxf(mloc, fmaxf(x[i], x[32 + i]));
+        x[i] = ((vmask >> i) & 1u) ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
+        mloc = fmaxf(mloc, x[i]);
       }
+      // P V_{j-1} was issued before Q K^T_j, so it has completed (in-order
+      // completion) -- the wait documents and checks that; the partner has read
+      // the value exchanged for tile j-1 before its pfull arrival
       if (j >= 1) {
         ok = mbar_wait(pvdone, (j - 1) & 1, &g_status_attn, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
       }
-      const float m_new = fmaxf(m, mloc);
+      float mo;
+      if (!t64_pair_swap(my_red, their_red, my_flag, their_flag, j + 1, mloc, &mo, lane, abort_flag)) {
+        ok = false;
+        break;
+      }
+      const float m_new = fmaxf(m, fmaxf(mloc, mo));   // identical in both warps of the pair
       const bool need = m_new > m + kRescaleThreshold;
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
         const float f = need ? exp2f(m - m_new) : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kT64ColO + cc * 32, o);
+          tmem_ld32(tmem + lane_off + col_o + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tmem + lane_off + kT64ColO + cc * 32, o);
+          tmem_st32(tmem + lane_off + col_o + cc * 32, o);
         }
       }
       if (need) {
@@ -950,9 +965,9 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       }
       const float msub = (m == -INFINITY) ? 0.f : m;
       float psum = 0.f, psum32 = 0.f;
-      uint32_t pk[32];
+      uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
+      for (int i = 0; i < 16; ++i) {
         const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
         psum32 += p0 + p1;
         __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
@@ -962,30 +977,73 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       }
       l += psum;
       l32 += psum32;
-      tmem_st32(tmem + lane_off + kT64ColP, pk);
+      tmem_st16(tmem + lane_off + kT64ColP + hf * 16, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(pfull);
+      if (lead) {
+        // every softmax thread has written P_j (and read S_j): P V_j, then Q K^T_{j+1}
+        ok = mbar_wait(pfull, j & 1, &g_status_attn, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+        if (elect_one()) {
+          const uint64_t dv = make_sdesc(kv_smem + st * kTile64Bytes + c * 4 * kBR64 * 128, kBR64 * 128, 1024,
+                                         kLayoutSw128);
+#pragma unroll
+          for (int kk = 0; kk < kBR64 / 16; ++kk)
+            umma_f16_tmem_a(tmem + kT64ColO, tmem + kT64ColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                            kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(pvdone);
+          umma_commit(&empty[st]);
+          if (j == ntiles - 1) umma_commit(ofull);
+        }
+        __syncwarp();
+        if (j + 1 < ntiles) {
+          const int sn = (j + 1) % kT64Stages;
+          ok = mbar_wait(&full[sn], ((j + 1) / kT64Stages) & 1, &g_status_attn, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+          if (elect_one()) {
+            t64_issue_s(tmem, make_sdesc(q_smem, 16, 1024, kLayoutSw128),
+                        make_sdesc(kv_smem + sn * kTile64Bytes, 16, 1024, kLayoutSw128));
+            umma_commit(sfull);
+          }
+          __syncwarp();
+        }
+      }
     }
     if (ok) {
       ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
     }
+    // the pair's partial denominators (each warp summed its own columns); the
+    // exchange goes through the query tile's shared memory, idle once ofull fired
+    float lo = 0.f, l32o = 0.f;
+    if (ok) {
+      volatile float* fin = reinterpret_cast<volatile float*>(sm + kT64OffQ);
+      ok = t64_pair_swap(fin + hf * kH + h, fin + (1 - hf) * kH + h, my_flag, their_flag, ntiles + 1, l, &lo,
+                         lane, abort_flag);
+      if (ok)
+        ok = t64_pair_swap(fin + (2 + hf) * kH + h, fin + (3 - hf) * kH + h, my_flag, their_flag, ntiles + 2, l32,
+                           &l32o, lane, abort_flag);
+    }
     if (ok) {
       tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const float lse = l32 > 0.f ? (m + log2f(l32)) * kLn2 : -INFINITY;
+      const float lt = l + lo, l32t = l32 + l32o;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      const float lse = l32t > 0.f ? (m + log2f(l32t)) * kLn2 : -INFINITY;
       const int64_t th = static_cast<int64_t>(t) * kH + h;
-      // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB each
-      const uint32_t stg = smem_u32(sm + kT64OffKV) + quarter * 4096;
+      // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB per warp
+      const uint32_t stg = smem_u32(sm + kT64OffKV) + (hf * 4 + quarter) * 4096;
       const int64_t th0 = static_cast<int64_t>(t) * kH + quarter * 32;   // this warp's first head
+      const int col0 = c * kDvHalf + hf * (kDvHalf / 2);                 // first value dim it writes
       if (p.n_split == 1) {
-        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + c * kDvHalf);
+        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + col0);
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+        for (int cc = 0; cc < kDvHalf / 128; ++cc) {
           uint32_t o0[32], o1[32];
-          tmem_ld32(tmem + lane_off + kT64ColO + cc * 64, o0);
-          tmem_ld32(tmem + lane_off + kT64ColO + cc * 64 + 32, o1);
+          tmem_ld32(tmem + lane_off + col_o + cc * 64, o0);
+          tmem_ld32(tmem + lane_off + col_o + cc * 64 + 32, o1);
           tmem_ld_wait();
           uint32_t pk[32];
 #pragma unroll
@@ -995,28 +1053,28 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
           }
           warp_store_rows128(stg, pk, out + cc * 128, kDv * 2, lane);
         }
-        if (c == 0 && p.a.lse) p.a.lse[th] = lse;
+        if (c == 0 && hf == 0 && p.a.lse) p.a.lse[th] = lse;
       } else {
         const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
         uint8_t* out = reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<int64_t>(split) * p.seq.T * kH + th0) * kDv +
-                                                  c * kDvHalf);
+                                                  col0);
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
+        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kT64ColO + cc * 32, o);
+          tmem_ld32(tmem + lane_off + col_o + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
           warp_store_rows128(stg, o, out + cc * 128, kDv * 4, lane);
         }
-        if (c == 0) p.ws_lse[sth] = lse;
+        if (c == 0 && hf == 0) p.ws_lse[sth] = lse;
       }
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kT64Lead) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }

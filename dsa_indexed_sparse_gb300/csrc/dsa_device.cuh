@@ -214,6 +214,11 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
+// Asks L2 to fetch the line holding addr (no data returned to the SM).
+__device__ __forceinline__ void prefetch_l2(const void* addr) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
+}
+
 // ---------------------------------------------------------------- cp.async (16 B)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
