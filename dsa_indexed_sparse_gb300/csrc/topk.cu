@@ -12,14 +12,17 @@
 //    turned into order-preserving uint32 keys (-0.0 folded onto +0.0) and cached
 //    in that CTA's shared memory;
 //  * up to four 8-bit digit passes narrow the K-th largest key: every CTA builds
-//    the histogram of its slice (lanes that hit the same bucket combine their
-//    counts), the cluster's histograms are summed through distributed shared
-//    memory, and every CTA picks the same digit; a pass stops early when the
+//    the histogram of its slice (one private histogram per warp, four keys per
+//    thread per step, then summed), and after one cluster barrier every CTA sums the cluster's
+//    histograms through distributed shared memory and picks the same digit by
+//    itself (histograms alternate between two buffers, so a pass needs no second
+//    barrier before the next one overwrites them); a pass stops early when the
 //    bucket holding the K-th key is taken whole;
 //  * an ordered compaction keeps every key above the threshold and, in position
 //    order, the first `remaining` keys equal to it: cluster-wide prefix counts
-//    give each CTA its offsets, contiguous per-thread chunks (two block scans)
-//    give each thread its own, so the output comes out in ascending order.
+//    give each CTA its offsets, a scan over warps gives each warp (which owns a
+//    contiguous range) its own, and within a warp ballots over 32 consecutive
+//    keys give each lane its slot, so the output comes out in ascending order.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -39,7 +42,7 @@ namespace cg = cooperative_groups;
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxCluster = 8;
-constexpr int kSliceKeys = 4096;        // target history slice per CTA
+constexpr int kMinSliceKeys = 1024;     // smallest history slice worth a CTA
 constexpr int kCacheKeys = 48 * 1024;   // shared-memory key cache per CTA (192 KB)
 
 __device__ __forceinline__ uint32_t order_key(float f) {
@@ -81,23 +84,10 @@ __device__ __forceinline__ void warp_offsets(uint32_t warp_count, uint32_t* buf,
   *total = buf[kWarps];
 }
 
-// Exclusive block-wide scan of one value per thread.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* buf) {
-  const int lane = threadIdx.x & 31;
-  uint32_t inc = v;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += u;
-  }
-  uint32_t w_excl, tot;
-  warp_offsets(__shfl_sync(0xffffffffu, inc, 31), buf, &w_excl, &tot);
-  return w_excl + inc - v;
-}
-
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   extern __shared__ uint32_t keys_s[];
-  __shared__ uint32_t hist[256];        // this CTA's slice
+  __shared__ uint32_t hist2[2][256];    // this CTA's slice (pass parity)
+  __shared__ uint32_t whist[kWarps][256];   // per-warp partial histograms
   __shared__ uint32_t ghist[256];       // the cluster's sum
   __shared__ uint32_t scan_buf[kWarps + 1];
   __shared__ uint32_t s_digit, s_rem, s_bucket;
@@ -145,22 +135,41 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   uint32_t rem = static_cast<uint32_t>(K);  // how many of the keys matching `prefix` to keep
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += kThreads) hist[i] = 0;
+    // this buffer was last read by the cluster two passes ago, before the
+    // barrier of the previous pass
+    uint32_t* hist = hist2[pass & 1];
+    {
+      uint32_t* wflat = &whist[0][0];
+      for (int i = tid; i < kWarps * 256; i += kThreads) wflat[i] = 0;
+    }
     __syncthreads();
-    for (int base = 0; base < len; base += kThreads) {
-      const int i = base + tid;
-      bool act = false;
-      uint32_t k = 0;
-      if (i < len) {
-        k = key_at(i);
-        act = (k & pmask) == prefix;
+    {
+      uint32_t* wh = whist[tid >> 5];
+      auto count = [&](uint32_t k) {
+        if ((k & pmask) == prefix) atomicAdd(&wh[(k >> shift) & 255u], 1u);
+      };
+      const int n4 = len >> 2;
+      for (int q = tid; q < n4; q += kThreads) {
+        uint4 k4;
+        if (cached) {
+          k4 = reinterpret_cast<const uint4*>(keys_s)[q];
+        } else {
+          const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
+          k4 = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+        }
+        count(k4.x);
+        count(k4.y);
+        count(k4.z);
+        count(k4.w);
       }
-      const uint32_t active = __ballot_sync(0xffffffffu, act);
-      if (act) {
-        const uint32_t bin = (k >> shift) & 255u;
-        const uint32_t peers = __match_any_sync(active, bin);
-        if (lane == __ffs(peers) - 1) atomicAdd(&hist[bin], static_cast<uint32_t>(__popc(peers)));
-      }
+      for (int i = 4 * n4 + tid; i < len; i += kThreads) count(key_at(i));
+    }
+    __syncthreads();
+    for (int b = tid; b < 256; b += kThreads) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) v += whist[w][b];
+      hist[b] = v;
     }
     cluster.sync();  // every slice's histogram complete
     for (int i = tid; i < 256; i += kThreads) {
@@ -197,7 +206,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
         }
       }
     }
-    cluster.sync();  // peers are done reading `hist`; s_* visible in this CTA
+    __syncthreads();  // s_* visible in this CTA
     prefix |= s_digit << shift;
     pmask |= 255u << shift;
     rem = s_rem;
@@ -206,33 +215,27 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     if (whole) break;  // cluster-uniform (same histogram everywhere)
   }
 
-  // Ordered compaction.  Thread `tid` owns slice positions [tid*c, tid*c + c),
-  // c odd (the shared-memory reads of a warp fall in distinct banks).
-  int c = (len + kThreads - 1) / kThreads;
-  c |= 1;
-  const int tlo = min(len, tid * c), thi = min(len, tlo + c);
+  // Ordered compaction.  Warp w owns slice positions [w*wl, w*wl + wl), wl a
+  // multiple of 32, and walks them 32 at a time.
+  const int warp = tid >> 5;
+  const int wl = ((len + kWarps - 1) / kWarps + 31) & ~31;
+  const int wlo = min(len, warp * wl), whi = min(len, wlo + wl);
+  const uint32_t lt_mask = (1u << lane) - 1u;
   uint32_t n_eq = 0, n_gt = 0;
-  for (int i = tlo; i < thi; ++i) {
-    const uint32_t km = key_at(i) & pmask;
-    n_eq += km == prefix;
-    n_gt += km > prefix;
+  for (int b = wlo; b < whi; b += 32) {
+    const int i = b + lane;
+    const uint32_t km = i < whi ? (key_at(i) & pmask) : 0u;
+    const bool in = i < whi;
+    n_eq += __popc(__ballot_sync(0xffffffffu, in && km == prefix));
+    n_gt += __popc(__ballot_sync(0xffffffffu, in && km > prefix));
   }
-  uint32_t eq_rank = block_excl_scan(n_eq, scan_buf);  // rank within this slice
-  const uint32_t slice_eq = scan_buf[kWarps];
+  uint32_t eq_w, slice_eq, gt_w, slice_gt;
+  warp_offsets(n_eq, scan_buf, &eq_w, &slice_eq);
   __syncthreads();
-  const uint32_t gt_total = [&] {
-    uint32_t v = n_gt;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-  }();
-  if (lane == 0) scan_buf[tid >> 5] = gt_total;
-  __syncthreads();
+  warp_offsets(n_gt, scan_buf, &gt_w, &slice_gt);
   if (tid == 0) {
-    uint32_t g = 0;
-    for (int w = 0; w < kWarps; ++w) g += scan_buf[w];
     s_counts[0] = slice_eq;
-    s_counts[1] = g;
+    s_counts[1] = slice_gt;
   }
   cluster.sync();  // every slice's counts visible cluster-wide
   // Earlier slices: their keys equal to the threshold (for this slice's ranks)
@@ -244,33 +247,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     sel_before += g + (eq_before >= rem ? 0u : min(e, rem - eq_before));
     eq_before += e;
   }
-  eq_rank += eq_before;
-  uint32_t n_sel = 0;
-  {
-    uint32_t r = eq_rank;
-    for (int i = tlo; i < thi; ++i) {
-      const uint32_t km = key_at(i) & pmask;
-      if (km > prefix) {
-        ++n_sel;
-      } else if (km == prefix) {
-        n_sel += r < rem;
-        ++r;
-      }
-    }
-  }
-  __syncthreads();
-  uint32_t pos = sel_before + block_excl_scan(n_sel, scan_buf);
-  for (int i = tlo; i < thi && n_sel > 0; ++i) {
-    const uint32_t km = key_at(i) & pmask;
-    bool sel = km > prefix;
-    if (km == prefix) {
-      sel = eq_rank < rem;
-      ++eq_rank;
-    }
-    if (sel) {
-      out[pos++] = lo + i;
-      --n_sel;
-    }
+  // this warp's first equal-key rank and first output slot
+  uint32_t eq_rank = eq_before + eq_w;
+  uint32_t pos = sel_before + gt_w + (eq_before >= rem ? 0u : min(eq_w, rem - eq_before));
+  for (int b = wlo; b < whi; b += 32) {
+    const int i = b + lane;
+    const bool in = i < whi;
+    const uint32_t km = in ? (key_at(i) & pmask) : 0u;
+    const bool eq = in && km == prefix;
+    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
+    const bool sel = (in && km > prefix) || (eq && eq_rank + __popc(eqm & lt_mask) < rem);
+    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
+    if (sel) out[pos + __popc(selm & lt_mask)] = lo + i;
+    eq_rank += __popc(eqm);
+    pos += __popc(selm);
   }
   cluster.sync();  // peers may still read s_counts
 }
@@ -283,7 +273,13 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
     *plan += "topk[empty]";
     return cudaSuccess;
   }
-  const int cl = std::max(1, std::min(kMaxCluster, (seq.max_ctx + kSliceKeys - 1) / kSliceKeys));
+  // Enough CTAs to cover the GPU (a small batch splits each history over a
+  // cluster), no more than the history can feed, and enough to keep a slice
+  // within the shared-memory key cache when the cluster can.
+  const int want = (std::max(1, env.num_sms) + seq.T - 1) / seq.T;
+  const int feed = std::max(1, seq.max_ctx / kMinSliceKeys);
+  const int fit = (seq.max_ctx + kCacheKeys - 1) / kCacheKeys;
+  const int cl = std::max(1, std::min(kMaxCluster, std::max(std::min(want, feed), fit)));
   const int slice = ((seq.max_ctx + cl - 1) / cl + 3) & ~3;
   const bool cached = slice <= kCacheKeys;
   const size_t smem = cached ? static_cast<size_t>(slice) * 4 : 0;

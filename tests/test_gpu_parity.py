@@ -2,6 +2,8 @@
 seeded inputs spanning several tiles, ragged tails and the edge cases of the
 method (history shorter than / equal to / one more than K, one-token history,
 shuffled pages, query groups of 1, 2 and 4)."""
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -153,7 +155,8 @@ def test_topk_long_history_cluster_and_uncached(dev):
     L = 70000
     scores = np.stack([rng.standard_normal(L), rng.integers(0, 50, L).astype(np.float64)]).astype(np.float32)
     plan = _topk_run(dev, scores, [L - 1, 60001], 2048)
-    assert "cluster=8,smem" in plan, plan
+    m = re.search(r"cluster=(\d+),smem", plan)
+    assert m and int(m.group(1)) > 1, plan
     L = 400000
     scores = np.stack([rng.standard_normal(L), rng.integers(0, 9, L).astype(np.float64)]).astype(np.float32)
     plan = _topk_run(dev, scores, [L - 1, 390001], 2048)
