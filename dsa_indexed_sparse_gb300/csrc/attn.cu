@@ -88,6 +88,7 @@ __device__ __forceinline__ float block_reduce_sum(float v, float* buf) {
 
 __global__ void __launch_bounds__(kGenThreads)
     attn_generic_kernel(SeqArgs seq, MlaArgs a) {
+  grid_dep_wait();
   extern __shared__ float sm_gen[];
   const int dqk = a.d_latent + a.d_rope, dv = a.d_latent, K = a.K;
   float* qs = sm_gen;                                            // [dqk]
@@ -215,6 +216,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
 template <bool kFp8>
 __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
   using C = AttnCfg<kFp8>;
+  grid_dep_wait();
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
@@ -615,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
     }
   }
 
+  grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   tc_fence_before();
   __syncthreads();
   if (warp == 8) {
@@ -718,6 +721,7 @@ __device__ __forceinline__ bool t64_pair_swap(volatile float* mine, volatile flo
 }
 
 __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams p) {
+  grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -1072,6 +1076,7 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
     }
   }
 
+  grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   tc_fence_before();
   __syncthreads();
   if (warp == kT64Lead) {
@@ -1088,6 +1093,7 @@ constexpr int kCombineHeads = 8;
 __global__ void __launch_bounds__(256)
     attn_combine_kernel(const float* ws_o, const float* ws_lse, int n_split, int T,
                         __nv_bfloat16* out, float* lse_out) {
+  grid_dep_wait();
   extern __shared__ float wts[];  // [kCombineHeads][n_split]
   constexpr int H = kH, kV4 = kDv / 4 / 32;   // float4 per lane
   const int t = blockIdx.x;
@@ -1222,9 +1228,12 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = seq.T * split * 2;
     if (fp8) {
-      attn_tc_kernel<true><<<grid, kThreads, AttnCfg<true>::kSmemBytes, env.stream>>>(p);
+      const cudaError_t le =
+          launch_kernel(attn_tc_kernel<true>, dim3(grid), dim3(kThreads), AttnCfg<true>::kSmemBytes, env.stream, true, 1, p);
+      if (le != cudaSuccess) return le;
     } else {
-      attn_tc64_kernel<<<grid, kT64Threads, kT64SmemBytes, env.stream>>>(p);
+      const cudaError_t le = launch_kernel(attn_tc64_kernel, dim3(grid), dim3(kT64Threads), kT64SmemBytes, env.stream, true, 1, p);
+      if (le != cudaSuccess) return le;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -1233,8 +1242,10 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     *plan += buf;
     if (split > 1) {
       const size_t smem = static_cast<size_t>(split) * kCombineHeads * sizeof(float);
-      attn_combine_kernel<<<dim3(seq.T, kH / kCombineHeads), 256, smem, env.stream>>>(
-          p.ws_o, p.ws_lse, split, seq.T, static_cast<__nv_bfloat16*>(a.out), a.lse);
+      e = launch_kernel(attn_combine_kernel, dim3(seq.T, kH / kCombineHeads), dim3(256), smem, env.stream, true, 1,
+                     static_cast<const float*>(p.ws_o), static_cast<const float*>(p.ws_lse), split, seq.T,
+                     static_cast<__nv_bfloat16*>(a.out), a.lse);
+      if (e != cudaSuccess) return e;
       *plan += "+attn_combine";
       e = cudaGetLastError();
     }
@@ -1251,7 +1262,8 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     cudaFuncSetAttribute(attn_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
   dim3 grid(a.H, seq.T);
-  attn_generic_kernel<<<grid, kGenThreads, smem, env.stream>>>(seq, a);
+  const cudaError_t le = launch_kernel(attn_generic_kernel, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
+  if (le != cudaSuccess) return le;
   *plan += "attn_generic";
   return cudaGetLastError();
 }

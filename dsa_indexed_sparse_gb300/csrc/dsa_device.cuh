@@ -214,6 +214,15 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
+// Programmatic dependent launch.  grid_dep_wait blocks until every grid this
+// launch depends on has completed and its writes are visible (at once when the
+// kernel was launched without programmatic stream serialization); nothing that
+// an earlier kernel may write -- inputs included -- is read before it.
+// grid_dep_launch lets the next kernel on the stream launch now, so that its
+// launch and set-up overlap this grid's tail.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Asks L2 to fetch the line holding addr (no data returned to the SM).
 __device__ __forceinline__ void prefetch_l2(const void* addr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(addr));
@@ -222,6 +231,11 @@ __device__ __forceinline__ void prefetch_l2(const void* addr) {
 // ---------------------------------------------------------------- cp.async (16 B)
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrives on the mbarrier once all of this thread's earlier cp.async copies have
+// landed (the arrival is counted in the barrier's expected count: .noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() {
   asm volatile("cp.async.commit_group;" ::: "memory");

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include <string>
+#include <utility>
 
 namespace dsa {
 
@@ -71,6 +72,38 @@ size_t attn_workspace_bytes(const SeqArgs& seq, const MlaArgs& a, int num_sms);
 cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, size_t ws_bytes,
                         const LaunchEnv& env, std::string* plan, bool* unsupported,
                         std::string* why);
+
+// Launches a kernel, when `pdl` with programmatic stream serialization (it
+// may launch while the previous kernel on the stream is finishing; every
+// kernel of this library waits for its predecessor with griddepcontrol.wait
+// before reading anything), and when cluster > 1 as clusters of `cluster` CTAs
+// along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                          bool pdl, int cluster, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  int n = 0;
+  if (pdl) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Sets the text dsa_last_error() returns on the calling thread.
 void set_last_error(const std::string& msg);

@@ -13,8 +13,10 @@
 //  * indexer_tc_kernel<G> -- the tensor-core path (FP8 e4m3, H_I = 64, D_I = 128,
 //    64-token pages).  Swap-AB tcgen05 GEMM: the 128 keys of a tile are the M
 //    rows (TMEM lanes), the G queries x 64 heads of a query group are the N
-//    columns, K = 128.  Keys arrive page by page through TMA (128-byte swizzle),
-//    accumulators live in TMEM (double buffered) and 4 epilogue warps turn each
+//    columns, K = 128.  Keys arrive page by page through TMA (128-byte swizzle)
+//    and their per-key scales through one warp-wide cp.async per tile (a TMA op
+//    costs ~0.1 us of issue time on this GPU, which paced the whole ring when
+//    the scales took two more); accumulators live in TMEM (double buffered) and 4 epilogue warps turn each
 //    key's row of G*64 dot products into G scores with an in-thread head sum.
 //    Persistent: every CTA takes an equal contiguous share of the (group, key
 //    tile) list, computed on the device from q_pos.
@@ -37,6 +39,7 @@ constexpr int kGenThreads = 256;
 template <bool kE4M3>
 __global__ void __launch_bounds__(kGenThreads)
     indexer_generic_kernel(SeqArgs seq, IndexerArgs a) {
+  grid_dep_wait();
   extern __shared__ float sm_gen[];
   float* qf = sm_gen;                   // [H_I * D_I] query codes (as float)
   float* wq = sm_gen + a.H_I * a.D_I;  // [H_I] w * q_scale
@@ -173,6 +176,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap, TcParams p) {
   using C = TcCfg<G>;
+  grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
@@ -234,8 +238,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   // ---- barriers and TMEM -------------------------------------------------
   if (threadIdx.x == 0) {
+    // full: the producer's expect_tx arrival, plus one cp.async arrival per lane
+    // of the producer warp when the keys carry scales
+    const uint32_t full_count = 1u + (p.a.k_scale != nullptr ? 32u : 0u);
     for (int i = 0; i < kTcStages; ++i) {
-      mbar_init(&full[i], 1);
+      mbar_init(&full[i], full_count);
       // freed by the MMA (keys read) and by the epilogue (key scales read)
       mbar_init(&empty[i], 1 + kTcEpiThreads);
     }
@@ -315,21 +322,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) {
-        const bool scaled = p.a.k_scale != nullptr;
-        const uint32_t per_page = C::kStageBytes / 2 + (scaled ? kTcPage * 4 : 0);
+        constexpr uint32_t per_page = C::kStageBytes / 2;
         valid_s[st] = (pid0 >= 0 ? 1u : 0u) | (pid1 >= 0 ? 2u : 0u);
         mbar_arrive_expect_tx(&full[st], (pid0 >= 0 ? per_page : 0u) + (pid1 >= 0 ? per_page : 0u));
         uint8_t* dst = sm + C::kOffStages + st * C::kStageBytes;
-        float* sdst = scale_s + st * kTcKeys;
-        if (pid0 >= 0) {
-          tma_load_2d(dst, &kmap, &full[st], 0, pid0 * kTcPage);
-          if (scaled) bulk_load(sdst, p.a.k_scale + static_cast<int64_t>(pid0) * kTcPage, kTcPage * 4, &full[st]);
-        }
-        if (pid1 >= 0) {
-          tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid1 * kTcPage);
-          if (scaled)
-            bulk_load(sdst + kTcPage, p.a.k_scale + static_cast<int64_t>(pid1) * kTcPage, kTcPage * 4, &full[st]);
-        }
+        if (pid0 >= 0) tma_load_2d(dst, &kmap, &full[st], 0, pid0 * kTcPage);
+        if (pid1 >= 0) tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid1 * kTcPage);
+      }
+      if (p.a.k_scale != nullptr) {
+        // lanes 0-15: the 64 scales of the first page, lanes 16-31: the second (16 B each)
+        const int half = lane >> 4;
+        const int32_t pid = half ? pid1 : pid0;
+        if (pid >= 0)
+          cp_async16(smem_u32(scale_s + st * kTcKeys + half * kTcPage + (lane & 15) * 4),
+                     p.a.k_scale + static_cast<int64_t>(pid) * kTcPage + (lane & 15) * 4);
+        cp_async_mbar_arrive(&full[st]);
       }
     }
   } else if (warp == 1) {
@@ -451,24 +458,34 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tmem_ld32(col, v0);
         tmem_ld32(col + 32, v1);
         tmem_ld_wait();
-        float acc0 = 0.f, acc1 = 0.f;
+        // head weights as 16-byte broadcast loads; four independent sums
+        const float4* w4 = reinterpret_cast<const float4*>(wq + j * kTcHeads);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          acc0 = fmaf(wq[j * kTcHeads + i], fmaxf(__uint_as_float(v0[i]), 0.f), acc0);
-          acc1 = fmaf(wq[j * kTcHeads + i + 1], fmaxf(__uint_as_float(v0[i + 1]), 0.f), acc1);
+        for (int i = 0; i < 8; ++i) {
+          const float4 wv = w4[i];
+          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v0[4 * i]), 0.f), acc[0]);
+          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v0[4 * i + 1]), 0.f), acc[1]);
+          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v0[4 * i + 2]), 0.f), acc[2]);
+          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v0[4 * i + 3]), 0.f), acc[3]);
         }
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          acc0 = fmaf(wq[j * kTcHeads + 32 + i], fmaxf(__uint_as_float(v1[i]), 0.f), acc0);
-          acc1 = fmaf(wq[j * kTcHeads + 33 + i], fmaxf(__uint_as_float(v1[i + 1]), 0.f), acc1);
+        for (int i = 0; i < 8; ++i) {
+          const float4 wv = w4[8 + i];
+          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v1[4 * i]), 0.f), acc[0]);
+          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v1[4 * i + 1]), 0.f), acc[1]);
+          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v1[4 * i + 2]), 0.f), acc[2]);
+          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v1[4 * i + 3]), 0.f), acc[3]);
         }
-        if (key_ok && s <= qp[j]) p.a.scores[static_cast<int64_t>(tq[j]) * p.a.ld + s] = (acc0 + acc1) * sk;
+        const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        if (key_ok && s <= qp[j]) p.a.scores[static_cast<int64_t>(tq[j]) * p.a.ld + s] = sum * sk;
       }
       tc_fence_before();
       mbar_arrive(&accempty[ab]);
     }
   }
 
+  grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -500,7 +517,9 @@ cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv&
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  indexer_tc_kernel<G><<<grid, kTcThreads, C::kSmemBytes, env.stream>>>(kmap, qmap, p);
+  const cudaError_t le = launch_kernel(indexer_tc_kernel<G>, dim3(grid), dim3(kTcThreads), C::kSmemBytes, env.stream, true, 1,
+                                    kmap, qmap, p);
+  if (le != cudaSuccess) return le;
   char buf[160];
   snprintf(buf, sizeof(buf), "indexer_tc<G=%d>[grid=%d,tiles<=%lld]", G, grid,
            static_cast<long long>(tiles_ub));
@@ -537,12 +556,14 @@ cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const Launc
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(indexer_generic_kernel<true>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    indexer_generic_kernel<true><<<grid, kGenThreads, smem, env.stream>>>(seq, a);
+    const cudaError_t le = launch_kernel(indexer_generic_kernel<true>, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
+    if (le != cudaSuccess) return le;
   } else {
     if (smem > 48 * 1024)
       cudaFuncSetAttribute(indexer_generic_kernel<false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    indexer_generic_kernel<false><<<grid, kGenThreads, smem, env.stream>>>(seq, a);
+    const cudaError_t le = launch_kernel(indexer_generic_kernel<false>, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
+    if (le != cudaSuccess) return le;
   }
   *plan += a.e4m3 ? "indexer_generic<e4m3>" : "indexer_generic<f32>";
   return cudaGetLastError();

@@ -85,6 +85,7 @@ __device__ __forceinline__ void warp_offsets(uint32_t warp_count, uint32_t* buf,
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
+  grid_dep_wait();
   extern __shared__ uint32_t keys_s[];
   __shared__ uint32_t hist2[2][256];    // this CTA's slice (pass parity)
   __shared__ uint32_t whist[kWarps][256];   // per-warp partial histograms
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     eq_rank += __popc(eqm);
     pos += __popc(selm);
   }
+  grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   cluster.sync();  // peers may still read s_counts
 }
 
@@ -291,19 +293,7 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
   });
   if (attr_err != cudaSuccess) return attr_err;
   TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, cached ? slice : 0};
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(seq.T * cl);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = env.stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, topk_kernel, a);
+  cudaError_t e = launch_kernel(topk_kernel, dim3(seq.T * cl), dim3(kThreads), smem, env.stream, /*pdl=*/false, cl, a);
   char buf[96];
   snprintf(buf, sizeof(buf), "topk_radix[cluster=%d,%s]", cl, cached ? "smem" : "global");
   *plan += buf;
