@@ -215,6 +215,33 @@ def host_cores():
 
 # ----------------------------------------------------------------------------- main
 
+def profile_stage(torch, dsa, W, wl, dev, stage, reps):
+    """Runs one stage `reps` times on one copy of the workload (its inputs made by
+    the stages before it), for profiler captures of a single kernel."""
+    d = W.device_tensors(wl, dev)
+    seq, idxr, mla = dsa.Seq(**d["seq"]), dsa.Indexer(**d["indexer"]), dsa.Mla(**d["mla"])
+    ld = (wl.max_ctx + 3) // 4 * 4
+    scores = torch.empty((wl.T, ld), dtype=torch.float32, device=dev)
+    sel = torch.empty((wl.T, wl.K), dtype=torch.int32, device=dev)
+    out = torch.empty((wl.T, wl.H, wl.d_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.T, wl.H), dtype=torch.float32, device=dev)
+    attn_ws = torch.empty(max(16, dsa.sparse_mla_attn_workspace_size(seq, mla, wl.K)), dtype=torch.uint8, device=dev)
+    ws = torch.empty(dsa.decode_workspace_size(seq, idxr, mla, wl.K), dtype=torch.uint8, device=dev)
+    fns = {"indexer": lambda: dsa.indexer_scores(seq, idxr, scores),
+           "topk": lambda: dsa.topk(seq, scores, wl.K, sel),
+           "attn": lambda: dsa.sparse_mla_attn(seq, mla, sel, wl.K, out, lse=lse, workspace=attn_ws),
+           "step": lambda: dsa.decode_step(seq, idxr, mla, wl.K, out, ws, lse=lse)}
+    for name in ("indexer", "topk", "attn"):   # the inputs of the profiled stage
+        fns[name]()
+    torch.cuda.synchronize()
+    for _ in range(reps):
+        fns[stage]()
+    torch.cuda.synchronize()
+    dsa.check_status()
+    print(f"profiled {stage} x{reps} on {wl.name}: {dsa.last_plan()}")
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -224,6 +251,10 @@ def main():
     ap.add_argument("--workload", default="decode_b1", choices=sorted(DESCRIPTIONS))
     ap.add_argument("--oracle-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--stage", choices=["indexer", "topk", "attn", "step"], default=None,
+                    help="profiling mode: run this stage --reps times on one input copy and exit "
+                         "(no timing, no JSON line); for ncu captures")
+    ap.add_argument("--reps", type=int, default=3)
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -265,6 +296,8 @@ def main():
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
     wl = W.make(args.workload, seed=0)
+    if args.stage:
+        return profile_stage(torch, dsa, W, wl, dev, args.stage, args.reps)
     alg = algorithmic(wl)
     copies_n = max(1, min(64, math.ceil(2 * L2_BYTES / max(alg["step_bytes"], 1)) + 1))
     default_steps = {"decode_b1": 20000, "decode_b64": 2000, "decode_b4_long": 5000, "prefill_16k": 10}
