@@ -627,117 +627,95 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 rows, 64-row tiles.
+// bf16 rows, 48-row tiles, three stages.
 //
-// Producers (warps 0-7): two groups of four warps own one stage each and load
-// alternate tiles (16 rows per warp).  Lanes resolve the rows (index -> page ->
-// cache row) as soon as the group's previous tile has landed, about one
-// tile-time before the stage frees, and ask L2 to fetch those rows right away;
-// once the stage is free every lane copies its fixed 16-byte chunks of each row
-// with cp.async into the 128B-swizzled K-major tile (the row loop is unrolled
-// so the swizzle is a constant per row), now mostly from L2; rows that select
-// nothing are zeroed.  (On this GPU a tile::gather4 TMA producer reached ~12
-// GB/s per SM and cp.async gathers ~60 GB/s.)
+// Producers (warps 0-8): three groups of three warps own one stage each and
+// load every third tile (16 rows per warp; a warp issues cp.async copies at
+// ~30 ns per instruction here, so the warps per tile set how fast it lands).  Lanes resolve the rows (index -> page
+// -> cache row) as soon as the group's previous tile has landed and ask L2 to
+// fetch them; once the stage is free every lane copies its fixed 16-byte
+// chunks of each row with cp.async into the 128B-swizzled K-major tile; rows
+// that select nothing are zeroed.  (On this GPU a tile::gather4 TMA producer
+// reached ~12 GB/s per SM and cp.async gathers ~60 GB/s.)
 //
-// Softmax (warps 8-15): two warps per TMEM lane quarter; warp half hf takes
-// logit columns [32 hf, 32 hf + 32) and output columns [128 hf, 128 hf + 128),
-// and the pair agrees on the running max each tile through a shared-memory
-// value and a sequence flag (bounded spin).  One warp (the lead, warp 8) also
-// issues the MMAs, in the order P V_j then Q K^T_{j+1}, right after P_j is
-// complete: P V then never queues behind a whole Q K^T (it frees the stage
-// sooner), and the softmax never waits for the previous P V.
+// MMA warp (warp 9): Q K^T_{j+1} (N = 48 rows) as soon as the softmax has read
+// S_j and tile j+1 has landed, so it runs during the softmax of tile j; P V_j
+// (N = 256 value dims, P read from TMEM) as soon as P_j is written.  An M=128
+// K=16 step whose A operand (the query) sits in shared memory reads 6 KB of
+// shared memory and takes ~53 clk, one with A in TMEM ~36 clk, so the first 320
+// query dims live in TMEM.
 //
-// Q K^T runs with N = 64 rows, P V with N = 256 value dims and P read from
-// TMEM.  An M=128 K=16 step whose A operand (the query) sits in shared memory
-// reads 6 KB of shared memory and takes ~53 clk, one with A in TMEM ~36 clk, so
-// the first 320 query dims live in TMEM.  TMEM: S [0,64), P [64,96), Q
-// [96,256), O [256,512).  Two tiles of 72 KB are in flight.
-constexpr int kBR64 = 64;
-constexpr int kTile64Bytes = kBR64 * kDqk * 2;                 // 73728
-constexpr int kT64Stages = 2;
-constexpr int kT64QTmemDims = 320;
-constexpr int kT64QTmemSteps = kT64QTmemDims / 16;             // 20
-constexpr int kT64QSmemAtoms = (kDqk - kT64QTmemDims) / 64;    // 4
-constexpr int kT64OffQ = 0;
-constexpr int kT64OffKV = kT64QSmemAtoms * kH * 128;           // 65536
-constexpr int kT64OffMask = kT64OffKV + kT64Stages * kTile64Bytes;  // uint64 [stages]
-constexpr int kT64OffRed = kT64OffMask + 16;                   // float [2 halves][128 heads]
-constexpr int kT64OffFlag = kT64OffRed + 2 * kH * 4;           // int [2 halves][4 quarters]
-constexpr int kT64OffBar = kT64OffFlag + 32;
-// barriers: full[2], empty[2], sfull, pfull, pvdone, ofull
-constexpr int kT64NumBars = 2 * kT64Stages + 4;
-constexpr int kT64OffMisc = kT64OffBar + kT64NumBars * 8;
-constexpr int kT64SmemBytes = kT64OffMisc + 16 + 1024;
-// 16 warps: 4 per SM sub-partition, so 128 registers a thread
-constexpr int kT64Threads = 512;   // warps 0-7 producers, warps 8-15 softmax (warp 8 also issues MMAs)
-constexpr int kT64Lead = 8;
-constexpr int kT64Softmax = 256;
-constexpr uint32_t kT64ColS = 0, kT64ColP = 64, kT64ColQ = 96, kT64ColO = 256;
-constexpr uint32_t kIdescS64 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR64);
-static_assert(kT64ColQ + kT64QTmemDims / 2 <= kT64ColO, "TMEM plan");
-static_assert(kT64SmemBytes <= 232448, "shared memory budget");
+// Softmax (warps 10-13): one thread per head (its TMEM lane), 48 logits a tile,
+// running max moved (and O rescaled in TMEM) only when it grows by more than
+// 2^8.
+//
+// TMEM: S [0,48), P [64,88), Q [96,256), O [256,512).  Shared memory: query
+// dims [320, 576) (64 KB) + three 54 KB tiles.  (A dedicated MMA warp issuing
+// Q K^T_{j+1} during softmax_j hides the softmax; the third stage hides the
+// gather of a tile behind the work on the other two.)
+constexpr int kBR48 = 48;
+constexpr int kTile48Bytes = kBR48 * kDqk * 2;                 // 55296
+constexpr int kT48Stages = 3;
+constexpr int kT48QTmemDims = 320;
+constexpr int kT48QTmemSteps = kT48QTmemDims / 16;             // 20
+constexpr int kT48QSmemAtoms = (kDqk - kT48QTmemDims) / 64;    // 4
+constexpr int kT48OffQ = 0;
+constexpr int kT48OffKV = kT48QSmemAtoms * kH * 128;           // 65536
+constexpr int kT48OffMask = kT48OffKV + kT48Stages * kTile48Bytes;  // uint16 [stages][4]
+constexpr int kT48OffBar = kT48OffMask + kT48Stages * 4 * 2 + 8;
+// barriers: full[3], empty[3], sfull, sfree, pfull, pvdone, ofull
+constexpr int kT48NumBars = 2 * kT48Stages + 5;
+constexpr int kT48OffMisc = kT48OffBar + kT48NumBars * 8;
+constexpr int kT48Used = kT48OffMisc + 16;                     // bytes used from the aligned base
+// the dynamic shared-memory base is re-aligned to 1024 B inside the kernel; this
+// much slack is requested for it (the kernel checks that it sufficed)
+constexpr int kT48Slack = 232448 - kT48Used;
+constexpr int kT48SmemBytes = kT48Used + kT48Slack;
+constexpr int kT48Threads = 448;   // warps 0-8 producers, warp 9 MMA, warps 10-13 softmax
+constexpr int kT48Mma = 9;
+constexpr int kT48Producers = 3;   // warps per stage group
+constexpr uint32_t kT48ColS = 0, kT48ColP = 64, kT48ColQ = 96, kT48ColO = 256;
+constexpr uint32_t kIdescS48 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR48);
+static_assert(kT48ColQ + kT48QTmemDims / 2 <= kT48ColO, "TMEM plan");
+static_assert(kT48ColP + kBR48 / 2 <= kT48ColQ && kT48ColS + kBR48 <= kT48ColP, "TMEM plan");
+static_assert(kT48Slack >= 128, "shared memory budget");
 
-// Q K^T of one tile (elected lane of the lead warp).
-__device__ __forceinline__ void t64_issue_s(uint32_t tmem, uint64_t dq0, uint64_t dk) {
+// Q K^T of one 48-row tile (elected lane of the MMA warp).
+__device__ __forceinline__ void t48_issue_s(uint32_t tmem, uint64_t dq0, uint64_t dk) {
 #pragma unroll
   for (int kk = 0; kk < kDqk / 16; ++kk) {
-    const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR64 * 128 + (kk & 3) * 32) >> 4);
+    const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR48 * 128 + (kk & 3) * 32) >> 4);
     const uint32_t acc = kk == 0 ? 0u : 1u;
-    if (kk < kT64QTmemSteps) {
-      umma_f16_tmem_a(tmem + kT64ColS, tmem + kT64ColQ + kk * 8, db, kIdescS64, acc);
+    if (kk < kT48QTmemSteps) {
+      umma_f16_tmem_a(tmem + kT48ColS, tmem + kT48ColQ + kk * 8, db, kIdescS48, acc);
     } else {
-      const int qk = kk - kT64QTmemSteps;
+      const int qk = kk - kT48QTmemSteps;
       const uint64_t da = dq0 + static_cast<uint64_t>(((qk >> 2) * kH * 128 + (qk & 3) * 32) >> 4);
-      umma_f16(tmem + kT64ColS, da, db, kIdescS64, acc);
+      umma_f16(tmem + kT48ColS, da, db, kIdescS48, acc);
     }
   }
 }
 
-// Exchanges one value per head with the partner warp of the pair: write own
-// value, publish sequence number `seq`, spin (bounded) on the partner's.
-__device__ __forceinline__ bool t64_pair_swap(volatile float* mine, volatile float* theirs, volatile int* my_flag,
-                                              volatile int* their_flag, int seq, float v, float* other, int lane,
-                                              volatile int* abort_flag) {
-  *mine = v;
-  __syncwarp();
-  if (lane == 0) {
-    __threadfence_block();
-    *my_flag = seq;
-  }
-  bool ok = true;
-  if (*their_flag < seq) {
-    const uint64_t t0 = globaltimer_ns();
-    uint32_t spins = 0;
-    while (*their_flag < seq) {
-      if ((++spins & 255u) == 0u && (*abort_flag || globaltimer_ns() - t0 > kWaitLimitNs)) {
-        ok = false;
-        break;
-      }
-    }
-  }
-  __threadfence_block();
-  *other = *theirs;
-  return __all_sync(0xffffffffu, ok);
-}
-
-__global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams p) {
+__global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams p) {
   grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
                                            ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kT64OffBar);
-  uint64_t* full = bars;            // [2] tile landed (one arrival per warp of the stage's group)
-  uint64_t* empty = bars + 2;       // [2] tile consumed by P V
-  uint64_t* sfull = bars + 4;       // logits ready
-  uint64_t* pfull = bars + 5;       // P written by all softmax threads
-  uint64_t* pvdone = bars + 6;
-  uint64_t* ofull = bars + 7;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kT64OffMisc);
+  if (sm - sm_raw > kT48Slack) {   // block-uniform: the re-aligned layout would not fit
+    if (threadIdx.x == 0) atomicOr(&g_status_attn, kDevTimeout);
+    return;
+  }
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kT48OffBar);
+  uint64_t* full = bars;            // [3] tile landed (one arrival per warp of the stage's group)
+  uint64_t* empty = bars + 3;       // [3] tile consumed by P V
+  uint64_t* sfull = bars + 6;       // logits ready
+  uint64_t* sfree = bars + 7;       // logits read by the softmax (S buffer reusable)
+  uint64_t* pfull = bars + 8;
+  uint64_t* pvdone = bars + 9;
+  uint64_t* ofull = bars + 10;
+  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kT48OffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
-  volatile uint64_t* mask_s = reinterpret_cast<volatile uint64_t*>(sm + kT64OffMask);
-  volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + kT64OffMask);
-  volatile float* red = reinterpret_cast<volatile float*>(sm + kT64OffRed);
-  volatile int* flags = reinterpret_cast<volatile int*>(sm + kT64OffFlag);
+  volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + kT48OffMask);   // [stage][warp]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x & 1;
@@ -747,7 +725,7 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
   const int K = p.a.K;
   const int r0 = split * p.rows_per_split;
   const int r1 = min(K, r0 + p.rows_per_split);
-  const int ntiles = (r1 - r0 + kBR64 - 1) / kBR64;
+  const int ntiles = (r1 - r0 + kBR48 - 1) / kBR48;
 
   int qp = __ldg(p.seq.q_pos + t);
   int b = __ldg(p.seq.q_seq + t);
@@ -759,19 +737,19 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
   const uint16_t* qg = static_cast<const uint16_t*>(p.a.q) + static_cast<int64_t>(t) * kH * kDqk;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kT64Stages; ++i) {
-      mbar_init(&full[i], 4);
+    for (int i = 0; i < kT48Stages; ++i) {
+      mbar_init(&full[i], kT48Producers);
       mbar_init(&empty[i], 1);
     }
     mbar_init(sfull, 1);
-    mbar_init(pfull, kT64Softmax);
+    mbar_init(sfree, 128);
+    mbar_init(pfull, 128);
     mbar_init(pvdone, 1);
     mbar_init(ofull, 1);
-    for (int i = 0; i < 8; ++i) flags[i] = 0;
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == kT64Lead) {
+  if (warp == kT48Mma) {
     tmem_alloc(misc, kTmemCols);
     tmem_relinquish();
   }
@@ -779,11 +757,51 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
+  // The producers start gathering tiles at once; warps 9-13 stage the query
+  // meanwhile (dims [320, 576) in shared memory, [0, 320) in TMEM) and meet at
+  // named barrier 1 before the first MMA.
+  constexpr uint32_t kQBar = 1, kQBarThreads = 5 * 32;
+  if (warp >= kT48Mma) {
+    const uint32_t qbase = smem_u32(sm + kT48OffQ);
+    constexpr int kChunks = (kDqk - kT48QTmemDims) / 8;
+    for (int i = threadIdx.x - kT48Mma * 32; i < kH * kChunks; i += kQBarThreads) {
+      const int h = i / kChunks, ch = i % kChunks;
+      cp_async16(qbase + sw128_offset(h, ch, kH), qg + h * kDqk + kT48QTmemDims + ch * 8);
+    }
+    cp_async_commit();
+  }
+  if (warp > kT48Mma) {
+    const int h = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
+#pragma unroll 1
+    for (int blk = 0; blk < kT48QTmemDims / 64; ++blk) {
+      uint32_t r[32];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint4 v = __ldg(qrow + blk * 8 + i);
+        r[4 * i] = v.x;
+        r[4 * i + 1] = v.y;
+        r[4 * i + 2] = v.z;
+        r[4 * i + 3] = v.w;
+      }
+      tmem_st32(tmem + lane_off + kT48ColQ + blk * 32, r);
+    }
+    tmem_st_wait();
+  }
+  if (warp >= kT48Mma) {
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_sync(kQBar, kQBarThreads);
+    tc_fence_after();
+  }
 
-  if (warp < kT64Lead) {
-    // ------------------------------------------------ producers: group g = warp / 4 loads tiles
-    // j = g mod 2 into stage g; warp w = warp % 4 copies tile rows [16w, 16w+16)
-    const int grp = warp >> 2, pw = warp & 3;
+  if (warp < kT48Mma) {
+    // ------------------------------------------------ producers: group g = warp / 3 loads tiles
+    // j = g mod 3 into stage g; warp w = warp % 3 copies tile rows [16w, 16w+16)
+    constexpr int kRows = kBR48 / kT48Producers;
+    const int grp = warp / kT48Producers, pw = warp % kT48Producers;
     const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);
     const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride;
     const int32_t* idx = p.a.idx + static_cast<int64_t>(t) * K;
@@ -793,15 +811,15 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
 #pragma unroll
     for (int k = 0; k < 3; ++k) {
       const int ch = lane + 32 * k;
-      dst_off[k] = static_cast<uint32_t>((ch >> 3) * kBR64 * 128);   // atom block
+      dst_off[k] = static_cast<uint32_t>((ch >> 3) * kBR48 * 128);   // atom block
       src_off[k] = static_cast<uint32_t>(ch * 16);
     }
     const int st = grp;
-    const uint32_t stage = smem_u32(sm + kT64OffKV + st * kTile64Bytes);
-    for (int j = grp; j < ntiles; j += kT64Stages) {
+    const uint32_t stage = smem_u32(sm + kT48OffKV + st * kTile48Bytes);
+    for (int j = grp; j < ntiles; j += kT48Stages) {
       int64_t my_row = -1;
-      if (lane < 16) {
-        const int gi = r0 + j * kBR64 + pw * 16 + lane;
+      if (lane < kRows) {
+        const int gi = r0 + j * kBR48 + pw * kRows + lane;
         if (gi < r1) {
           const int pos = __ldg(idx + gi);
           if (pos >= 0) {
@@ -812,23 +830,27 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
           }
         }
       }
-      const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & 0xFFFFu;
-      if (j >= kT64Stages) {
-        // the stage is still busy: have L2 fetch this warp's 16 rows (9 lines of 128 B each) meanwhile
+      const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & ((1u << kRows) - 1u);
+      if (j >= kT48Stages) {
+        // the stage is still busy: have L2 fetch this warp's rows (9 lines of 128 B each) meanwhile
 #pragma unroll
-        for (int k = 0; k < (16 * 9 + 31) / 32; ++k) {
+        for (int k = 0; k < (kRows * 9 + 31) / 32; ++k) {
           const int i = lane + 32 * k;
-          const int64_t prow = __shfl_sync(0xffffffffu, my_row, min(i / 9, 15));
-          if (i < 16 * 9 && prow >= 0) prefetch_l2(kv + prow * p.a.row_bytes + (i % 9) * 128);
+          const int64_t prow = __shfl_sync(0xffffffffu, my_row, min(i / 9, kRows - 1));
+          if (i < kRows * 9 && prow >= 0) prefetch_l2(kv + prow * p.a.row_bytes + (i % 9) * 128);
         }
-        const bool ok = mbar_wait(&empty[st], ((j / kT64Stages) - 1) & 1, &g_status_attn, abort_flag);
+        const bool ok = mbar_wait(&empty[st], ((j / kT48Stages) - 1) & 1, &g_status_attn, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) mask16[st * 4 + pw] = static_cast<uint16_t>(bits);
+      // every row number first: a shuffle queues behind earlier cp.async copies
+      int32_t rows[kRows];
 #pragma unroll
-      for (int rr = 0; rr < 16; ++rr) {
-        const int r = pw * 16 + rr;                          // row within the tile
-        const int64_t prow = __shfl_sync(0xffffffffu, my_row, rr);
+      for (int rr = 0; rr < kRows; ++rr) rows[rr] = __shfl_sync(0xffffffffu, static_cast<int32_t>(my_row), rr);
+#pragma unroll
+      for (int rr = 0; rr < kRows; ++rr) {
+        const int r = pw * kRows + rr;                       // row within the tile
+        const int64_t prow = rows[rr];
         const uint32_t drow = stage + static_cast<uint32_t>(r * 128);
         if (prow >= 0) {
           const uint8_t* srow = kv + prow * p.a.row_bytes;
@@ -855,110 +877,118 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
     }
-  } else {
-    // ------------------------------------------------ softmax + epilogue (warps 8-15)
-    // The query: dims [320, 576) into shared memory (all 256 threads), dims
-    // [0, 320) into TMEM lane h (the pair splits the five 64-dim blocks 3 + 2).
-    const int quarter = warp & 3;                 // TMEM lane quarter this warp may access
-    const int hf = warp >= kT64Lead + 4 ? 1 : 0;
-    const int h = quarter * 32 + lane;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const bool lead = warp == kT64Lead;
-    {
-      const uint32_t qbase = smem_u32(sm + kT64OffQ);
-      constexpr int kChunks = (kDqk - kT64QTmemDims) / 8;
-      for (int i = threadIdx.x - kT64Lead * 32; i < kH * kChunks; i += kT64Softmax) {
-        const int hh = i / kChunks, ch = i % kChunks;
-        cp_async16(qbase + sw128_offset(hh, ch, kH), qg + hh * kDqk + kT64QTmemDims + ch * 8);
-      }
-      cp_async_commit();
-      const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
-#pragma unroll 1
-      for (int blk = hf * 3; blk < (hf ? kT64QTmemDims / 64 : 3); ++blk) {
-        uint32_t r[32];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint4 v = __ldg(qrow + blk * 8 + i);
-          r[4 * i] = v.x;
-          r[4 * i + 1] = v.y;
-          r[4 * i + 2] = v.z;
-          r[4 * i + 3] = v.w;
-        }
-        tmem_st32(tmem + lane_off + kT64ColQ + blk * 32, r);
-      }
-      tmem_st_wait();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      tc_fence_before();
-      named_bar_sync(1, kT64Softmax);
-      tc_fence_after();
-    }
-    // MMA descriptors (lead warp only; rebuilt where used to keep registers free)
-    const uint32_t q_smem = smem_u32(sm + kT64OffQ), kv_smem = smem_u32(sm + kT64OffKV);
-    bool ok = true;
-    if (lead && ntiles > 0) {
-      ok = mbar_wait(&full[0], 0, &g_status_attn, abort_flag);
-      ok = __all_sync(0xffffffffu, ok);
-      if (ok) {
+  } else if (warp == kT48Mma) {
+    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
+    const uint64_t dq0 = make_sdesc(smem_u32(sm + kT48OffQ), 16, 1024, kLayoutSw128);
+    const uint64_t dk0 = make_sdesc(smem_u32(sm + kT48OffKV), 16, 1024, kLayoutSw128);
+    const uint64_t dv0 = make_sdesc(smem_u32(sm + kT48OffKV) + c * 4 * kBR48 * 128, kBR48 * 128, 1024, kLayoutSw128);
+    int next_s = 0, next_pv = 0;
+    uint32_t spins = 0;
+    uint64_t stall_t0 = 0;
+    while (next_pv < ntiles) {
+      bool progress = false;
+      // P V_j as soon as P_j is written (it frees stage j)
+      const bool p_ready = next_pv < next_s && mbar_test_wait(smem_u32(pfull), next_pv & 1);
+      if (__shfl_sync(0xffffffffu, p_ready, 0)) {
         tc_fence_after();
+        const int j = next_pv;
+        const uint64_t dv = dv0 + static_cast<uint64_t>(((j % kT48Stages) * kTile48Bytes) >> 4);
         if (elect_one()) {
-          t64_issue_s(tmem, make_sdesc(q_smem, 16, 1024, kLayoutSw128), make_sdesc(kv_smem, 16, 1024, kLayoutSw128));
+#pragma unroll
+          for (int kk = 0; kk < kBR48 / 16; ++kk)
+            umma_f16_tmem_a(tmem + kT48ColO, tmem + kT48ColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
+                            kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(pvdone);
+          umma_commit(&empty[j % kT48Stages]);
+          if (j == ntiles - 1) umma_commit(ofull);
+        }
+        __syncwarp();
+        ++next_pv;
+        progress = true;
+      }
+      // Q K^T_j as soon as tile j has landed and the softmax has read S_{j-1}
+      const bool s_ready = next_s < ntiles &&
+                           (next_s == 0 || mbar_test_wait(smem_u32(sfree), (next_s - 1) & 1)) &&
+                           mbar_test_wait(smem_u32(&full[next_s % kT48Stages]), (next_s / kT48Stages) & 1);
+      if (__shfl_sync(0xffffffffu, s_ready, 0)) {
+        tc_fence_after();
+        const int j = next_s;
+        const uint64_t dk = dk0 + static_cast<uint64_t>(((j % kT48Stages) * kTile48Bytes) >> 4);
+        if (elect_one()) {
+          t48_issue_s(tmem, dq0, dk);
           umma_commit(sfull);
         }
         __syncwarp();
+        ++next_s;
+        progress = true;
+      }
+      if (progress) {
+        stall_t0 = 0;
+      } else if ((++spins & 63u) == 0u) {
+        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+        if (stall_t0 == 0) {
+          stall_t0 = now;
+        } else if (now - stall_t0 > kWaitLimitNs) {
+          if (lane == 0) {
+            atomicOr(&g_status_attn, kDevTimeout);
+            *abort_flag = 1;
+          }
+          break;
+        }
       }
     }
-    const uint32_t col_o = kT64ColO + hf * (kDvHalf / 2);
-    volatile float* my_red = red + hf * kH + h;
-    volatile float* their_red = red + (1 - hf) * kH + h;
-    volatile int* my_flag = flags + hf * 4 + quarter;
-    volatile int* their_flag = flags + (1 - hf) * 4 + quarter;
+  } else {
+    // ------------------------------------------------ softmax + epilogue (warps 10-13)
+    const int quarter = warp & 3;
+    const int h = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.a.softmax_scale * kLog2e;
     float m = -INFINITY, l = 0.f, l32 = 0.f;
-    for (int j = 0; ok && j < ntiles; ++j) {
-      const int st = j % kT64Stages;
+    bool ok = true;
+    for (int j = 0; j < ntiles; ++j) {
+      const int st = j % kT48Stages;
       ok = mbar_wait(sfull, j & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // the producers' row mask is ordered by their release on full[st] (still the
       // current phase: the stage is refilled only after this tile's P V)
-      ok = mbar_wait(&full[st], (j / kT64Stages) & 1, &g_status_attn, abort_flag);
+      ok = mbar_wait(&full[st], (j / kT48Stages) & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[32];
-      tmem_ld32(tmem + lane_off + kT64ColS + hf * 32, sv);
+      uint32_t s0[32], s1[16];
+      tmem_ld32(tmem + lane_off + kT48ColS, s0);
+      tmem_ld16(tmem + lane_off + kT48ColS + 32, s1);
       tmem_ld_wait();
-      const uint32_t vmask = static_cast<uint32_t>(mask_s[st] >> (32 * hf));
-      float x[32];
+      tc_fence_before();
+      mbar_arrive(sfree);
+      const uint64_t vmask = static_cast<uint64_t>(mask16[st * 4]) | (static_cast<uint64_t>(mask16[st * 4 + 1]) << 16) |
+                             (static_cast<uint64_t>(mask16[st * 4 + 2]) << 32);
+      float x[kBR48];
       float mloc = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        x[i] = ((vmask >> i) & 1u) ? __uint_as_float(sv[i]) * sl2 : -INFINITY;
+      for (int i = 0; i < kBR48; ++i) {
+        const uint32_t raw = i < 32 ? s0[i & 31] : s1[(i - 32) & 15];
+        x[i] = ((vmask >> i) & 1u) ? __uint_as_float(raw) * sl2 : -INFINITY;
         mloc = fmaxf(mloc, x[i]);
       }
-      // P V_{j-1} was issued before Q K^T_j, so it has completed (in-order
-      // completion) -- the wait documents and checks that; the partner has read
-      // the value exchanged for tile j-1 before its pfull arrival
       if (j >= 1) {
+        // P V_{j-1} has read P and written O
         ok = mbar_wait(pvdone, (j - 1) & 1, &g_status_attn, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
       }
-      float mo;
-      if (!t64_pair_swap(my_red, their_red, my_flag, their_flag, j + 1, mloc, &mo, lane, abort_flag)) {
-        ok = false;
-        break;
-      }
-      const float m_new = fmaxf(m, fmaxf(mloc, mo));   // identical in both warps of the pair
+      const float m_new = fmaxf(m, mloc);
       const bool need = m_new > m + kRescaleThreshold;
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
         const float f = need ? exp2f(m - m_new) : 1.f;
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + col_o + cc * 32, o);
+          tmem_ld32(tmem + lane_off + kT48ColO + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tmem + lane_off + col_o + cc * 32, o);
+          tmem_st32(tmem + lane_off + kT48ColO + cc * 32, o);
         }
       }
       if (need) {
@@ -969,9 +999,9 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       }
       const float msub = (m == -INFINITY) ? 0.f : m;
       float psum = 0.f, psum32 = 0.f;
-      uint32_t pk[16];
+      uint32_t pk[kBR48 / 2];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
+      for (int i = 0; i < kBR48 / 2; ++i) {
         const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
         psum32 += p0 + p1;
         __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
@@ -981,97 +1011,62 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
       }
       l += psum;
       l32 += psum32;
-      tmem_st16(tmem + lane_off + kT64ColP + hf * 16, pk);
+      {
+        uint32_t pa[16], pb[8];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pa[i] = pk[i];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pb[i] = pk[16 + i];
+        tmem_st16(tmem + lane_off + kT48ColP, pa);
+        tmem_st8(tmem + lane_off + kT48ColP + 16, pb);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(pfull);
-      if (lead) {
-        // every softmax thread has written P_j (and read S_j): P V_j, then Q K^T_{j+1}
-        ok = mbar_wait(pfull, j & 1, &g_status_attn, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-        if (elect_one()) {
-          const uint64_t dv = make_sdesc(kv_smem + st * kTile64Bytes + c * 4 * kBR64 * 128, kBR64 * 128, 1024,
-                                         kLayoutSw128);
-#pragma unroll
-          for (int kk = 0; kk < kBR64 / 16; ++kk)
-            umma_f16_tmem_a(tmem + kT64ColO, tmem + kT64ColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
-                            kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(pvdone);
-          umma_commit(&empty[st]);
-          if (j == ntiles - 1) umma_commit(ofull);
-        }
-        __syncwarp();
-        if (j + 1 < ntiles) {
-          const int sn = (j + 1) % kT64Stages;
-          ok = mbar_wait(&full[sn], ((j + 1) / kT64Stages) & 1, &g_status_attn, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-          tc_fence_after();
-          if (elect_one()) {
-            t64_issue_s(tmem, make_sdesc(q_smem, 16, 1024, kLayoutSw128),
-                        make_sdesc(kv_smem + sn * kTile64Bytes, 16, 1024, kLayoutSw128));
-            umma_commit(sfull);
-          }
-          __syncwarp();
-        }
-      }
     }
     if (ok) {
       ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag);
       ok = __all_sync(0xffffffffu, ok);
     }
-    // the pair's partial denominators (each warp summed its own columns); the
-    // exchange goes through the query tile's shared memory, idle once ofull fired
-    float lo = 0.f, l32o = 0.f;
-    if (ok) {
-      volatile float* fin = reinterpret_cast<volatile float*>(sm + kT64OffQ);
-      ok = t64_pair_swap(fin + hf * kH + h, fin + (1 - hf) * kH + h, my_flag, their_flag, ntiles + 1, l, &lo,
-                         lane, abort_flag);
-      if (ok)
-        ok = t64_pair_swap(fin + (2 + hf) * kH + h, fin + (3 - hf) * kH + h, my_flag, their_flag, ntiles + 2, l32,
-                           &l32o, lane, abort_flag);
-    }
     if (ok) {
       tc_fence_after();
-      const float lt = l + lo, l32t = l32 + l32o;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const float lse = l32t > 0.f ? (m + log2f(l32t)) * kLn2 : -INFINITY;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const float lse = l32 > 0.f ? (m + log2f(l32)) * kLn2 : -INFINITY;
       const int64_t th = static_cast<int64_t>(t) * kH + h;
       // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB per warp
-      const uint32_t stg = smem_u32(sm + kT64OffKV) + (hf * 4 + quarter) * 4096;
+      const uint32_t stg = smem_u32(sm + kT48OffKV) + quarter * 4096;
       const int64_t th0 = static_cast<int64_t>(t) * kH + quarter * 32;   // this warp's first head
-      const int col0 = c * kDvHalf + hf * (kDvHalf / 2);                 // first value dim it writes
       if (p.n_split == 1) {
-        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + col0);
+        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + c * kDvHalf);
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 128; ++cc) {
+        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
           uint32_t o0[32], o1[32];
-          tmem_ld32(tmem + lane_off + col_o + cc * 64, o0);
-          tmem_ld32(tmem + lane_off + col_o + cc * 64 + 32, o1);
+          tmem_ld32(tmem + lane_off + kT48ColO + cc * 64, o0);
+          tmem_ld32(tmem + lane_off + kT48ColO + cc * 64 + 32, o1);
           tmem_ld_wait();
-          uint32_t pk[32];
+          uint32_t pk2[32];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            pk[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
-            pk[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
+            pk2[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+            pk2[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
           }
-          warp_store_rows128(stg, pk, out + cc * 128, kDv * 2, lane);
+          warp_store_rows128(stg, pk2, out + cc * 128, kDv * 2, lane);
         }
-        if (c == 0 && hf == 0 && p.a.lse) p.a.lse[th] = lse;
+        if (c == 0 && p.a.lse) p.a.lse[th] = lse;
       } else {
         const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
         uint8_t* out = reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<int64_t>(split) * p.seq.T * kH + th0) * kDv +
-                                                  col0);
+                                                  c * kDvHalf);
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + col_o + cc * 32, o);
+          tmem_ld32(tmem + lane_off + kT48ColO + cc * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
           warp_store_rows128(stg, o, out + cc * 128, kDv * 4, lane);
         }
-        if (c == 0 && hf == 0) p.ws_lse[sth] = lse;
+        if (c == 0) p.ws_lse[sth] = lse;
       }
     }
   }
@@ -1079,7 +1074,7 @@ __global__ void __launch_bounds__(kT64Threads, 1) attn_tc64_kernel(TcAttnParams 
   grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   tc_fence_before();
   __syncthreads();
-  if (warp == kT64Lead) {
+  if (warp == kT48Mma) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -1204,7 +1199,7 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
   }
   if (tc_supported(seq, a)) {
     const bool fp8 = a.kind == MlaKind::kFP8Row;
-    const int tile_rows = fp8 ? kBR : kBR64;
+    const int tile_rows = fp8 ? kBR : kBR48;
     int split = choose_split(seq, a, env.num_sms);
     if (split > 1 && (workspace == nullptr || ws_bytes < attn_workspace_bytes(seq, a, env.num_sms)))
       split = 1;  // no room for partials: one slice per query
@@ -1219,8 +1214,8 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(attn_tc64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kT64SmemBytes);
+      attr_err = cudaFuncSetAttribute(attn_tc48_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      kT48SmemBytes);
       if (attr_err == cudaSuccess)
         attr_err = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         AttnCfg<true>::kSmemBytes);
@@ -1232,13 +1227,14 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
           launch_kernel(attn_tc_kernel<true>, dim3(grid), dim3(kThreads), AttnCfg<true>::kSmemBytes, env.stream, true, 1, p);
       if (le != cudaSuccess) return le;
     } else {
-      const cudaError_t le = launch_kernel(attn_tc64_kernel, dim3(grid), dim3(kT64Threads), kT64SmemBytes, env.stream, true, 1, p);
+      const cudaError_t le =
+          launch_kernel(attn_tc48_kernel, dim3(grid), dim3(kT48Threads), kT48SmemBytes, env.stream, true, 1, p);
       if (le != cudaSuccess) return le;
     }
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     char buf[128];
-    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8" : "bf16x64", split, grid);
+    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8" : "bf16x48", split, grid);
     *plan += buf;
     if (split > 1) {
       const size_t smem = static_cast<size_t>(split) * kCombineHeads * sizeof(float);
