@@ -629,8 +629,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 // ---------------------------------------------------------------------------
 // bf16 rows, 48-row tiles, three stages.
 //
-// Producers (warps 0-8): three groups of three warps own one stage each and
-// load every third tile (16 rows per warp; a warp issues cp.async copies at
+// Producers (warps 0-11): three groups of four warps own one stage each and
+// load every third tile (12 rows per warp; a warp issues cp.async copies at
 // ~30 ns per instruction here, so the warps per tile set how fast it lands).  Lanes resolve the rows (index -> page
 // -> cache row) as soon as the group's previous tile has landed and ask L2 to
 // fetch them; once the stage is free every lane copies its fixed 16-byte
@@ -638,14 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 // that select nothing are zeroed.  (On this GPU a tile::gather4 TMA producer
 // reached ~12 GB/s per SM and cp.async gathers ~60 GB/s.)
 //
-// MMA warp (warp 9): Q K^T_{j+1} (N = 48 rows) as soon as the softmax has read
+// MMA warp (warp 12): Q K^T_{j+1} (N = 48 rows) as soon as the softmax has read
 // S_j and tile j+1 has landed, so it runs during the softmax of tile j; P V_j
 // (N = 256 value dims, P read from TMEM) as soon as P_j is written.  An M=128
 // K=16 step whose A operand (the query) sits in shared memory reads 6 KB of
 // shared memory and takes ~53 clk, one with A in TMEM ~36 clk, so the first 320
 // query dims live in TMEM.
 //
-// Softmax (warps 10-13): one thread per head (its TMEM lane), 48 logits a tile,
+// Softmax (warps 13-16): one thread per head (its TMEM lane), 48 logits a tile,
 // running max moved (and O rescaled in TMEM) only when it grows by more than
 // 2^8.
 //
@@ -671,9 +671,9 @@ constexpr int kT48Used = kT48OffMisc + 16;                     // bytes used fro
 // much slack is requested for it (the kernel checks that it sufficed)
 constexpr int kT48Slack = 232448 - kT48Used;
 constexpr int kT48SmemBytes = kT48Used + kT48Slack;
-constexpr int kT48Threads = 448;   // warps 0-8 producers, warp 9 MMA, warps 10-13 softmax
-constexpr int kT48Mma = 9;
-constexpr int kT48Producers = 3;   // warps per stage group
+constexpr int kT48Threads = 544;   // warps 0-11 producers, warp 12 MMA, warps 13-16 softmax
+constexpr int kT48Mma = 12;
+constexpr int kT48Producers = 4;   // warps per stage group
 constexpr uint32_t kT48ColS = 0, kT48ColP = 64, kT48ColQ = 96, kT48ColO = 256;
 constexpr uint32_t kIdescS48 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR48);
 static_assert(kT48ColQ + kT48QTmemDims / 2 <= kT48ColO, "TMEM plan");
@@ -757,7 +757,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // The producers start gathering tiles at once; warps 9-13 stage the query
+  // The producers start gathering tiles at once; warps 12-16 stage the query
   // meanwhile (dims [320, 576) in shared memory, [0, 320) in TMEM) and meet at
   // named barrier 1 before the first MMA.
   constexpr uint32_t kQBar = 1, kQBarThreads = 5 * 32;
@@ -798,8 +798,8 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   }
 
   if (warp < kT48Mma) {
-    // ------------------------------------------------ producers: group g = warp / 3 loads tiles
-    // j = g mod 3 into stage g; warp w = warp % 3 copies tile rows [16w, 16w+16)
+    // ------------------------------------------------ producers: group g = warp / 4 loads tiles
+    // j = g mod 3 into stage g; warp w = warp % 4 copies tile rows [12w, 12w+12)
     constexpr int kRows = kBR48 / kT48Producers;
     const int grp = warp / kT48Producers, pw = warp % kT48Producers;
     const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);
@@ -939,7 +939,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       }
     }
   } else {
-    // ------------------------------------------------ softmax + epilogue (warps 10-13)
+    // ------------------------------------------------ softmax + epilogue (warps 13-16)
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
@@ -961,8 +961,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(sfree);
-      const uint64_t vmask = static_cast<uint64_t>(mask16[st * 4]) | (static_cast<uint64_t>(mask16[st * 4 + 1]) << 16) |
-                             (static_cast<uint64_t>(mask16[st * 4 + 2]) << 32);
+      uint64_t vmask = 0;
+#pragma unroll
+      for (int w = 0; w < kT48Producers; ++w)
+        vmask |= static_cast<uint64_t>(mask16[st * 4 + w]) << (w * (kBR48 / kT48Producers));
       float x[kBR48];
       float mloc = -INFINITY;
 #pragma unroll
