@@ -89,8 +89,15 @@ constexpr int kTcDim = 128;        // D_I (bytes per key row)
 constexpr int kTcKeys = 128;       // keys per tile = UMMA M
 constexpr int kTcPage = 64;        // tokens per page
 constexpr int kTcStages = 6;       // key-tile ring depth (16 KB each)
-constexpr int kTcThreads = 192;    // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kTcEpiThreads = 128;
+// warp 0 TMA, warp 1 MMA, then the epilogue: 4 warps (one per TMEM lane
+// quarter) for a single query, 8 (two per quarter, splitting the query group)
+// for groups of 2 or 4 -- there the ReLU-weighted head sums, not the MMAs, set
+// the tile rate.
+template <int G>
+struct TcWarps {
+  static constexpr int kEpiThreads = G == 1 ? 128 : 256;
+  static constexpr int kThreads = 64 + kEpiThreads;
+};
 
 template <int G>
 struct TcCfg {
@@ -157,8 +164,8 @@ struct TileWalker {
   }
 };
 
-__device__ __forceinline__ int block_sum_192(int v, int* red) {
-  // 6 warps
+template <int kThreads>
+__device__ __forceinline__ int block_sum(int v, int* red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -167,15 +174,17 @@ __device__ __forceinline__ int block_sum_192(int v, int* red) {
   __syncthreads();
   int tot = 0;
 #pragma unroll
-  for (int w = 0; w < kTcThreads / 32; ++w) tot += red[w];
+  for (int w = 0; w < kThreads / 32; ++w) tot += red[w];
   return tot;
 }
 
 template <int G>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap, TcParams p) {
   using C = TcCfg<G>;
+  constexpr int kTcThreads = TcWarps<G>::kThreads;
+  constexpr int kTcEpiThreads = TcWarps<G>::kEpiThreads;
   grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
@@ -190,7 +199,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   int* sched = reinterpret_cast<int*>(misc + 2);   // g0, kt0
-  int* red = reinterpret_cast<int*>(misc + 4);     // 6 ints
+  int* red = reinterpret_cast<int*>(misc + 4);     // one int per warp
   float* wq_s = reinterpret_cast<float*>(sm + C::kOffWq);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -201,7 +210,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int g = g0 + threadIdx.x;
     int nh;
     const int c = (g < p.n_groups) ? group_tiles<G>(p, g, &nh) : 0;
-    total += block_sum_192(c, red);
+    total += block_sum<kTcThreads>(c, red);
   }
   const int64_t begin = static_cast<int64_t>(blockIdx.x) * total / gridDim.x;
   const int64_t end = static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x;
@@ -380,8 +389,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..5)
+    // ------------------------------------------------ epilogue (warps 2..9)
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;             // which part of the query group (0 when G == 1)
+    const int jlo = G == 1 ? 0 : half * (G / 2);
+    const int jhi = G == 1 ? (half == 0 ? 1 : 0) : jlo + G / 2;
     const int row = quarter * 32 + lane;          // key within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const int etid = threadIdx.x - 64;
@@ -452,7 +464,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                               : 0.f;
       mbar_arrive(&empty[st]);
 #pragma unroll 1
-      for (int j = 0; j < G; ++j) {
+      for (int j = jlo; j < jhi; ++j) {
         uint32_t v0[32], v1[32];
         const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
         tmem_ld32(col, v0);
@@ -517,7 +529,8 @@ cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv&
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const cudaError_t le = launch_kernel(indexer_tc_kernel<G>, dim3(grid), dim3(kTcThreads), C::kSmemBytes, env.stream, true, 1,
+  const cudaError_t le = launch_kernel(indexer_tc_kernel<G>, dim3(grid), dim3(TcWarps<G>::kThreads), C::kSmemBytes,
+                                       env.stream, true, 1,
                                     kmap, qmap, p);
   if (le != cudaSuccess) return le;
   char buf[160];
