@@ -237,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
   const int c = blockIdx.x & 1;                     // value half
   const int rest = blockIdx.x >> 1;
   const int split = rest % p.n_split;
-  const int t = rest / p.n_split;
+  const int t = p.seq.T - 1 - rest / p.n_split;   // last query first (longest causal history)
   const int K = p.a.K;
   const int r0 = split * p.rows_per_split;
   const int r1 = min(K, r0 + p.rows_per_split);
@@ -721,7 +721,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   const int c = blockIdx.x & 1;
   const int rest = blockIdx.x >> 1;
   const int split = rest % p.n_split;
-  const int t = rest / p.n_split;
+  const int t = p.seq.T - 1 - rest / p.n_split;   // last query first (longest causal history)
   const int K = p.a.K;
   const int r0 = split * p.rows_per_split;
   const int r1 = min(K, r0 + p.rows_per_split);

@@ -59,6 +59,7 @@ struct TopkArgs {
   int32_t K;
   int32_t* idx;
   int32_t cache_keys;  // keys cached per CTA in dynamic smem (0 = none)
+  int32_t T;
 };
 
 // Exclusive scan of one value per warp; every thread gets (its warp's offset,
@@ -97,7 +98,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
   const int rank = static_cast<int>(cluster.block_rank());
-  const int t = blockIdx.x / CL;
+  // clusters take queries last-first: with causal histories (prefill) the longest
+  // histories start first and the short ones fill the tail of the launch
+  const int t = a.T - 1 - static_cast<int>(blockIdx.x) / CL;
   const int tid = threadIdx.x, lane = tid & 31;
   int qp = __ldg(a.q_pos + t);
   if (qp < 0 || qp >= a.max_ctx) {
@@ -292,7 +295,7 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
                                     kCacheKeys * 4);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, cached ? slice : 0};
+  TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, cached ? slice : 0, seq.T};
   cudaError_t e = launch_kernel(topk_kernel, dim3(seq.T * cl), dim3(kThreads), smem, env.stream, /*pdl=*/false, cl, a);
   char buf[96];
   snprintf(buf, sizeof(buf), "topk_radix[cluster=%d,%s]", cl, cached ? "smem" : "global");

@@ -1,7 +1,8 @@
 """GPU parity of every stage against the CPU oracle, through the C ABI, on
 seeded inputs spanning several tiles, ragged tails and the edge cases of the
 method (history shorter than / equal to / one more than K, one-token history,
-shuffled pages, query groups of 1, 2 and 4)."""
+shuffled pages, query groups of 1, 2 and 4, and 2-8 consecutive query tokens
+per sequence as in speculative verification)."""
 import re
 
 import numpy as np
@@ -27,6 +28,10 @@ CASES = {
     "prefill_700": ("prefill_16k", dict(ctx=[700], q_len=700, K=64)),
     "qlen2": ("decode_b1", dict(ctx=[900], q_len=2, K=128)),
     "qlen3": ("decode_b1", dict(ctx=[900], q_len=3, K=128)),
+    # speculative-verify shapes: several consecutive query tokens per sequence
+    "qlen5": ("decode_b1", dict(ctx=[700], q_len=5, K=64)),
+    "qlen8": ("decode_b1", dict(ctx=[900], q_len=8, K=128)),
+    "qlen8_b3_shuffled": ("decode_b64", dict(ctx_range=(300, 2500), B=3, q_len=8, K=256)),
 }
 
 
