@@ -33,6 +33,17 @@ Readings taken where the pages are silent (each also listed in the design doc):
   then -1 padding up to K;
 * attention skips -1 entries; an empty selection gives out = 0, lse = -inf.
 
+0. (the prolog side) writing a new token into the paged caches: its indexer
+   key quantised to FP8 e4m3 with one fp32 scale, its latent row copied (bf16
+   cache) or quantised the same way with the rope part kept bf16 (FP8 cache)
+   (page "Large Language Model Inference Acceleration in Practice", section 3.2
+   "Indexer Prolog" -- K normalisation and the KV-cache update -- and section 4
+   "Layered Quantization"; page "Day0 ... Kimi K3.1 Pro", section 4).  The
+   quantisation rule is the reading taken for the cache formats: scale =
+   amax / 448 in float32 (1 for an all-zero row), code = the E4M3 value nearest
+   to x / scale (float32 quotient), ties to the even code, magnitudes beyond
+   448 saturated.
+
 Parity pins for every function live in ``tests/test_oracle.py``.
 """
 from __future__ import annotations
@@ -76,6 +87,35 @@ def decode_bf16(bits: np.ndarray) -> np.ndarray:
     """bfloat16 is the upper 16 bits of an IEEE binary32."""
     wide = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return wide.view(np.float32).astype(np.float64)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 code of each float32 value: the finite E4M3 value nearest to x, ties
+    to the code with an even mantissa, magnitudes beyond 448 saturated to 448;
+    the sign bit is kept (so -0.0 -> 0x80).  Codes 0..126 hold the positive
+    finite magnitudes in increasing order (``e4m3_table``)."""
+    x = np.asarray(x, dtype=np.float32)
+    mags = _E4M3[:127]                                  # 0, 2**-9, ..., 448 (ascending)
+    a = np.abs(x).astype(np.float64)
+    hi = np.clip(np.searchsorted(mags, a, side="left"), 0, 126)   # first magnitude >= a
+    lo = np.clip(hi - 1, 0, 126)
+    d_hi = np.abs(mags[hi] - a)
+    d_lo = np.abs(a - mags[lo])
+    pick_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    mag_code = np.where(pick_lo, lo, hi)
+    mag_code = np.where(a >= 448.0, 126, mag_code)      # saturate
+    sign = np.signbit(x).astype(np.int64) << 7
+    return (sign | mag_code).astype(np.uint8)
+
+
+def quantize_e4m3_row(x) -> tuple:
+    """One token's vector -> (uint8 codes, float32 scale): scale = amax / 448 in
+    float32 (1 when the row is all zero), codes = e4m3_encode(x / scale) with the
+    quotient formed in float32."""
+    x = np.asarray(x, dtype=np.float32)
+    amax = np.float32(np.max(np.abs(x))) if x.size else np.float32(0)
+    scale = np.float32(amax / np.float32(448.0)) if amax > 0 else np.float32(1.0)
+    return e4m3_encode((x / scale).astype(np.float32)), scale
 
 
 def physical_rows(block_table_row: np.ndarray, page_size: int, pos: np.ndarray) -> np.ndarray:
@@ -229,3 +269,48 @@ def decode_step(wl, ts=None):
     idx = topk(scores, q_pos, wl.K)
     out, lse = sparse_mla_attn(wl, idx, ts)
     return scores, idx, out, lse
+
+
+# ---------------------------------------------------------------------------
+# step 0: writing new tokens into the paged caches (the prolog side)
+# ---------------------------------------------------------------------------
+
+
+def index_cache_append(block_table, page_size, q_seq, q_pos, k_new, k_cache, k_scale):
+    """Quantise k_new[t] (float32 [T, D]) and store it at the cache row of
+    position q_pos[t] of sequence q_seq[t].  Returns updated copies of k_cache
+    (uint8 [rows, D]) and k_scale (float32 [rows])."""
+    k_cache = np.array(k_cache, dtype=np.uint8, copy=True)
+    k_scale = np.array(k_scale, dtype=np.float32, copy=True)
+    for t in range(len(q_pos)):
+        row = int(physical_rows(block_table[int(q_seq[t])], page_size, np.array([q_pos[t]]))[0])
+        codes, scale = quantize_e4m3_row(k_new[t])
+        k_cache[row] = codes
+        k_scale[row] = scale
+    return k_cache, k_scale
+
+
+def latent_cache_append(block_table, page_size, q_seq, q_pos, kv_new_bits, cache, fp8_rows: bool,
+                        d_latent: int = 512, d_rope: int = 64):
+    """Store the new latent rows (bfloat16 bit patterns, uint16 [T, d_latent +
+    d_rope]) at the cache rows of their positions.  `cache` is uint8 [rows,
+    row_bytes].  bf16 cache: the row's bytes are the input's.  FP8 cache (656-byte
+    rows): [0, 512) e4m3 codes of the latent part quantised as one vector,
+    [512, 516) its float32 scale, [516, 528) zero, [528, 656) the rope part's bf16
+    bytes.  Returns an updated copy of the cache."""
+    cache = np.array(cache, dtype=np.uint8, copy=True)
+    bits = np.asarray(kv_new_bits, dtype=np.uint16)
+    for t in range(len(q_pos)):
+        row = int(physical_rows(block_table[int(q_seq[t])], page_size, np.array([q_pos[t]]))[0])
+        if not fp8_rows:
+            b = bits[t].astype("<u2").tobytes()
+            cache[row, :len(b)] = np.frombuffer(b, dtype=np.uint8)
+            continue
+        latent = decode_bf16(bits[t, :d_latent]).astype(np.float32)
+        codes, scale = quantize_e4m3_row(latent)
+        cache[row, :d_latent] = codes
+        cache[row, d_latent:d_latent + 4] = np.frombuffer(np.float32(scale).astype("<f4").tobytes(), dtype=np.uint8)
+        cache[row, d_latent + 4:d_latent + 16] = 0
+        rope = bits[t, d_latent:d_latent + d_rope].astype("<u2").tobytes()
+        cache[row, d_latent + 16:d_latent + 16 + len(rope)] = np.frombuffer(rope, dtype=np.uint8)
+    return cache

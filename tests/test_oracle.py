@@ -346,3 +346,80 @@ def test_hand_worked_golden_example():
     # closed form holds to ~1e-7 relative
     np.testing.assert_allclose(out[0, 0], exp["out"], rtol=1e-7)
     np.testing.assert_allclose(lse[0, 0], exp["lse"], rtol=1e-7)
+
+
+# --------------------------------------------------------------------------- cache writers (step 0)
+
+def test_e4m3_encode_matches_torch_cast_within_range():
+    """torch's float8_e4m3fn cast (a library routine: round to nearest, ties to
+    even) agrees with the encoder wherever it does not overflow (|x| <= 464),
+    including every tie between adjacent codes, subnormals and signed zero."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(21)
+    vals = O.e4m3_table()[:127]
+    mids = ((vals[:-1] + vals[1:]) / 2).astype(np.float32)     # exact ties
+    x = np.concatenate([rng.uniform(-464, 464, 50000).astype(np.float32),
+                        rng.normal(0, 0.01, 5000).astype(np.float32), vals.astype(np.float32),
+                        mids, -mids, np.array([0.0, -0.0, 464.0, -464.0], np.float32)])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(O.e4m3_encode(x), ref)
+
+
+def test_e4m3_encode_round_trip_and_saturation():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    vals = O.decode_e4m3(codes).astype(np.float32)
+    got = O.e4m3_encode(vals)
+    assert np.array_equal(O.decode_e4m3(got), vals.astype(np.float64))   # +-0 both decode to 0
+    sat = O.e4m3_encode(np.array([465.0, 500.0, 1e30, -465.0, -1e30], np.float32))
+    assert sat.tolist() == [0x7E, 0x7E, 0x7E, 0xFE, 0xFE]                # +-448, never NaN
+
+
+def test_quantize_row_rule():
+    rng = np.random.default_rng(22)
+    x = rng.normal(0, 3, 128).astype(np.float32)
+    codes, scale = O.quantize_e4m3_row(x)
+    amax = np.float32(np.abs(x).max())
+    assert scale == np.float32(amax / np.float32(448.0))
+    k = int(np.argmax(np.abs(x)))
+    assert O.decode_e4m3(codes[k:k + 1])[0] == np.sign(x[k]) * 448.0       # the largest element maps to +-448
+    deq = O.decode_e4m3(codes) * np.float64(scale)
+    # nearest-value rounding: within half a step of E4M3 (2**-4 relative for normals,
+    # 2**-10 * scale absolute in the subnormal range)
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, 2.0 ** -10 * float(scale)) * (1 + 1e-6)
+    assert np.all(np.abs(deq - x) <= bound)
+    zc, zs = O.quantize_e4m3_row(np.zeros(64, np.float32))
+    assert zs == np.float32(1.0) and not zc.any()
+
+
+def test_cache_append_oracle_layout_and_untouched_rows():
+    """Rows other than the targets keep their bytes; the FP8 row holds codes,
+    the float32 scale (little endian), 12 zero bytes and the rope bits."""
+    rng = np.random.default_rng(23)
+    page, pages = 64, 6
+    block_table = np.array([[4, 1, 5], [0, 3, 2]], dtype=np.int32)
+    q_seq = np.array([0, 1, 1], dtype=np.int32)
+    q_pos = np.array([130, 5, 64], dtype=np.int32)
+    rows = [5 * 64 + 2, 0 * 64 + 5, 3 * 64 + 0]
+    k_new = rng.normal(0, 1, (3, 128)).astype(np.float32)
+    kc0 = rng.integers(0, 256, (pages * page, 128)).astype(np.uint8)
+    ks0 = rng.normal(0, 1, pages * page).astype(np.float32)
+    kc, ks = O.index_cache_append(block_table, page, q_seq, q_pos, k_new, kc0, ks0)
+    other = np.setdiff1d(np.arange(pages * page), rows)
+    assert np.array_equal(kc[other], kc0[other]) and np.array_equal(ks[other], ks0[other])
+    for t, r in enumerate(rows):
+        codes, scale = O.quantize_e4m3_row(k_new[t])
+        assert np.array_equal(kc[r], codes) and ks[r] == scale
+    bits = (rng.normal(0, 1, (3, 576)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    cache0 = rng.integers(0, 256, (pages * page, 656)).astype(np.uint8)
+    cache = O.latent_cache_append(block_table, page, q_seq, q_pos, bits, cache0, fp8_rows=True)
+    assert np.array_equal(cache[other], cache0[other])
+    for t, r in enumerate(rows):
+        codes, scale = O.quantize_e4m3_row(O.decode_bf16(bits[t, :512]).astype(np.float32))
+        assert np.array_equal(cache[r, :512], codes)
+        assert cache[r, 512:516].view("<f4")[0] == scale
+        assert not cache[r, 516:528].any()
+        assert np.array_equal(cache[r, 528:656].view("<u2"), bits[t, 512:])
+    cacheb0 = rng.integers(0, 256, (pages * page, 1152)).astype(np.uint8)
+    cacheb = O.latent_cache_append(block_table, page, q_seq, q_pos, bits, cacheb0, fp8_rows=False)
+    assert np.array_equal(cacheb[other], cacheb0[other])
+    assert all(np.array_equal(cacheb[r].view("<u2"), bits[t]) for t, r in enumerate(rows))
