@@ -25,7 +25,8 @@ DSA_F32, DSA_BF16, DSA_E4M3 = 0, 1, 2
 EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_plan",
             "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn_workspace_size",
             "dsa_sparse_mla_attn", "dsa_decode_workspace_size", "dsa_decode_step",
-            "dsa_decode_step_static_ws", "dsa_check_status")
+            "dsa_decode_step_static_ws", "dsa_index_cache_append", "dsa_latent_cache_append",
+            "dsa_check_status")
 STATIC_WORKSPACE_BYTES = 32 << 20   # DSA_STATIC_WORKSPACE_BYTES
 
 
@@ -71,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "dsa_decode_workspace_size": (ctypes.c_size_t, [P, P, P, ctypes.c_int32]),
         "dsa_decode_step": (C, [P, P, P, ctypes.c_int32, P, P, P, P, ctypes.c_size_t, P]),
         "dsa_decode_step_static_ws": (C, [P, P, P, ctypes.c_int32, P, P, P, P]),
+        "dsa_index_cache_append": (C, [P, ctypes.c_int32, C, P, P, P, P]),
+        "dsa_latent_cache_append": (C, [P, P, P, P, P]),
         "dsa_check_status": (C, [P]),
     }
     for name, (res, args) in sig.items():
@@ -226,6 +229,23 @@ def decode_step_static_ws(seq: Seq, idx: Indexer, mla: Mla, K: int, out: torch.T
     _check(_lib.dsa_decode_step_static_ws(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), K, _ptr(out),
                                           _ptr(lse), _ptr(idx_out), _stream(stream)))
     return out
+
+
+def index_cache_append(seq: Seq, k_new: torch.Tensor, k_cache: torch.Tensor, k_scale: torch.Tensor,
+                       stream=None) -> None:
+    """Quantises the new tokens' index keys k_new [T, D_I] (fp32 or bf16) to e4m3
+    + per-token scale and writes them at their positions' cache rows."""
+    s = seq.desc()
+    _check(_lib.dsa_index_cache_append(ctypes.byref(s), k_new.shape[1], _dtype_code(k_new), _ptr(k_new),
+                                       _ptr(k_cache), _ptr(k_scale), _stream(stream)))
+
+
+def latent_cache_append(seq: Seq, mla: Mla, kv_new: torch.Tensor, stream=None) -> None:
+    """Writes the new tokens' latent rows kv_new [T, d_latent + d_rope] into
+    mla.kv_cache (copied, or quantised into 656-byte FP8 rows)."""
+    s, m = seq.desc(), mla.desc()
+    _check(_lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), _ptr(kv_new), _ptr(mla.kv_cache),
+                                        _stream(stream)))
 
 
 def check_status(stream=None) -> None:

@@ -370,12 +370,68 @@ dsa_status_t dsa_decode_step(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t
   }
 }
 
+dsa_status_t dsa_index_cache_append(const dsa_seq_desc_t* seq, int32_t D_I, dsa_dtype_t src_dtype,
+                                    const void* k_new, uint8_t* k_cache, float* k_scale, dsa_stream_t stream) {
+  try {
+    dsa::SeqArgs s;
+    dsa_status_t st = check_seq(seq, &s);
+    if (st != DSA_OK) return st;
+    if (D_I < 4 || D_I > 1024 || D_I % 4 != 0)
+      return fail(DSA_ERR_UNSUPPORTED, "index-key append needs D_I in [4, 1024], a multiple of 4");
+    if (src_dtype != DSA_F32 && src_dtype != DSA_BF16)
+      return fail(DSA_ERR_UNSUPPORTED, "new index keys must be DSA_F32 or DSA_BF16");
+    if (s.T > 0 && (!k_new || !k_cache || !k_scale))
+      return fail(DSA_ERR_INVALID_ARG, "k_new, k_cache and k_scale must be non-NULL");
+    if (!aligned16(k_new) || !aligned16(k_cache) || !aligned16(k_scale))
+      return fail(DSA_ERR_INVALID_ARG, "k_new, k_cache and k_scale must be 16-byte aligned");
+    dsa::LaunchEnv env;
+    if ((st = make_env(stream, &env)) != DSA_OK) return st;
+    std::string plan;
+    cudaError_t e = dsa::launch_index_append(s, D_I, src_dtype == DSA_BF16, k_new, k_cache, k_scale, env, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "index-key append launch");
+    g_last_plan = plan;
+    return DSA_OK;
+  } catch (...) {
+    return fail(DSA_ERR_CUDA, "unexpected host exception");
+  }
+}
+
+dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, const void* kv_new,
+                                     void* kv_cache, dsa_stream_t stream) {
+  try {
+    dsa::SeqArgs s;
+    dsa::MlaArgs a;
+    dsa_status_t st = check_seq(seq, &s);
+    if (st != DSA_OK) return st;
+    if ((st = check_mla_shape(mla, 1, &a)) != DSA_OK) return st;
+    if (a.kind != dsa::MlaKind::kFP8Row) {
+      const int64_t row_in = static_cast<int64_t>(a.d_latent + a.d_rope) * (a.kind == dsa::MlaKind::kF32 ? 4 : 2);
+      if (row_in % 16 != 0 || a.row_bytes % 16 != 0)
+        return fail(DSA_ERR_UNSUPPORTED, "latent append copies 16-byte vectors: row and row_bytes must be multiples of 16");
+    } else if (a.row_bytes % 16 != 0) {
+      return fail(DSA_ERR_INVALID_ARG, "row_bytes must be a multiple of 16");
+    }
+    if (s.T > 0 && (!kv_new || !kv_cache)) return fail(DSA_ERR_INVALID_ARG, "kv_new and kv_cache must be non-NULL");
+    if (!aligned16(kv_new) || !aligned16(kv_cache))
+      return fail(DSA_ERR_INVALID_ARG, "kv_new and kv_cache must be 16-byte aligned");
+    dsa::LaunchEnv env;
+    if ((st = make_env(stream, &env)) != DSA_OK) return st;
+    std::string plan;
+    cudaError_t e = dsa::launch_latent_append(s, a, kv_new, kv_cache, env, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "latent append launch");
+    g_last_plan = plan;
+    return DSA_OK;
+  } catch (...) {
+    return fail(DSA_ERR_CUDA, "unexpected host exception");
+  }
+}
+
 dsa_status_t dsa_check_status(dsa_stream_t stream) {
   try {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     const uint32_t f = dsa_status_read_clear_indexer() | dsa_status_read_clear_topk() |
-                       dsa_status_read_clear_attn();
+                       dsa_status_read_clear_attn() | dsa_status_read_clear_cache();
     if (f == 0) return DSA_OK;
     if (f == 0xFFFFFFFFu) return fail(DSA_ERR_CUDA, "could not read the device status word");
     std::string msg = "device flags:";

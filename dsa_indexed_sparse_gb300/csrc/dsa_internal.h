@@ -105,6 +105,12 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Cache writers (the new tokens' index keys / latent rows into the paged caches).
+cudaError_t launch_index_append(const SeqArgs& seq, int32_t D, bool bf16_in, const void* k_new, uint8_t* k_cache,
+                                float* k_scale, const LaunchEnv& env, std::string* plan);
+cudaError_t launch_latent_append(const SeqArgs& seq, const MlaArgs& a, const void* kv_new, void* kv_cache,
+                                 const LaunchEnv& env, std::string* plan);
+
 // Sets the text dsa_last_error() returns on the calling thread.
 void set_last_error(const std::string& msg);
 
@@ -122,3 +128,4 @@ bool encode_tmap_2d(void* tmap_out, const void* base, int elem_bytes, uint64_t i
 uint32_t dsa_status_read_clear_indexer();
 uint32_t dsa_status_read_clear_topk();
 uint32_t dsa_status_read_clear_attn();
+uint32_t dsa_status_read_clear_cache();

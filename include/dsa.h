@@ -192,6 +192,34 @@ dsa_status_t dsa_decode_step_static_ws(const dsa_seq_desc_t* seq, const dsa_inde
                                        const dsa_mla_desc_t* mla, int32_t K, void* out, float* lse,
                                        int32_t* idx_out, dsa_stream_t stream);
 
+/* Cache writers -- the prolog side of a step: new tokens into the paged caches.
+ * "Large Language Model Inference Acceleration in Practice", section 3.2 (the
+ * indexer prolog normalises K and updates the key cache) and section 4 (FP8
+ * index keys and KV cache); "Day0 Inference Adaptation and Performance
+ * Optimization for Kimi K3.1 Pro", section 4.  New token t goes to the cache
+ * row of position q_pos[t] in sequence q_seq[t] (page table as above); the
+ * positions of one call must be distinct.  A position or page out of range is
+ * skipped and flagged (dsa_check_status).
+ *
+ * Index keys: k_new device [T, D_I] fp32 or bf16 (src_dtype); per token
+ *   scale = amax_i |k_new[t,i]| / 448 in fp32 (1 when the row is all zero),
+ *   code_i = the E4M3 value nearest to k_new[t,i] / scale (fp32 quotient), ties
+ *   to the even code, magnitudes beyond 448 saturated;
+ *   writes k_cache[row, 0:D_I] (uint8, row stride D_I) and k_scale[row] (fp32),
+ *   the formats dsa_indexer_scores reads.  4 <= D_I <= 1024, D_I % 4 == 0. */
+dsa_status_t dsa_index_cache_append(const dsa_seq_desc_t* seq, int32_t D_I, dsa_dtype_t src_dtype,
+                                    const void* k_new, uint8_t* k_cache, float* k_scale, dsa_stream_t stream);
+/* Latent rows: kv_new device [T, d_latent + d_rope], bf16 (fp32 when
+ *   mla->dtype == DSA_F32); mla gives d_latent, d_rope, the cache dtype and
+ *   row_bytes (its q and kv_cache fields are not used); the rows are written to
+ *   kv_cache:
+ *    DSA_BF16 / DSA_F32: the row copied (its byte size and row_bytes multiples of 16);
+ *    DSA_E4M3 (656-byte rows, 512 + 64): the 512 latent values quantised as one
+ *      vector by the rule above into [0,512), the fp32 scale at [512,516), zero
+ *      bytes at [516,528), the 64 bf16 rope values copied to [528,656). */
+dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, const void* kv_new,
+                                     void* kv_cache, dsa_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK (dsa_last_error() names the
  * flags), or DSA_ERR_CUDA if the stream itself reports an error. */
