@@ -309,11 +309,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
   tc_fence_after();
 
   if (warp < kProducerWarps) {
-    // ------------------------------------------------ producers: warp w owns tiles j = w mod 4
+    // ------------------------------------------------ producers: warp w < S owns stage w and
+    // loads its tiles j = w mod S.  (A stage's empty barrier must be waited on by
+    // one warp in phase order: a warp waiting two phases ahead of the barrier's
+    // pending phase would see that parity as completed and overwrite a tile in use.)
     const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);
     const int32_t* bt = p.seq.block_table + static_cast<int64_t>(b) * p.seq.bt_stride;
     const int32_t* idx = p.a.idx + static_cast<int64_t>(t) * K;
-    for (int j = warp; j < ntiles; j += kProducerWarps) {
+    for (int j = warp; warp < S && j < ntiles; j += S) {
       const int st = j % S;
       // lane r resolves tile row r (index -> page -> cache row) before the wait
       int64_t my_row = -1;

@@ -32,6 +32,8 @@ CASES = {
     "qlen5": ("decode_b1", dict(ctx=[700], q_len=5, K=64)),
     "qlen8": ("decode_b1", dict(ctx=[900], q_len=8, K=128)),
     "qlen8_b3_shuffled": ("decode_b64", dict(ctx_range=(300, 2500), B=3, q_len=8, K=256)),
+    # FP8 cache at a batch where every query gets one row slice: 64 tiles per CTA
+    "fp8_b80_single_slice": ("decode_b4_long", dict(ctx=[2100] * 80, B=80, K=2048)),
 }
 
 
@@ -195,6 +197,20 @@ def test_attention_split_equals_single_slice(dev):
     # the same tolerances (they round P against different running maxima)
     assert np.abs(a_out - b_out).max() <= 2e-2 and np.abs(a_out - b_out).mean() <= 2e-3
     assert np.abs(a_lse - b_lse).max() <= 2e-3
+
+
+@pytest.mark.parametrize("name,over", [("decode_b4_long", dict(ctx=[5000], B=1, K=2048)),
+                                       ("decode_b1", dict(ctx=[6000], K=2048))])
+def test_attention_single_slice_many_tiles(dev, name, over):
+    """No workspace: one row slice per query, so each CTA streams all of its
+    2048 rows through the stage ring (every stage reused many times)."""
+    wl = W.make(name, seed=8, **over)
+    run = P.Run(wl, dev)
+    idx = O.topk(O.indexer_scores(wl), wl.q_pos, wl.K)
+    g_out, g_lse, plan = run.attn(idx, workspace=False)
+    assert "split=1," in plan, plan
+    o_out, o_lse = O.sparse_mla_attn(wl, idx)
+    P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
 
 
 # --------------------------------------------------------------------------- device checks
