@@ -641,14 +641,17 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
 // that select nothing are zeroed.  (On this GPU a tile::gather4 TMA producer
 // reached ~12 GB/s per SM and cp.async gathers ~60 GB/s.)
 //
-// MMA warp (warp 12): Q K^T_{j+1} (N = 48 rows) as soon as the softmax has read
-// S_j and tile j+1 has landed, so it runs during the softmax of tile j; P V_j
-// (N = 256 value dims, P read from TMEM) as soon as P_j is written.  An M=128
+// MMA warps: warp 12 issues Q K^T_{j+1} (N = 48 rows) as soon as the softmax
+// has read S_j and tile j+1 has landed, so it runs during the softmax of tile
+// j; warp 13 issues P V_j (N = 256 value dims, P read from TMEM) as soon as P_j
+// is written.  (One warp issuing both made a ready P V wait behind the issue
+// of a Q K^T and vice versa: the issuing thread blocks until the tensor pipe
+// has taken the instructions.)  An M=128
 // K=16 step whose A operand (the query) sits in shared memory reads 6 KB of
 // shared memory and takes ~53 clk, one with A in TMEM ~36 clk, so the first 320
 // query dims live in TMEM.
 //
-// Softmax (warps 13-16): one thread per head (its TMEM lane), 48 logits a tile,
+// Softmax (warps 14-17): one thread per head (its TMEM lane), 48 logits a tile,
 // running max moved (and O rescaled in TMEM) only when it grows by more than
 // 2^8.
 //
@@ -674,8 +677,10 @@ constexpr int kT48Used = kT48OffMisc + 16;                     // bytes used fro
 // much slack is requested for it (the kernel checks that it sufficed)
 constexpr int kT48Slack = 232448 - kT48Used;
 constexpr int kT48SmemBytes = kT48Used + kT48Slack;
-constexpr int kT48Threads = 544;   // warps 0-11 producers, warp 12 MMA, warps 13-16 softmax
-constexpr int kT48Mma = 12;
+constexpr int kT48Threads = 576;   // warps 0-11 producers, 12 Q K^T, 13 P V, 14-17 softmax
+constexpr int kT48Mma = 12;        // Q K^T issuer; also allocates TMEM
+constexpr int kT48Pv = 13;         // P V issuer
+constexpr int kT48Soft = 14;       // first softmax warp
 constexpr int kT48Producers = 4;   // warps per stage group
 constexpr uint32_t kT48ColS = 0, kT48ColP = 64, kT48ColQ = 96, kT48ColO = 256;
 constexpr uint32_t kIdescS48 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, kBR48);
@@ -760,10 +765,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = misc[0];
-  // The producers start gathering tiles at once; warps 12-16 stage the query
+  // The producers start gathering tiles at once; warps 12-17 stage the query
   // meanwhile (dims [320, 576) in shared memory, [0, 320) in TMEM) and meet at
   // named barrier 1 before the first MMA.
-  constexpr uint32_t kQBar = 1, kQBarThreads = 5 * 32;
+  constexpr uint32_t kQBar = 1, kQBarThreads = 6 * 32;
   if (warp >= kT48Mma) {
     const uint32_t qbase = smem_u32(sm + kT48OffQ);
     constexpr int kChunks = (kDqk - kT48QTmemDims) / 8;
@@ -773,7 +778,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     }
     cp_async_commit();
   }
-  if (warp > kT48Mma) {
+  if (warp >= kT48Soft) {
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
@@ -880,21 +885,52 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
     }
-  } else if (warp == kT48Mma) {
-    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
-    const uint64_t dq0 = make_sdesc(smem_u32(sm + kT48OffQ), 16, 1024, kLayoutSw128);
-    const uint64_t dk0 = make_sdesc(smem_u32(sm + kT48OffKV), 16, 1024, kLayoutSw128);
-    const uint64_t dv0 = make_sdesc(smem_u32(sm + kT48OffKV) + c * 4 * kBR48 * 128, kBR48 * 128, 1024, kLayoutSw128);
-    int next_s = 0, next_pv = 0;
-    uint32_t spins = 0;
-    uint64_t stall_t0 = 0;
-    while (next_pv < ntiles) {
-      bool progress = false;
-      // P V_j as soon as P_j is written (it frees stage j)
-      const bool p_ready = next_pv < next_s && mbar_test_wait(smem_u32(pfull), next_pv & 1);
-      if (__shfl_sync(0xffffffffu, p_ready, 0)) {
+  } else if (warp == kT48Mma || warp == kT48Pv) {
+    // ------------------------------------------------ MMA issuers (whole warp, elected lane issues)
+    // Bounded polls on the non-suspending test_wait: these waits are on the
+    // critical path of every tile.
+    auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
+      const uint32_t addr = smem_u32(bar);
+      uint64_t t0 = 0;
+      for (uint32_t it = 0;; ++it) {
+        if (__shfl_sync(0xffffffffu, mbar_test_wait(addr, parity) ? 1 : 0, 0)) return true;
+        if ((it & 255u) == 255u) {
+          if (__shfl_sync(0xffffffffu, *abort_flag, 0)) return false;
+          const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
+          if (t0 == 0) {
+            t0 = now;
+          } else if (now - t0 > kWaitLimitNs) {
+            if (lane == 0) {
+              atomicOr(&g_status_attn, kDevTimeout);
+              *abort_flag = 1;
+            }
+            return false;
+          }
+        }
+      }
+    };
+    if (warp == kT48Mma) {
+      const uint64_t dq0 = make_sdesc(smem_u32(sm + kT48OffQ), 16, 1024, kLayoutSw128);
+      const uint64_t dk0 = make_sdesc(smem_u32(sm + kT48OffKV), 16, 1024, kLayoutSw128);
+      for (int j = 0; j < ntiles; ++j) {
+        // Q K^T_j: tile j has landed and the softmax has read S_{j-1}
+        if (j >= 1 && !poll(sfree, (j - 1) & 1)) break;
+        if (!poll(&full[j % kT48Stages], (j / kT48Stages) & 1)) break;
         tc_fence_after();
-        const int j = next_pv;
+        if (elect_one()) {
+          t48_issue_s(tmem, dq0, dk0 + static_cast<uint64_t>(((j % kT48Stages) * kTile48Bytes) >> 4));
+          umma_commit(sfull);
+        }
+        __syncwarp();
+      }
+    } else {
+      const uint64_t dv0 = make_sdesc(smem_u32(sm + kT48OffKV) + c * 4 * kBR48 * 128, kBR48 * 128, 1024, kLayoutSw128);
+      for (int j = 0; j < ntiles; ++j) {
+        // P V_j as soon as P_j is written.  Its commits also cover Q K^T_j (complete
+        // before the softmax wrote P_j), so empty[st] frees the whole stage and
+        // ofull marks every MMA of the CTA done.
+        if (!poll(pfull, j & 1)) break;
+        tc_fence_after();
         const uint64_t dv = dv0 + static_cast<uint64_t>(((j % kT48Stages) * kTile48Bytes) >> 4);
         if (elect_one()) {
 #pragma unroll
@@ -906,43 +942,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           if (j == ntiles - 1) umma_commit(ofull);
         }
         __syncwarp();
-        ++next_pv;
-        progress = true;
-      }
-      // Q K^T_j as soon as tile j has landed and the softmax has read S_{j-1}
-      const bool s_ready = next_s < ntiles &&
-                           (next_s == 0 || mbar_test_wait(smem_u32(sfree), (next_s - 1) & 1)) &&
-                           mbar_test_wait(smem_u32(&full[next_s % kT48Stages]), (next_s / kT48Stages) & 1);
-      if (__shfl_sync(0xffffffffu, s_ready, 0)) {
-        tc_fence_after();
-        const int j = next_s;
-        const uint64_t dk = dk0 + static_cast<uint64_t>(((j % kT48Stages) * kTile48Bytes) >> 4);
-        if (elect_one()) {
-          t48_issue_s(tmem, dq0, dk);
-          umma_commit(sfull);
-        }
-        __syncwarp();
-        ++next_s;
-        progress = true;
-      }
-      if (progress) {
-        stall_t0 = 0;
-      } else if ((++spins & 63u) == 0u) {
-        if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-        const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
-        if (stall_t0 == 0) {
-          stall_t0 = now;
-        } else if (now - stall_t0 > kWaitLimitNs) {
-          if (lane == 0) {
-            atomicOr(&g_status_attn, kDevTimeout);
-            *abort_flag = 1;
-          }
-          break;
-        }
       }
     }
   } else {
-    // ------------------------------------------------ softmax + epilogue (warps 13-16)
+    // ------------------------------------------------ softmax + epilogue (warps 14-17)
     const int quarter = warp & 3;
     const int h = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
