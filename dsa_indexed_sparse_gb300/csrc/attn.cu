@@ -203,7 +203,7 @@ struct TcAttnParams {
   MlaArgs a;
   int32_t n_split;       // row slices per query
   int32_t rows_per_split;
-  float* ws_o;           // [n_split, T, H, 512] fp32 partials (n_split > 1)
+  uint16_t* ws_o;        // [n_split, T, H, 512] bf16 partials (n_split > 1), each normalised by its own sum
   float* ws_lse;         // [n_split, T, H]
 };
 
@@ -585,37 +585,30 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
       // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB per warp
       const uint32_t stg = smem_u32(sm + C::kOffKV) + quarter * 4096;
       const int64_t th0 = static_cast<int64_t>(t) * kH + quarter * 32;   // this warp's first head
-      if (p.n_split == 1) {
-        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + c * kDvHalf);
+      // bf16 rows of this warp's 32 heads: the output, or this slice's partial
+      // (normalised by its own sum; the combine weights it by its LSE)
+      const bool part = p.n_split > 1;
+      const int64_t row0 = part ? static_cast<int64_t>(split) * p.seq.T * kH + th0 : th0;
+      uint8_t* out = reinterpret_cast<uint8_t*>(part ? p.ws_o : static_cast<uint16_t*>(p.a.out)) +
+                     (row0 * kDv + c * kDvHalf) * 2;
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tmem + lane_off + C::kColO + cc * 64, o0);
-          tmem_ld32(tmem + lane_off + C::kColO + cc * 64 + 32, o1);
-          tmem_ld_wait();
-          uint32_t pk[32];
+      for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tmem + lane_off + C::kColO + cc * 64, o0);
+        tmem_ld32(tmem + lane_off + C::kColO + cc * 64 + 32, o1);
+        tmem_ld_wait();
+        uint32_t pk2[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            pk[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
-            pk[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
-          }
-          warp_store_rows128(stg, pk, out + cc * 128, kDv * 2, lane);
+        for (int i = 0; i < 16; ++i) {
+          pk2[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+          pk2[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
         }
-        if (c == 0 && p.a.lse) p.a.lse[th] = lse;
-      } else {
-        const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
-        uint8_t* out = reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<int64_t>(split) * p.seq.T * kH + th0) * kDv +
-                                                  c * kDvHalf);
-#pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + C::kColO + cc * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
-          warp_store_rows128(stg, o, out + cc * 128, kDv * 4, lane);
-        }
-        if (c == 0) p.ws_lse[sth] = lse;
+        warp_store_rows128(stg, pk2, out + cc * 128, kDv * 2, lane);
+      }
+      if (part) {
+        if (c == 0) p.ws_lse[static_cast<int64_t>(split) * p.seq.T * kH + th] = lse;
+      } else if (c == 0 && p.a.lse) {
+        p.a.lse[th] = lse;
       }
     }
   }
@@ -1044,37 +1037,30 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       // all MMAs are complete (ofull), so the stage buffers are idle: 4 KB per warp
       const uint32_t stg = smem_u32(sm + kT48OffKV) + quarter * 4096;
       const int64_t th0 = static_cast<int64_t>(t) * kH + quarter * 32;   // this warp's first head
-      if (p.n_split == 1) {
-        uint8_t* out = reinterpret_cast<uint8_t*>(static_cast<__nv_bfloat16*>(p.a.out) + th0 * kDv + c * kDvHalf);
+      // bf16 rows of this warp's 32 heads: the output, or this slice's partial
+      // (normalised by its own sum; the combine weights it by its LSE)
+      const bool part = p.n_split > 1;
+      const int64_t row0 = part ? static_cast<int64_t>(split) * p.seq.T * kH + th0 : th0;
+      uint8_t* out = reinterpret_cast<uint8_t*>(part ? p.ws_o : static_cast<uint16_t*>(p.a.out)) +
+                     (row0 * kDv + c * kDvHalf) * 2;
 #pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 64; ++cc) {
-          uint32_t o0[32], o1[32];
-          tmem_ld32(tmem + lane_off + kT48ColO + cc * 64, o0);
-          tmem_ld32(tmem + lane_off + kT48ColO + cc * 64 + 32, o1);
-          tmem_ld_wait();
-          uint32_t pk2[32];
+      for (int cc = 0; cc < kDvHalf / 64; ++cc) {
+        uint32_t o0[32], o1[32];
+        tmem_ld32(tmem + lane_off + kT48ColO + cc * 64, o0);
+        tmem_ld32(tmem + lane_off + kT48ColO + cc * 64 + 32, o1);
+        tmem_ld_wait();
+        uint32_t pk2[32];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            pk2[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
-            pk2[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
-          }
-          warp_store_rows128(stg, pk2, out + cc * 128, kDv * 2, lane);
+        for (int i = 0; i < 16; ++i) {
+          pk2[i] = pack_bf16x2(__uint_as_float(o0[2 * i]) * inv, __uint_as_float(o0[2 * i + 1]) * inv);
+          pk2[16 + i] = pack_bf16x2(__uint_as_float(o1[2 * i]) * inv, __uint_as_float(o1[2 * i + 1]) * inv);
         }
-        if (c == 0 && p.a.lse) p.a.lse[th] = lse;
-      } else {
-        const int64_t sth = static_cast<int64_t>(split) * p.seq.T * kH + th;
-        uint8_t* out = reinterpret_cast<uint8_t*>(p.ws_o + (static_cast<int64_t>(split) * p.seq.T * kH + th0) * kDv +
-                                                  c * kDvHalf);
-#pragma unroll 1
-        for (int cc = 0; cc < kDvHalf / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32(tmem + lane_off + kT48ColO + cc * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
-          warp_store_rows128(stg, o, out + cc * 128, kDv * 4, lane);
-        }
-        if (c == 0) p.ws_lse[sth] = lse;
+        warp_store_rows128(stg, pk2, out + cc * 128, kDv * 2, lane);
+      }
+      if (part) {
+        if (c == 0) p.ws_lse[static_cast<int64_t>(split) * p.seq.T * kH + th] = lse;
+      } else if (c == 0 && p.a.lse) {
+        p.a.lse[th] = lse;
       }
     }
   }
@@ -1089,16 +1075,17 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 }
 
 // Merges row slices: out[t,h,:] = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max_s lse_s);
-// lse = max + log sum_s w_s.  One CTA per (query, group of 8 heads); a warp per
-// head, each lane owning 4 float4 columns; the slices' loads are issued four
-// slices at a time so that 16 loads per lane are in flight.
+// lse = max + log sum_s w_s.  The partials O_s are bf16 rows, each normalised by
+// its own slice's sum.  One CTA per (query, group of 8 heads); a warp per head,
+// each lane owning 16 value dims (two 16-byte vectors per slice); the loads of
+// four slices are issued before their sums.
 constexpr int kCombineHeads = 8;
 __global__ void __launch_bounds__(256)
-    attn_combine_kernel(const float* ws_o, const float* ws_lse, int n_split, int T,
+    attn_combine_kernel(const uint16_t* ws_o, const float* ws_lse, int n_split, int T,
                         __nv_bfloat16* out, float* lse_out) {
   grid_dep_wait();
   extern __shared__ float wts[];  // [kCombineHeads][n_split]
-  constexpr int H = kH, kV4 = kDv / 4 / 32;   // float4 per lane
+  constexpr int H = kH;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * kCombineHeads + warp;
@@ -1120,48 +1107,37 @@ __global__ void __launch_bounds__(256)
   if (lane == 0 && lse_out) lse_out[static_cast<int64_t>(t) * H + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
   const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const int64_t th = static_cast<int64_t>(t) * H + h;
-  const int64_t slice_stride = static_cast<int64_t>(T) * H * (kDv / 4);   // in float4
-  const float4* src = reinterpret_cast<const float4*>(ws_o) + th * (kDv / 4) + lane;
-  float4 acc[kV4];
+  const int64_t slice_stride = static_cast<int64_t>(T) * H * (kDv / 8);   // in 16-byte vectors
+  const uint4* src = reinterpret_cast<const uint4*>(ws_o) + th * (kDv / 8) + 2 * lane;
+  float acc[16];
 #pragma unroll
-  for (int k = 0; k < kV4; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int k = 0; k < 16; ++k) acc[k] = 0.f;
+  auto add = [&](const uint4& v0, const uint4& v1, float ww) {
+    const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      acc[2 * k] = fmaf(ww, __uint_as_float(u[k] << 16), acc[2 * k]);
+      acc[2 * k + 1] = fmaf(ww, __uint_as_float(u[k] & 0xFFFF0000u), acc[2 * k + 1]);
+    }
+  };
   int s = 0;
   for (; s + 4 <= n_split; s += 4) {
-    float4 v[4][kV4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int k = 0; k < kV4; ++k) v[u][k] = __ldcs(src + (s + u) * slice_stride + 32 * k);
+    uint4 v[4][2];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const float ww = w[s + u];
-#pragma unroll
-      for (int k = 0; k < kV4; ++k) {
-        acc[k].x = fmaf(ww, v[u][k].x, acc[k].x);
-        acc[k].y = fmaf(ww, v[u][k].y, acc[k].y);
-        acc[k].z = fmaf(ww, v[u][k].z, acc[k].z);
-        acc[k].w = fmaf(ww, v[u][k].w, acc[k].w);
-      }
+      v[u][0] = __ldcs(src + (s + u) * slice_stride);
+      v[u][1] = __ldcs(src + (s + u) * slice_stride + 1);
     }
-  }
-  for (; s < n_split; ++s) {
-    const float ww = w[s];
 #pragma unroll
-    for (int k = 0; k < kV4; ++k) {
-      const float4 v = __ldcs(src + s * slice_stride + 32 * k);
-      acc[k].x = fmaf(ww, v.x, acc[k].x);
-      acc[k].y = fmaf(ww, v.y, acc[k].y);
-      acc[k].z = fmaf(ww, v.z, acc[k].z);
-      acc[k].w = fmaf(ww, v.w, acc[k].w);
-    }
+    for (int u = 0; u < 4; ++u) add(v[u][0], v[u][1], w[s + u]);
   }
+  for (; s < n_split; ++s) add(__ldcs(src + s * slice_stride), __ldcs(src + s * slice_stride + 1), w[s]);
+  uint32_t pk[8];
 #pragma unroll
-  for (int k = 0; k < kV4; ++k) {
-    __nv_bfloat162 lo = __floats2bfloat162_rn(acc[k].x * inv, acc[k].y * inv);
-    __nv_bfloat162 hi = __floats2bfloat162_rn(acc[k].z * inv, acc[k].w * inv);
-    reinterpret_cast<uint2*>(out + th * kDv)[lane + 32 * k] =
-        make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
-  }
+  for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
+  uint4* dst = reinterpret_cast<uint4*>(out + th * kDv) + 2 * lane;
+  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
 }
 
 bool tc_supported(const SeqArgs& seq, const MlaArgs& a) {
@@ -1192,7 +1168,7 @@ size_t attn_workspace_bytes(const SeqArgs& seq, const MlaArgs& a, int num_sms) {
   if (!tc_supported(seq, a) || seq.T == 0) return 0;
   const int split = choose_split(seq, a, num_sms);
   if (split <= 1) return 0;
-  const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(float);
+  const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(uint16_t);
   const size_t l = static_cast<size_t>(split) * seq.T * kH * sizeof(float);
   return ((o + 255) / 256) * 256 + ((l + 255) / 256) * 256;
 }
@@ -1215,8 +1191,8 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     split = (a.K + rps - 1) / rps;  // every slice non-empty
     TcAttnParams p{seq, a, split, rps, nullptr, nullptr};
     if (split > 1) {
-      const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(float);
-      p.ws_o = static_cast<float*>(workspace);
+      const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(uint16_t);
+      p.ws_o = static_cast<uint16_t*>(workspace);
       p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o + 255) / 256) * 256);
     }
     static std::once_flag once;
@@ -1247,7 +1223,7 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     if (split > 1) {
       const size_t smem = static_cast<size_t>(split) * kCombineHeads * sizeof(float);
       e = launch_kernel(attn_combine_kernel, dim3(seq.T, kH / kCombineHeads), dim3(256), smem, env.stream, true, 1,
-                     static_cast<const float*>(p.ws_o), static_cast<const float*>(p.ws_lse), split, seq.T,
+                     static_cast<const uint16_t*>(p.ws_o), static_cast<const float*>(p.ws_lse), split, seq.T,
                      static_cast<__nv_bfloat16*>(a.out), a.lse);
       if (e != cudaSuccess) return e;
       *plan += "+attn_combine";
