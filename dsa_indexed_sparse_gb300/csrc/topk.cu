@@ -135,6 +135,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     for (int i = 4 * n4 + tid; i < len; i += kThreads) keys_s[i] = order_key(__ldg(row + i));
   }
 
+  // Warp w owns slice positions [w*wl, w*wl + wl) (wl a multiple of 128) in both
+  // the digit passes and the compaction, so its per-warp histograms also give it
+  // the counts the compaction needs: keys above the threshold and keys equal to it.
+  const int warp = tid >> 5;
+  const int wl = ((len + kWarps - 1) / kWarps + 127) & ~127;
+  const int wlo = min(len, warp * wl), whi = min(len, wlo + wl);
+  uint32_t n_gt = 0, n_eq = 0;
   uint32_t prefix = 0, pmask = 0;
   uint32_t rem = static_cast<uint32_t>(K);  // how many of the keys matching `prefix` to keep
   for (int pass = 0; pass < 4; ++pass) {
@@ -148,25 +155,29 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     }
     __syncthreads();
     {
-      uint32_t* wh = whist[tid >> 5];
+      uint32_t* wh = whist[warp];
       auto count = [&](uint32_t k) {
         if ((k & pmask) == prefix) atomicAdd(&wh[(k >> shift) & 255u], 1u);
       };
-      const int n4 = len >> 2;
-      for (int q = tid; q < n4; q += kThreads) {
-        uint4 k4;
-        if (cached) {
-          k4 = reinterpret_cast<const uint4*>(keys_s)[q];
+      for (int b = wlo; b < whi; b += 128) {
+        const int i4 = b + 4 * lane;   // this lane's four consecutive keys
+        if (i4 + 3 < whi) {
+          uint4 k4;
+          if (cached) {
+            k4 = reinterpret_cast<const uint4*>(keys_s)[i4 >> 2];
+          } else {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(row + i4));
+            k4 = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+          }
+          count(k4.x);
+          count(k4.y);
+          count(k4.z);
+          count(k4.w);
         } else {
-          const float4 v = __ldg(reinterpret_cast<const float4*>(row) + q);
-          k4 = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+          for (int e = 0; e < 4; ++e)
+            if (i4 + e < whi) count(key_at(i4 + e));
         }
-        count(k4.x);
-        count(k4.y);
-        count(k4.z);
-        count(k4.w);
       }
-      for (int i = 4 * n4 + tid; i < len; i += kThreads) count(key_at(i));
     }
     __syncthreads();
     for (int b = tid; b < 256; b += kThreads) {
@@ -177,8 +188,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     }
     cluster.sync();  // every slice's histogram complete
     for (int i = tid; i < 256; i += kThreads) {
+      // all ranks' loads in flight at once (the loop is unrolled to the largest cluster)
+      uint32_t part[kMaxCluster];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) part[r] = r < CL ? cluster.map_shared_rank(hist, r)[i] : 0u;
       uint32_t v = 0;
-      for (int r = 0; r < CL; ++r) v += cluster.map_shared_rank(hist, r)[i];
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r) v += part[r];
       ghist[i] = v;
     }
     __syncthreads();
@@ -211,28 +227,31 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       }
     }
     __syncthreads();  // s_* visible in this CTA
+    {
+      // this warp's keys above the chosen digit (above the threshold for good)
+      // and on it (equal to the threshold so far)
+      const uint32_t d = s_digit;
+      uint32_t above = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t bin = 8u * lane + j;
+        above += bin > d ? whist[warp][bin] : 0u;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
+      n_gt += above;
+      n_eq = whist[warp][d];
+    }
     prefix |= s_digit << shift;
     pmask |= 255u << shift;
     rem = s_rem;
     const bool whole = (s_bucket == rem);
-    __syncthreads();  // s_* are rewritten next pass
+    __syncthreads();  // s_* and the per-warp histograms are rewritten next pass
     if (whole) break;  // cluster-uniform (same histogram everywhere)
   }
 
-  // Ordered compaction.  Warp w owns slice positions [w*wl, w*wl + wl), wl a
-  // multiple of 32, and walks them 32 at a time.
-  const int warp = tid >> 5;
-  const int wl = ((len + kWarps - 1) / kWarps + 31) & ~31;
-  const int wlo = min(len, warp * wl), whi = min(len, wlo + wl);
+  // Ordered compaction over the same warp ranges, 32 positions at a time.
   const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t n_eq = 0, n_gt = 0;
-  for (int b = wlo; b < whi; b += 32) {
-    const int i = b + lane;
-    const uint32_t km = i < whi ? (key_at(i) & pmask) : 0u;
-    const bool in = i < whi;
-    n_eq += __popc(__ballot_sync(0xffffffffu, in && km == prefix));
-    n_gt += __popc(__ballot_sync(0xffffffffu, in && km > prefix));
-  }
   uint32_t eq_w, slice_eq, gt_w, slice_gt;
   warp_offsets(n_eq, scan_buf, &eq_w, &slice_eq);
   __syncthreads();
@@ -245,12 +264,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   // Earlier slices: their keys equal to the threshold (for this slice's ranks)
   // and how many of their keys are selected (for this slice's output offset).
   uint32_t eq_before = 0, sel_before = 0;
-  for (int r = 0; r < rank; ++r) {
-    const uint32_t* pc = cluster.map_shared_rank(s_counts, r);
-    const uint32_t e = pc[0], g = pc[1];
-    sel_before += g + (eq_before >= rem ? 0u : min(e, rem - eq_before));
-    eq_before += e;
+  uint32_t ce[kMaxCluster], cg[kMaxCluster];
+#pragma unroll
+  for (int r = 0; r < kMaxCluster; ++r) {
+    const uint32_t* pc = cluster.map_shared_rank(s_counts, r < rank ? r : 0);
+    ce[r] = r < rank ? pc[0] : 0u;
+    cg[r] = r < rank ? pc[1] : 0u;
   }
+#pragma unroll
+  for (int r = 0; r < kMaxCluster; ++r) {
+    sel_before += cg[r] + (eq_before >= rem ? 0u : min(ce[r], rem - eq_before));
+    eq_before += ce[r];
+  }
+  // peers' counts are read: signal that, and wait for the others only before exit
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   // this warp's first equal-key rank and first output slot
   uint32_t eq_rank = eq_before + eq_w;
   uint32_t pos = sel_before + gt_w + (eq_before >= rem ? 0u : min(eq_w, rem - eq_before));
@@ -267,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     pos += __popc(selm);
   }
   grid_dep_launch();  // this CTA's work is done: the next kernel may launch
-  cluster.sync();  // peers may still read s_counts
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers may still read s_counts
 }
 
 }  // namespace
