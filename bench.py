@@ -255,6 +255,9 @@ def main():
                     help="profiling mode: run this stage --reps times on one input copy and exit "
                          "(no timing, no JSON line); for ncu captures")
     ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--prefill-len", type=int, default=None,
+                    help="profiling mode only: run the prefill recipe at this many tokens (a small "
+                         "case of the same kernels for profiler captures)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -295,7 +298,13 @@ def main():
     peaks = load_peaks()
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
-    wl = W.make(args.workload, seed=0)
+    if args.prefill_len is not None:
+        if not (args.stage and args.workload == "prefill_16k"):
+            ap.error("--prefill-len needs --stage and --workload prefill_16k")
+        n = args.prefill_len
+        wl = W.make(args.workload, seed=0, ctx=[n], q_len=n)
+    else:
+        wl = W.make(args.workload, seed=0)
     if args.stage:
         return profile_stage(torch, dsa, W, wl, dev, args.stage, args.reps)
     alg = algorithmic(wl)

@@ -16,8 +16,9 @@
 //    columns, K = 128.  Keys arrive page by page through TMA (128-byte swizzle)
 //    and their per-key scales through one warp-wide cp.async per tile (a TMA op
 //    costs ~0.1 us of issue time on this GPU, which paced the whole ring when
-//    the scales took two more); accumulators live in TMEM (double buffered) and 4 epilogue warps turn each
-//    key's row of G*64 dot products into G scores with an in-thread head sum.
+//    the scales took two more); accumulators live in TMEM (double buffered) and
+//    4*G epilogue warps, one per (query, TMEM lane quarter), turn each key's 64
+//    dot products of a query into its score with an in-thread head sum.
 //    Persistent: every CTA takes an equal contiguous share of the (group, key
 //    tile) list, computed on the device from q_pos.
 //  * indexer_generic_kernel -- CUDA cores, any H_I/D_I, fp32 or e4m3.
@@ -89,14 +90,14 @@ constexpr int kTcDim = 128;        // D_I (bytes per key row)
 constexpr int kTcKeys = 128;       // keys per tile = UMMA M
 constexpr int kTcPage = 64;        // tokens per page
 constexpr int kTcStages = 6;       // key-tile ring depth (16 KB each)
-// warp 0 TMA, warp 1 MMA, then the epilogue: 4 warps (one per TMEM lane
-// quarter) for a single query, 8 (two per quarter, splitting the query group)
-// for groups of 2 or 4 -- there the ReLU-weighted head sums, not the MMAs, set
-// the tile rate.
+// warp 0 TMA, warp 1 MMA, then the epilogue: one warp per (query of the group,
+// TMEM lane quarter), so 4*G warps.  The ReLU-weighted head sums (two CUDA-core
+// operations per key, query and head) cost about as much issue time as the
+// MMAs' tensor time, so they get every warp slot the register budget allows.
 template <int G>
 struct TcWarps {
-  static constexpr int kEpiThreads = G == 1 ? 128 : 256;
-  static constexpr int kThreads = 64 + kEpiThreads;
+  static constexpr int kEpiWarps = 4 * G;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
 };
 
 template <int G>
@@ -107,14 +108,14 @@ struct TcCfg {
   static constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128u : ((2 * N <= 256) ? 256u : 512u);
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kOffStages + kTcStages * kStageBytes;
-  static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [2][G*64]
-  static constexpr int kOffScale = kOffWq + 2 * N * 4;    // float [stages][128] key scales
+  static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [4G][64]: each epilogue warp's head weights
+  static constexpr int kOffScale = kOffWq + TcWarps<G>::kEpiWarps * kTcHeads * 4;  // float [stages][128] key scales
   static constexpr int kOffValid = kOffScale + kTcStages * kTcKeys * 4;  // uint32 [stages]
   static constexpr int kOffBar = kOffValid + kTcStages * 4 + 8;
   // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2]
   static constexpr int kNumBars = 2 * kTcStages + 8;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, sched[4]
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, sched[2], red[one per warp]
+  static constexpr int kSmemBytes = kOffMisc + 256 + 1024;  // + alignment slack
   static constexpr uint32_t kIdesc = make_idesc(kFmtE4M3, kFmtE4M3, false, false, kTcKeys, N);
 };
 
@@ -184,7 +185,8 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
                       const __grid_constant__ CUtensorMap qmap, TcParams p) {
   using C = TcCfg<G>;
   constexpr int kTcThreads = TcWarps<G>::kThreads;
-  constexpr int kTcEpiThreads = TcWarps<G>::kEpiThreads;
+  constexpr int kEpiWarps = TcWarps<G>::kEpiWarps;
+  static_assert(4 + kTcThreads / 32 <= 64, "misc area holds one int per warp");
   grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       const int g = g0 + threadIdx.x;
       int nh;
       const int c = (g < p.n_groups) ? group_tiles<G>(p, g, &nh) : 0;
-      // inclusive scan within the block (6 warps)
+      // inclusive scan within the block
       int v = c;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -252,14 +254,14 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     const uint32_t full_count = 1u + (p.a.k_scale != nullptr ? 32u : 0u);
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&full[i], full_count);
-      // freed by the MMA (keys read) and by the epilogue (key scales read)
-      mbar_init(&empty[i], 1 + kTcEpiThreads);
+      // freed by the MMA (keys read) and by each epilogue warp (key scales read)
+      mbar_init(&empty[i], 1 + kEpiWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
       mbar_init(&qempty[i], 1);
       mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], kTcEpiThreads);
+      mbar_init(&accempty[i], kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -389,111 +391,104 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       __syncwarp();
     }
   } else {
-    // ------------------------------------------------ epilogue (warps 2..9)
+    // ------------------------------------------------ epilogue (warps 2 .. 2 + 4G - 1)
+    // Warp e reduces query j = e / 4 of every group over the 32 keys of TMEM lane
+    // quarter warp % 4.  Its head weights (w * q_scale) live in its own 64-float
+    // slice of shared memory; the next group's weights and positions are fetched
+    // into registers while the current group runs, so a group switch costs no
+    // global-memory round trip.
+    const int e = warp - 2;
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;             // which part of the query group (0 when G == 1)
-    const int jlo = G == 1 ? 0 : half * (G / 2);
-    const int jhi = G == 1 ? (half == 0 ? 1 : 0) : jlo + G / 2;
+    const int j = e >> 2;
     const int row = quarter * 32 + lane;          // key within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const int etid = threadIdx.x - 64;
+    float* wq = wq_s + e * kTcHeads;
     TileWalker<G> w;
     w.init(p, g_start, kt_start);
-    int cur_g = -1, gcount = 0;
-    int tq[G], qp[G];
-    int b = 0;
-    // After a failed wait a warp stops computing but keeps walking the tile list,
-    // so that every epilogue warp reaches the same named barriers.
-    bool dead = false;
+    int cur_g = -1, tq = 0, qp = -1;
+    // prefetched group: its first query's sequence, this warp's query's sequence
+    // and position, and lanes' two head weights and query scales
+    int pf_g = -1, pf_b = 0, pf_qs = 0, pf_qp = -1;
+    float pf_w0 = 0.f, pf_w1 = 0.f, pf_s0 = 1.f, pf_s1 = 1.f;
+    auto prefetch = [&](int g) {
+      pf_g = g;
+      const int t = g * G + j;
+      pf_b = __ldg(p.seq.q_seq + g * G);
+      pf_qs = pf_b;
+      pf_qp = -1;
+      pf_w0 = pf_w1 = 0.f;
+      pf_s0 = pf_s1 = 1.f;
+      if (t < p.seq.T) {
+        pf_qs = __ldg(p.seq.q_seq + t);
+        pf_qp = __ldg(p.seq.q_pos + t);
+        const int64_t o = static_cast<int64_t>(t) * kTcHeads + 2 * lane;
+        pf_w0 = __ldg(p.a.w + o);
+        pf_w1 = __ldg(p.a.w + o + 1);
+        if (p.a.q_scale) {
+          pf_s0 = __ldg(p.a.q_scale + o);
+          pf_s1 = __ldg(p.a.q_scale + o + 1);
+        }
+      }
+    };
     for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
       if (w.g != cur_g) {
-        const int wb = gcount & 1;
-        b = __ldg(p.seq.q_seq + w.g * G);
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          tq[j] = w.g * G + j;
-          qp[j] = -1;
-          if (tq[j] < p.seq.T) {
-            qp[j] = __ldg(p.seq.q_pos + tq[j]);
-            if (qp[j] >= p.seq.max_ctx) qp[j] = -1;
-            if (__ldg(p.seq.q_seq + tq[j]) != b) {
-              if (etid == 0) atomicOr(&g_status_indexer, kDevBadGroup);
-            }
-          }
+        if (pf_g != w.g) prefetch(w.g);
+        tq = w.g * G + j;
+        qp = (tq < p.seq.T && pf_qp < p.seq.max_ctx) ? pf_qp : -1;
+        if (tq < p.seq.T && pf_qs != pf_b && lane == 0) atomicOr(&g_status_indexer, kDevBadGroup);
+        if (pf_b < 0 || pf_b >= p.seq.B) {
+          if (lane == 0) atomicOr(&g_status_indexer, kDevBadIndex);
+          qp = -1;
         }
-        if (b < 0 || b >= p.seq.B) {
-          if (etid == 0) atomicOr(&g_status_indexer, kDevBadIndex);
-#pragma unroll
-          for (int j = 0; j < G; ++j) qp[j] = -1;
-          b = 0;
-        }
-        for (int i = etid; i < C::N; i += kTcEpiThreads) {
-          const int j = i / kTcHeads, h = i % kTcHeads;
-          float v = 0.f;
-          if (tq[j] < p.seq.T) {
-            const int64_t o = static_cast<int64_t>(tq[j]) * kTcHeads + h;
-            v = __ldg(p.a.w + o) * (p.a.q_scale ? __ldg(p.a.q_scale + o) : 1.f);
-          }
-          wq_s[wb * C::N + i] = v;
-        }
-        named_bar_sync(1, kTcEpiThreads);
+        // the previous group's tiles are done: this warp alone reads its slice
+        wq[2 * lane] = pf_w0 * pf_s0;
+        wq[2 * lane + 1] = pf_w1 * pf_s1;
+        __syncwarp();
         cur_g = w.g;
-        ++gcount;
+        if (w.g + 1 < p.n_groups) prefetch(w.g + 1);
       }
-      if (dead) continue;
-      const float* wq = wq_s + ((gcount - 1) & 1) * C::N;
       const int ab = static_cast<int>(it & 1);
-      const bool ok = mbar_wait(&accfull[ab], (it >> 1) & 1, &g_status_indexer, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) {
-        dead = true;
-        continue;
-      }
+      bool ok = mbar_wait(&accfull[ab], (it >> 1) & 1, &g_status_indexer, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // the stage (keys, scales, page validity) is still this tile's: the
-      // producer refills it only after this thread's arrival on empty[st]
+      // producer refills it only after this warp's arrival on empty[st]
       const int st = static_cast<int>(it % kTcStages);
-      const bool okf = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
-      if (!__all_sync(0xffffffffu, okf)) {
-        dead = true;
-        continue;
-      }
+      ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
       const int s = w.kt * kTcKeys + row;
       const uint32_t vmask = reinterpret_cast<const volatile uint32_t*>(sm + C::kOffValid)[st];
       const bool key_ok = s < w.nhist && ((vmask >> (row >> 6)) & 1u);
       const float sk = key_ok ? (p.a.k_scale ? reinterpret_cast<const float*>(sm + C::kOffScale)[st * kTcKeys + row] : 1.f)
                               : 0.f;
-      mbar_arrive(&empty[st]);
-#pragma unroll 1
-      for (int j = jlo; j < jhi; ++j) {
-        uint32_t v0[32], v1[32];
-        const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
-        tmem_ld32(col, v0);
-        tmem_ld32(col + 32, v1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+      // the 64 heads in two halves of 32 columns (fewer live registers: 18 warps
+      // leave 96 a thread); head weights as 16-byte broadcast loads
+      const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
+      const float4* w4 = reinterpret_cast<const float4*>(wq);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t v[32];
+        tmem_ld32(col + 32 * hh, v);
         tmem_ld_wait();
-        // head weights as 16-byte broadcast loads; four independent sums
-        const float4* w4 = reinterpret_cast<const float4*>(wq + j * kTcHeads);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 wv = w4[i];
-          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v0[4 * i]), 0.f), acc[0]);
-          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v0[4 * i + 1]), 0.f), acc[1]);
-          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v0[4 * i + 2]), 0.f), acc[2]);
-          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v0[4 * i + 3]), 0.f), acc[3]);
+        if (hh == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&accempty[ab]);   // the accumulator is in registers
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 wv = w4[8 + i];
-          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v1[4 * i]), 0.f), acc[0]);
-          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v1[4 * i + 1]), 0.f), acc[1]);
-          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v1[4 * i + 2]), 0.f), acc[2]);
-          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v1[4 * i + 3]), 0.f), acc[3]);
+          const float4 wv = w4[8 * hh + i];
+          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i]), 0.f), acc[0]);
+          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), acc[1]);
+          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), acc[2]);
+          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), acc[3]);
         }
-        const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-        if (key_ok && s <= qp[j]) p.a.scores[static_cast<int64_t>(tq[j]) * p.a.ld + s] = sum * sk;
       }
-      tc_fence_before();
-      mbar_arrive(&accempty[ab]);
+      const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+      if (key_ok && s <= qp) p.a.scores[static_cast<int64_t>(tq) * p.a.ld + s] = sum * sk;
     }
   }
 
