@@ -279,7 +279,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = misc[0];
   const int g_start = sched[0], kt_start = sched[1];
-  const int64_t ntiles = end - begin;
+  const int ntiles = static_cast<int>(end - begin);   // <= total, an int
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (warp 0)
@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     bool b_ok = false;
     uint32_t* valid_s = reinterpret_cast<uint32_t*>(sm + C::kOffValid);
     float* scale_s = reinterpret_cast<float*>(sm + C::kOffScale);
-    for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+    for (int it = 0; it < ntiles; ++it, w.advance(p)) {
       if (w.g != cur_g) {
         const int qb = qcount & 1;
         if (qcount >= 2) {
@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       const int32_t pid0 = __shfl_sync(0xffffffffu, my_page, lp0 - win);
       int32_t pid1 = __shfl_sync(0xffffffffu, my_page, min(lp0 + 1 - win, 31));
       if (lp0 + 1 >= npg) pid1 = -1;
-      const int st = static_cast<int>(it % kTcStages);
+      const int st = it % kTcStages;
       if (it >= kTcStages) {
         const bool ok = mbar_wait(&empty[st], ((it / kTcStages) - 1) & 1, &g_status_indexer, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     TileWalker<G> w;
     w.init(p, g_start, kt_start);
     int cur_g = -1, qcount = 0, qb = 0;
-    for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+    for (int it = 0; it < ntiles; ++it, w.advance(p)) {
       if (w.g != cur_g) {
         if (qcount > 0) {
           if (elect_one()) umma_commit(&qempty[qb]);  // previous group's MMAs release its Q
@@ -367,10 +367,10 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         cur_g = w.g;
         ++qcount;
       }
-      const int st = static_cast<int>(it % kTcStages);
+      const int st = it % kTcStages;
       bool ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const int ab = static_cast<int>(it & 1);
+      const int ab = it & 1;
       if (it >= 2) {
         ok = mbar_wait(&accempty[ab], ((it >> 1) - 1) & 1, &g_status_indexer, abort_flag);
         if (!__all_sync(0xffffffffu, ok)) break;
@@ -405,7 +405,10 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     float* wq = wq_s + e * kTcHeads;
     TileWalker<G> w;
     w.init(p, g_start, kt_start);
-    int cur_g = -1, tq = 0, qp = -1;
+    int cur_g = -1, qp = -1;
+    float* srow = p.a.scores;   // this warp's query's score row
+    const uint32_t valid_addr = smem_u32(sm + C::kOffValid);
+    const uint32_t scale_addr = smem_u32(sm + C::kOffScale) + row * 4;
     // prefetched group: its first query's sequence, this warp's query's sequence
     // and position, and lanes' two head weights and query scales
     int pf_g = -1, pf_b = 0, pf_qs = 0, pf_qp = -1;
@@ -430,44 +433,50 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         }
       }
     };
-    for (int64_t it = 0; it < ntiles; ++it, w.advance(p)) {
+    for (int it = 0; it < ntiles; ++it, w.advance(p)) {
       if (w.g != cur_g) {
         if (pf_g != w.g) prefetch(w.g);
-        tq = w.g * G + j;
+        const int tq = w.g * G + j;
         qp = (tq < p.seq.T && pf_qp < p.seq.max_ctx) ? pf_qp : -1;
+        srow = p.a.scores + static_cast<int64_t>(tq < p.seq.T ? tq : 0) * p.a.ld;
         if (tq < p.seq.T && pf_qs != pf_b && lane == 0) atomicOr(&g_status_indexer, kDevBadGroup);
         if (pf_b < 0 || pf_b >= p.seq.B) {
           if (lane == 0) atomicOr(&g_status_indexer, kDevBadIndex);
           qp = -1;
         }
-        // the previous group's tiles are done: this warp alone reads its slice
-        wq[2 * lane] = pf_w0 * pf_s0;
-        wq[2 * lane + 1] = pf_w1 * pf_s1;
+        // the previous group's tiles are done: this warp alone reads its slice.
+        // Half weights: w * ReLU(x) = (w / 2) * (x + |x|) exactly (the halving and
+        // doubling are exact), and x + |x| runs on the FMA pipe instead of a
+        // max on the half-rate ALU pipe.
+        wq[2 * lane] = 0.5f * (pf_w0 * pf_s0);
+        wq[2 * lane + 1] = 0.5f * (pf_w1 * pf_s1);
         __syncwarp();
         cur_g = w.g;
         if (w.g + 1 < p.n_groups) prefetch(w.g + 1);
       }
-      const int ab = static_cast<int>(it & 1);
+      const int ab = it & 1;
       bool ok = mbar_wait(&accfull[ab], (it >> 1) & 1, &g_status_indexer, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // the stage (keys, scales, page validity) is still this tile's: the
       // producer refills it only after this warp's arrival on empty[st]
-      const int st = static_cast<int>(it % kTcStages);
+      const int st = it % kTcStages;
       ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int s = w.kt * kTcKeys + row;
-      const uint32_t vmask = reinterpret_cast<const volatile uint32_t*>(sm + C::kOffValid)[st];
+      uint32_t vmask;
+      asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vmask) : "r"(valid_addr + st * 4) : "memory");
       const bool key_ok = s < w.nhist && ((vmask >> (row >> 6)) & 1u);
-      const float sk = key_ok ? (p.a.k_scale ? reinterpret_cast<const float*>(sm + C::kOffScale)[st * kTcKeys + row] : 1.f)
-                              : 0.f;
+      float sk = 1.f;
+      if (p.a.k_scale)
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sk) : "r"(scale_addr + st * (kTcKeys * 4)) : "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
       // the 64 heads in two halves of 32 columns (fewer live registers: 18 warps
       // leave 96 a thread); head weights as 16-byte broadcast loads
       const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
-      const float4* w4 = reinterpret_cast<const float4*>(wq);
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t wq_addr = smem_u32(wq);
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t v[32];
@@ -478,17 +487,23 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&accempty[ab]);   // the accumulator is in registers
         }
+        // x + |x| per head, then packed fmas over head pairs: eight running sums
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 wv = w4[8 * hh + i];
-          acc[0] = fmaf(wv.x, fmaxf(__uint_as_float(v[4 * i]), 0.f), acc[0]);
-          acc[1] = fmaf(wv.y, fmaxf(__uint_as_float(v[4 * i + 1]), 0.f), acc[1]);
-          acc[2] = fmaf(wv.z, fmaxf(__uint_as_float(v[4 * i + 2]), 0.f), acc[2]);
-          acc[3] = fmaf(wv.w, fmaxf(__uint_as_float(v[4 * i + 3]), 0.f), acc[3]);
+          const float4 wv = lds_f4(wq_addr + (8 * hh + i) * 16);
+          const int a = 4 * (i & 1);
+          float y[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float x = __uint_as_float(v[4 * i + k]);
+            y[k] = x + fabsf(x);
+          }
+          fma2(acc[a], acc[a + 1], wv.x, wv.y, y[0], y[1]);
+          fma2(acc[a + 2], acc[a + 3], wv.z, wv.w, y[2], y[3]);
         }
       }
-      const float sum = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-      if (key_ok && s <= qp) p.a.scores[static_cast<int64_t>(tq) * p.a.ld + s] = sum * sk;
+      const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+      if (key_ok && s <= qp) srow[s] = sum * sk;
     }
   }
 
