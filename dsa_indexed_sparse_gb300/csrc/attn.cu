@@ -219,8 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_tc_kernel(TcAttnParams p) {
   grid_dep_wait();
   constexpr int S = C::kStages;
   extern __shared__ __align__(1024) uint8_t sm_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // re-aligned by pointer arithmetic on the shared array, so that the compiler
+  // keeps every access through `sm` in the shared window
+  uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* full = bars;          // [S] tile landed (32 producer lanes)
   uint64_t* empty = bars + S;     // [S] tile consumed by P V (MMA commit)
@@ -700,8 +701,9 @@ __device__ __forceinline__ void t48_issue_s(uint32_t tmem, uint64_t dq0, uint64_
 __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams p) {
   grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // re-aligned by pointer arithmetic on the shared array, so that the compiler
+  // keeps every access through `sm` in the shared window
+  uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   if (sm - sm_raw > kT48Slack) {   // block-uniform: the re-aligned layout would not fit
     if (threadIdx.x == 0) atomicOr(&g_status_attn, kDevTimeout);
     return;

@@ -189,8 +189,9 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   static_assert(4 + kTcThreads / 32 <= 64, "misc area holds one int per warp");
   grid_dep_wait();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) &
-                                           ~static_cast<uintptr_t>(1023));
+  // re-aligned by pointer arithmetic on the shared array, so that the compiler
+  // keeps every access through `sm` in the shared window
+  uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = bars + kTcStages;
@@ -475,7 +476,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       // the 64 heads in two halves of 32 columns (fewer live registers: 18 warps
       // leave 96 a thread); head weights as 16-byte broadcast loads
       const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
-      const uint32_t wq_addr = smem_u32(wq);
+      const float4* w4 = reinterpret_cast<const float4*>(wq);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         // x + |x| per head, then packed fmas over head pairs: eight running sums
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const float4 wv = lds_f4(wq_addr + (8 * hh + i) * 16);
+          const float4 wv = w4[8 * hh + i];
           const int a = 4 * (i & 1);
           float y[4];
 #pragma unroll
