@@ -1078,62 +1078,68 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 
 // Merges row slices: out[t,h,:] = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max_s lse_s);
 // lse = max + log sum_s w_s.  The partials O_s are bf16 rows, each normalised by
-// its own slice's sum.  One CTA per (query, group of 8 heads); a warp per head,
-// each lane owning 16 value dims (two 16-byte vectors per slice); the loads of
-// four slices are issued before their sums.
-constexpr int kCombineHeads = 8;
-__global__ void __launch_bounds__(256)
+// its own slice's sum.  One CTA of two warps per (query, pair of heads); a warp per
+// head, each lane owning 16 value dims (two 16-byte vectors per slice).  Slices go
+// in batches of 16 whose row loads and LSE loads are all in flight together (one
+// L2 round trip per batch), merged with a running maximum across batches.
+constexpr int kCombineHeads = 2;
+constexpr int kCombineBatch = 16;
+__global__ void __launch_bounds__(32 * kCombineHeads)
     attn_combine_kernel(const uint16_t* ws_o, const float* ws_lse, int n_split, int T,
                         __nv_bfloat16* out, float* lse_out) {
   grid_dep_wait();
-  extern __shared__ float wts[];  // [kCombineHeads][n_split]
   constexpr int H = kH;
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y * kCombineHeads + warp;
-  float* w = wts + warp * n_split;
-  float m = -INFINITY;
-  for (int s = lane; s < n_split; s += 32) m = fmaxf(m, ws_lse[(static_cast<int64_t>(s) * T + t) * H + h]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  float sum = 0.f;
-  for (int s = lane; s < n_split; s += 32) {
-    const float l = ws_lse[(static_cast<int64_t>(s) * T + t) * H + h];
-    const float wv = (m == -INFINITY) ? 0.f : __expf(l - m);
-    w[s] = wv;
-    sum += wv;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-  __syncwarp();
-  if (lane == 0 && lse_out) lse_out[static_cast<int64_t>(t) * H + h] = sum > 0.f ? m + logf(sum) : -INFINITY;
-  const float inv = sum > 0.f ? 1.f / sum : 0.f;
   const int64_t th = static_cast<int64_t>(t) * H + h;
   const int64_t slice_stride = static_cast<int64_t>(T) * H * (kDv / 8);   // in 16-byte vectors
   const uint4* src = reinterpret_cast<const uint4*>(ws_o) + th * (kDv / 8) + 2 * lane;
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
-  auto add = [&](const uint4& v0, const uint4& v1, float ww) {
-    const uint32_t u[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+  float m = -INFINITY, l = 0.f;
+  for (int s0 = 0; s0 < n_split; s0 += kCombineBatch) {
+    const int nb = min(kCombineBatch, n_split - s0);
+    uint4 v[kCombineBatch][2];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      acc[2 * k] = fmaf(ww, __uint_as_float(u[k] << 16), acc[2 * k]);
-      acc[2 * k + 1] = fmaf(ww, __uint_as_float(u[k] & 0xFFFF0000u), acc[2 * k + 1]);
+    for (int u = 0; u < kCombineBatch; ++u) {
+      if (u < nb) {
+        v[u][0] = __ldcs(src + (s0 + u) * slice_stride);
+        v[u][1] = __ldcs(src + (s0 + u) * slice_stride + 1);
+      }
     }
-  };
-  int s = 0;
-  for (; s + 4 <= n_split; s += 4) {
-    uint4 v[4][2];
+    const float ls = lane < nb ? ws_lse[(static_cast<int64_t>(s0 + lane) * T + t) * H + h] : -INFINITY;
+    float mb = ls;
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      v[u][0] = __ldcs(src + (s + u) * slice_stride);
-      v[u][1] = __ldcs(src + (s + u) * slice_stride + 1);
+    for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+    const float m_new = fmaxf(m, mb);
+    // previous batches rescaled to the new maximum (all zero while m is -inf)
+    const float f = (m == -INFINITY) ? 0.f : __expf(m - m_new);
+    const float wl = (ls == -INFINITY) ? 0.f : __expf(ls - m_new);
+    float wsum = wl;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    l = l * f + wsum;
+    m = m_new;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) acc[k] *= f;
+#pragma unroll
+    for (int u = 0; u < kCombineBatch; ++u) {
+      const float ww = __shfl_sync(0xffffffffu, wl, u);
+      if (u < nb) {
+        const uint32_t w8[8] = {v[u][0].x, v[u][0].y, v[u][0].z, v[u][0].w,
+                                v[u][1].x, v[u][1].y, v[u][1].z, v[u][1].w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          acc[2 * k] = fmaf(ww, __uint_as_float(w8[k] << 16), acc[2 * k]);
+          acc[2 * k + 1] = fmaf(ww, __uint_as_float(w8[k] & 0xFFFF0000u), acc[2 * k + 1]);
+        }
+      }
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u) add(v[u][0], v[u][1], w[s + u]);
   }
-  for (; s < n_split; ++s) add(__ldcs(src + s * slice_stride), __ldcs(src + s * slice_stride + 1), w[s]);
+  if (lane == 0 && lse_out) lse_out[th] = l > 0.f ? m + logf(l) : -INFINITY;
+  const float inv = l > 0.f ? 1.f / l : 0.f;
   uint32_t pk[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
@@ -1223,8 +1229,8 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8" : "bf16x48", split, grid);
     *plan += buf;
     if (split > 1) {
-      const size_t smem = static_cast<size_t>(split) * kCombineHeads * sizeof(float);
-      e = launch_kernel(attn_combine_kernel, dim3(seq.T, kH / kCombineHeads), dim3(256), smem, env.stream, true, 1,
+      e = launch_kernel(attn_combine_kernel, dim3(seq.T, kH / kCombineHeads), dim3(32 * kCombineHeads), 0, env.stream,
+                        true, 1,
                      static_cast<const uint16_t*>(p.ws_o), static_cast<const float*>(p.ws_lse), split, seq.T,
                      static_cast<__nv_bfloat16*>(a.out), a.lse);
       if (e != cudaSuccess) return e;
