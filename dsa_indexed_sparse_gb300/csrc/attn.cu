@@ -277,7 +277,9 @@ template <bool kFp8>
 __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams p) {
   using C = T48<kFp8>;
   constexpr int S = C::kStages;
-  grid_dep_wait();
+  // No grid_dep_wait() here: setup and the query staging overlap the kernel
+  // before (Top-K), which lets this grid launch early; the producers wait for
+  // it before they read the selected indices.
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   // re-aligned by pointer arithmetic on the shared array, so that the compiler
   // keeps every access through `sm` in the shared window
@@ -382,6 +384,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   if (warp < C::kProducers * S) {
     // ------------------------------------------------ producers: group g = warp / 4 loads tiles
     // j = g mod S into stage g; warp w of the group copies tile rows [w*kRows, (w+1)*kRows)
+    grid_dep_wait();   // the selected indices come from the kernel before
     constexpr int kRows = C::kRows;
     const int grp = warp / C::kProducers, pw = warp % C::kProducers;
     const uint8_t* kv = static_cast<const uint8_t*>(p.a.kv);

@@ -87,6 +87,9 @@ __device__ __forceinline__ void warp_offsets(uint32_t warp_count, uint32_t* buf,
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   grid_dep_wait();
+  // The attention kernel that follows may start now: it stages its query and
+  // waits for this grid before it reads the indices.
+  grid_dep_launch();
   extern __shared__ uint32_t keys_s[];
   __shared__ uint32_t hist2[2][256];    // this CTA's slice (pass parity)
   __shared__ uint32_t whist[kWarps][256];   // per-warp partial histograms
@@ -293,7 +296,6 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     eq_rank += __popc(eqm);
     pos += __popc(selm);
   }
-  grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers may still read s_counts
 }
 
@@ -305,10 +307,10 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
     *plan += "topk[empty]";
     return cudaSuccess;
   }
-  // Enough CTAs to cover the GPU (a small batch splits each history over a
-  // cluster), no more than the history can feed, and enough to keep a slice
-  // within the shared-memory key cache when the cluster can.
-  const int want = (std::max(1, env.num_sms) + seq.T - 1) / seq.T;
+  // As many CTAs as fit the GPU in one wave (a small batch splits each history
+  // over a cluster), no more than the history can feed, and enough to keep a
+  // slice within the shared-memory key cache when the cluster can.
+  const int want = std::max(1, env.num_sms / seq.T);   // one wave: T x cluster <= SMs
   const int feed = std::max(1, seq.max_ctx / kMinSliceKeys);
   const int fit = (seq.max_ctx + kCacheKeys - 1) / kCacheKeys;
   const int cl = std::max(1, std::min(kMaxCluster, std::max(std::min(want, feed), fit)));
