@@ -279,7 +279,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   constexpr int S = C::kStages;
   // No grid_dep_wait() here: setup and the query staging overlap the kernel
   // before (Top-K), which lets this grid launch early; the producers wait for
-  // it before they read the selected indices.
+  // it before they read the selected indices.  The kernel after (the combine,
+  // or the next step's indexer) may launch at once too: each waits for this
+  // grid before it reads anything this grid writes.
+  grid_dep_launch();
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   // re-aligned by pointer arithmetic on the shared array, so that the compiler
   // keeps every access through `sm` in the shared window
@@ -725,7 +728,6 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     }
   }
 
-  grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   tc_fence_before();
   __syncthreads();
   if (warp == kT48Mma) {
@@ -745,6 +747,7 @@ constexpr int kCombineBatch = 16;
 __global__ void __launch_bounds__(32 * kCombineHeads)
     attn_combine_kernel(const uint16_t* ws_o, const float* ws_lse, int n_split, int T,
                         __nv_bfloat16* out, float* lse_out) {
+  grid_dep_launch();   // the next kernel waits for this grid before it uses out
   grid_dep_wait();
   constexpr int H = kH;
   const int t = blockIdx.x;

@@ -187,7 +187,8 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   constexpr int kTcThreads = TcWarps<G>::kThreads;
   constexpr int kEpiWarps = TcWarps<G>::kEpiWarps;
   static_assert(4 + kTcThreads / 32 <= 64, "misc area holds one int per warp");
-  grid_dep_wait();
+  // No grid_dep_wait() yet: the work split, barriers and TMEM (inputs only)
+  // overlap the tail of the kernel before when that one lets this grid start early.
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   // re-aligned by pointer arithmetic on the shared array, so that the compiler
   // keeps every access through `sm` in the shared window
@@ -281,6 +282,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   const uint32_t tmem = misc[0];
   const int g_start = sched[0], kt_start = sched[1];
   const int ntiles = static_cast<int>(end - begin);   // <= total, an int
+  grid_dep_wait();
 
   if (warp == 0) {
     // ------------------------------------------------ TMA producer (warp 0)
