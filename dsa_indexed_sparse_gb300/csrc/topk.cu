@@ -6,23 +6,26 @@
 // the min(K, n) positions with the largest fp32 scores, ties to the lower
 // position, as an ascending list followed by -1 padding.
 //
-// Exact radix select, one CTA (1024 threads) per query:
+// Exact radix select:
 //  * a query's history is split into contiguous slices over the CTAs of a
 //    thread-block cluster (1 to 8 CTAs of 512 threads), each slice's scores
 //    turned into order-preserving uint32 keys (-0.0 folded onto +0.0) and cached
 //    in that CTA's shared memory;
 //  * up to four 8-bit digit passes narrow the K-th largest key: every CTA builds
-//    the histogram of its slice (one private histogram per warp, four keys per
-//    thread per step, then summed), and after one cluster barrier every CTA sums the cluster's
-//    histograms through distributed shared memory and picks the same digit by
-//    itself (histograms alternate between two buffers, so a pass needs no second
-//    barrier before the next one overwrites them); a pass stops early when the
-//    bucket holding the K-th key is taken whole;
+//    the histogram of its slice (one private histogram per warp over the warp's
+//    contiguous range, four keys per thread per step, then summed), and after
+//    one cluster barrier every CTA reads the cluster's histograms through
+//    distributed shared memory and picks the same digit by itself (histograms
+//    alternate between two buffers, so a pass needs no second barrier before the
+//    next one overwrites them); a pass stops early when the bucket holding the
+//    K-th key is taken whole;
 //  * an ordered compaction keeps every key above the threshold and, in position
-//    order, the first `remaining` keys equal to it: cluster-wide prefix counts
-//    give each CTA its offsets, a scan over warps gives each warp (which owns a
-//    contiguous range) its own, and within a warp ballots over 32 consecutive
-//    keys give each lane its slot, so the output comes out in ascending order.
+//    order, the first `remaining` keys equal to it.  Each warp's own histograms
+//    give its counts above and on the threshold, and the other slices'
+//    histograms (read in every pass anyway) give the counts of the slices before
+//    this one, so no further exchange is needed: a scan over warps gives each
+//    warp its offsets, and within a warp ballots over 32 consecutive keys give
+//    each lane its slot, so the output comes out in ascending order.
 #include <cooperative_groups.h>
 
 #include <algorithm>
@@ -62,27 +65,29 @@ struct TopkArgs {
   int32_t T;
 };
 
-// Exclusive scan of one value per warp; every thread gets (its warp's offset,
-// block total).  Uses `buf` [kWarps + 1] and two __syncthreads.
-__device__ __forceinline__ void warp_offsets(uint32_t warp_count, uint32_t* buf, uint32_t* excl,
-                                             uint32_t* total) {
+// Exclusive scans over the warps of two per-warp values at once: every thread
+// gets its warp's two offsets.  Uses `buf` [2][kWarps + 1] and two __syncthreads.
+__device__ __forceinline__ void warp_offsets2(uint32_t c0, uint32_t c1, uint32_t (*buf)[kWarps + 1],
+                                              uint32_t* excl0, uint32_t* excl1) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) buf[warp] = warp_count;
+  if (lane == 0) {
+    buf[0][warp] = c0;
+    buf[1][warp] = c1;
+  }
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t v = lane < kWarps ? buf[lane] : 0u;
+  if (warp < 2) {
+    const uint32_t v = lane < kWarps ? buf[warp][lane] : 0u;
     uint32_t inc = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const uint32_t u = __shfl_up_sync(0xffffffffu, inc, o);
       if (lane >= o) inc += u;
     }
-    if (lane < kWarps) buf[lane] = inc - v;   // exclusive
-    if (lane == 31) buf[kWarps] = inc;        // total
+    if (lane < kWarps) buf[warp][lane] = inc - v;
   }
   __syncthreads();
-  *excl = buf[warp];
-  *total = buf[kWarps];
+  *excl0 = buf[0][warp];
+  *excl1 = buf[1][warp];
 }
 
 __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
@@ -94,9 +99,11 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   __shared__ uint32_t hist2[2][256];    // this CTA's slice (pass parity)
   __shared__ uint32_t whist[kWarps][256];   // per-warp partial histograms
   __shared__ uint32_t ghist[256];       // the cluster's sum
-  __shared__ uint32_t scan_buf[kWarps + 1];
+  __shared__ uint32_t scan_buf[2][kWarps + 1];
   __shared__ uint32_t s_digit, s_rem, s_bucket;
-  __shared__ uint32_t s_counts[2];      // this slice: keys == prefix, keys selected
+  // keys of the slices before this one (lower cluster ranks): above the
+  // threshold, and equal to it -- read off their histograms, pass by pass
+  __shared__ uint32_t s_gt_before, s_eq_before;
 
   cg::cluster_group cluster = cg::this_cluster();
   const int CL = static_cast<int>(cluster.num_blocks());
@@ -146,6 +153,10 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   const int wlo = min(len, warp * wl), whi = min(len, wlo + wl);
   uint32_t n_gt = 0, n_eq = 0;
   uint32_t prefix = 0, pmask = 0;
+  if (tid == 0) {
+    s_gt_before = 0;
+    s_eq_before = 0;
+  }
   uint32_t rem = static_cast<uint32_t>(K);  // how many of the keys matching `prefix` to keep
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
@@ -190,15 +201,20 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       hist[b] = v;
     }
     cluster.sync();  // every slice's histogram complete
-    for (int i = tid; i < 256; i += kThreads) {
-      // all ranks' loads in flight at once (the loop is unrolled to the largest cluster)
+    // thread i < 256 reads bin i of every slice (all ranks' loads in flight at
+    // once), keeping the sum over the slices before this one for later
+    uint32_t before_i = 0;
+    if (tid < 256) {
       uint32_t part[kMaxCluster];
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) part[r] = r < CL ? cluster.map_shared_rank(hist, r)[i] : 0u;
+      for (int r = 0; r < kMaxCluster; ++r) part[r] = r < CL ? cluster.map_shared_rank(hist, r)[tid] : 0u;
       uint32_t v = 0;
 #pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r) v += part[r];
-      ghist[i] = v;
+      for (int r = 0; r < kMaxCluster; ++r) {
+        v += part[r];
+        before_i += r < rank ? part[r] : 0u;
+      }
+      ghist[tid] = v;
     }
     __syncthreads();
     if (tid < 32) {
@@ -244,6 +260,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
       for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xffffffffu, above, o);
       n_gt += above;
       n_eq = whist[warp][d];
+      // the earlier slices' keys above the chosen digit, and on it
+      if (tid < 256) {
+        uint32_t bg = tid > static_cast<int>(d) ? before_i : 0u;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bg += __shfl_xor_sync(0xffffffffu, bg, o);
+        if (lane == 0 && bg) atomicAdd(&s_gt_before, bg);
+        if (tid == static_cast<int>(d)) s_eq_before = before_i;
+      }
     }
     prefix |= s_digit << shift;
     pmask |= 255u << shift;
@@ -253,34 +277,18 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     if (whole) break;  // cluster-uniform (same histogram everywhere)
   }
 
-  // Ordered compaction over the same warp ranges, 32 positions at a time.
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t eq_w, slice_eq, gt_w, slice_gt;
-  warp_offsets(n_eq, scan_buf, &eq_w, &slice_eq);
-  __syncthreads();
-  warp_offsets(n_gt, scan_buf, &gt_w, &slice_gt);
-  if (tid == 0) {
-    s_counts[0] = slice_eq;
-    s_counts[1] = slice_gt;
-  }
-  cluster.sync();  // every slice's counts visible cluster-wide
-  // Earlier slices: their keys equal to the threshold (for this slice's ranks)
-  // and how many of their keys are selected (for this slice's output offset).
-  uint32_t eq_before = 0, sel_before = 0;
-  uint32_t ce[kMaxCluster], cg[kMaxCluster];
-#pragma unroll
-  for (int r = 0; r < kMaxCluster; ++r) {
-    const uint32_t* pc = cluster.map_shared_rank(s_counts, r < rank ? r : 0);
-    ce[r] = r < rank ? pc[0] : 0u;
-    cg[r] = r < rank ? pc[1] : 0u;
-  }
-#pragma unroll
-  for (int r = 0; r < kMaxCluster; ++r) {
-    sel_before += cg[r] + (eq_before >= rem ? 0u : min(ce[r], rem - eq_before));
-    eq_before += ce[r];
-  }
-  // peers' counts are read: signal that, and wait for the others only before exit
+  // The last distributed read of the peers' histograms is done: signal that,
+  // and wait for the others only before exit.
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // Ordered compaction over the same warp ranges, 32 positions at a time.  The
+  // slices before this one hold eq_before keys equal to the threshold (the first
+  // ones in position order, so min(eq_before, rem) of them are selected) and
+  // gt_before keys above it.
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t eq_w, gt_w;
+  warp_offsets2(n_eq, n_gt, scan_buf, &eq_w, &gt_w);
+  const uint32_t eq_before = s_eq_before;
+  const uint32_t sel_before = s_gt_before + min(eq_before, rem);
   // this warp's first equal-key rank and first output slot
   uint32_t eq_rank = eq_before + eq_w;
   uint32_t pos = sel_before + gt_w + (eq_before >= rem ? 0u : min(eq_w, rem - eq_before));
@@ -296,7 +304,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
     eq_rank += __popc(eqm);
     pos += __popc(selm);
   }
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers may still read s_counts
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers may still read this histogram
 }
 
 }  // namespace
