@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   // The last distributed read of the peers' histograms is done: signal that,
   // and wait for the others only before exit.
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  // Ordered compaction over the same warp ranges, 32 positions at a time.  The
+  // Ordered compaction over the same warp ranges.  The
   // slices before this one hold eq_before keys equal to the threshold (the first
   // ones in position order, so min(eq_before, rem) of them are selected) and
   // gt_before keys above it.
@@ -292,17 +292,58 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(TopkArgs a) {
   // this warp's first equal-key rank and first output slot
   uint32_t eq_rank = eq_before + eq_w;
   uint32_t pos = sel_before + gt_w + (eq_before >= rem ? 0u : min(eq_w, rem - eq_before));
-  for (int b = wlo; b < whi; b += 32) {
-    const int i = b + lane;
-    const bool in = i < whi;
-    const uint32_t km = in ? (key_at(i) & pmask) : 0u;
-    const bool eq = in && km == prefix;
-    const uint32_t eqm = __ballot_sync(0xffffffffu, eq);
-    const bool sel = (in && km > prefix) || (eq && eq_rank + __popc(eqm & lt_mask) < rem);
-    const uint32_t selm = __ballot_sync(0xffffffffu, sel);
-    if (sel) out[pos + __popc(selm & lt_mask)] = lo + i;
-    eq_rank += __popc(eqm);
-    pos += __popc(selm);
+  // 128 positions per step, four consecutive ones per lane (lane-major order);
+  // one ballot per sub-position gives every lane the counts before its keys
+  for (int b = wlo; b < whi; b += 128) {
+    const int i4 = b + 4 * lane;
+    uint32_t k[4];
+    if (cached && i4 + 3 < whi) {
+      const uint4 k4 = reinterpret_cast<const uint4*>(keys_s)[i4 >> 2];
+      k[0] = k4.x;
+      k[1] = k4.y;
+      k[2] = k4.z;
+      k[3] = k4.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k[e] = i4 + e < whi ? key_at(i4 + e) : 0u;
+    }
+    uint32_t eqb = 0, gtb = 0;   // bit e: key i4 + e equal to / above the threshold
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t km = k[e] & pmask;
+      const bool valid = i4 + e < whi;
+      eqb |= (valid && km == prefix) ? (1u << e) : 0u;
+      gtb |= (valid && km > prefix) ? (1u << e) : 0u;
+    }
+    uint32_t eq_before_lane = 0, eq_total = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t m = __ballot_sync(0xffffffffu, (eqb >> e) & 1u);
+      eq_before_lane += __popc(m & lt_mask);
+      eq_total += __popc(m);
+    }
+    uint32_t selb = gtb, r = eq_rank + eq_before_lane;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if ((eqb >> e) & 1u) {
+        if (r < rem) selb |= 1u << e;
+        ++r;
+      }
+    }
+    uint32_t sel_before_lane = 0, sel_total = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const uint32_t m = __ballot_sync(0xffffffffu, (selb >> e) & 1u);
+      sel_before_lane += __popc(m & lt_mask);
+      sel_total += __popc(m);
+    }
+    uint32_t o = pos + sel_before_lane;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if ((selb >> e) & 1u) out[o++] = lo + i4 + e;
+    }
+    eq_rank += eq_total;
+    pos += sel_total;
   }
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");   // peers may still read this histogram
 }
