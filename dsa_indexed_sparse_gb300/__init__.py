@@ -126,8 +126,27 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise ValueError(f"unsupported dtype {t.dtype}")
 
 
+class _CachedDesc:
+    """The C descriptor is built on first use and kept until a field is reassigned
+    (a step call then costs no Python-side struct building).  Tensors are
+    referenced by their data pointers, so resizing a tensor in place needs the
+    field reassigned."""
+
+    def __setattr__(self, name, value):
+        if name != "_desc":
+            object.__setattr__(self, "_desc", None)
+        object.__setattr__(self, name, value)
+
+    def desc(self):
+        d = self.__dict__.get("_desc")
+        if d is None:
+            d = self._build_desc()
+            object.__setattr__(self, "_desc", d)
+        return d
+
+
 @dataclasses.dataclass
-class Seq:
+class Seq(_CachedDesc):
     """Queries and paging (device int32 tensors); see dsa_seq_desc_t."""
     q_seq: torch.Tensor
     q_pos: torch.Tensor
@@ -137,14 +156,14 @@ class Seq:
     page_size: int = 64
     q_per_seq: int = 0
 
-    def desc(self) -> SeqDesc:
+    def _build_desc(self) -> SeqDesc:
         B, stride = self.block_table.shape
         return SeqDesc(B, self.q_seq.shape[0], self.max_ctx, self.q_per_seq, _ptr(self.q_seq),
                        _ptr(self.q_pos), _ptr(self.block_table), stride, self.page_size, self.cache_rows)
 
 
 @dataclasses.dataclass
-class Indexer:
+class Indexer(_CachedDesc):
     """Lightning-indexer inputs; see dsa_indexer_desc_t."""
     q: torch.Tensor                    # [T, H_I, D_I] e4m3 codes (uint8) or fp32
     w: torch.Tensor                    # [T, H_I] fp32
@@ -152,14 +171,14 @@ class Indexer:
     q_scale: Optional[torch.Tensor] = None
     k_scale: Optional[torch.Tensor] = None
 
-    def desc(self) -> IndexerDesc:
+    def _build_desc(self) -> IndexerDesc:
         _, H_I, D_I = self.q.shape
         return IndexerDesc(H_I, D_I, _dtype_code(self.k_cache), _ptr(self.q), _ptr(self.q_scale),
                            _ptr(self.w), _ptr(self.k_cache), _ptr(self.k_scale))
 
 
 @dataclasses.dataclass
-class Mla:
+class Mla(_CachedDesc):
     """Latent attention inputs; see dsa_mla_desc_t.  kv_cache is [cache_rows, row] of
     bf16/fp32 values or uint8 656-byte FP8 rows (dtype given explicitly then)."""
     q: torch.Tensor                    # [T, H, d_latent + d_rope]
@@ -169,7 +188,7 @@ class Mla:
     softmax_scale: float
     dtype: Optional[int] = None
 
-    def desc(self) -> MlaDesc:
+    def _build_desc(self) -> MlaDesc:
         dt = self.dtype if self.dtype is not None else _dtype_code(self.kv_cache)
         row_bytes = self.kv_cache.stride(0) * self.kv_cache.element_size()
         return MlaDesc(self.q.shape[1], self.d_latent, self.d_rope, dt, _ptr(self.q), _ptr(self.kv_cache),

@@ -518,13 +518,14 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     }
   } else if (warp == kT48Mma || warp == kT48Pv) {
     // ------------------------------------------------ MMA issuers (whole warp, elected lane issues)
-    // Bounded polls on the non-suspending test_wait: these waits are on the
-    // critical path of every tile.
+    // Bounded waits on the suspending try_wait: the issuing warps share their
+    // sub-partitions with softmax warps, whose issue slots a spinning poll took
+    // (prefill attention 2 % slower with test_wait spins).
     auto poll = [&](uint64_t* bar, uint32_t parity) -> bool {
       const uint32_t addr = smem_u32(bar);
       uint64_t t0 = 0;
       for (uint32_t it = 0;; ++it) {
-        if (__shfl_sync(0xffffffffu, mbar_test_wait(addr, parity) ? 1 : 0, 0)) return true;
+        if (__shfl_sync(0xffffffffu, mbar_try_wait(addr, parity) ? 1 : 0, 0)) return true;
         if ((it & 255u) == 255u) {
           if (__shfl_sync(0xffffffffu, *abort_flag, 0)) return false;
           const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
