@@ -58,7 +58,7 @@ class Workload:
     block_table: np.ndarray      # int32 [B, max_pages]  (-1 = unused slot)
     cache_rows: int
     # lightning indexer
-    idx_dtype: str               # "e4m3" | "f32"
+    idx_dtype: str               # "e4m3" (per-token / per-head fp32 scales) | "mx_e4m3" (E8M0 per 32) | "f32"
     H_I: int
     D_I: int
     q_i: np.ndarray
@@ -95,6 +95,7 @@ class Spec:
     H_I: int = 64
     D_I: int = 128
     idx_dtype: str = "e4m3"
+    mx_block_spread: int = 4     # "mx_e4m3": block magnitudes 2**U{-4..4} before quantising
     w_var: float = 1.0 / 64.0
     H: int = 128
     d_latent: int = 512
@@ -142,6 +143,34 @@ def _quant_rows_e4m3(x: torch.Tensor):
     scale = torch.where(amax > 0, amax / E4M3_MAX, torch.ones_like(amax))
     codes = (x / scale).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
     return codes.view(torch.uint8).numpy(), scale.squeeze(-1).to(torch.float32).numpy()
+
+
+MX_BLOCK = 32        # elements sharing one E8M0 scale (OCP MXFP8)
+E4M3_EMAX = 8        # exponent of the largest normal E4M3 value (448 = 1.75 * 2**8)
+
+
+def _quant_blocks_mx(x: torch.Tensor):
+    """OCP MXFP8 along the last axis: blocks of 32 elements share an E8M0 scale
+    2**(e - 127) with e - 127 = floor(log2(amax of the block)) - 8 (-127 for an
+    all-zero block); elements are the E4M3 values nearest to x / scale (ties to
+    even), clamped to +-448.  Returns (uint8 codes, uint8 E8M0 exponents with
+    the block axis last)."""
+    shp = x.shape
+    xb = x.reshape(*shp[:-1], shp[-1] // MX_BLOCK, MX_BLOCK)
+    amax = xb.abs().amax(dim=-1, keepdim=True)
+    _, e = torch.frexp(amax)                          # amax = m * 2**e, m in [0.5, 1)
+    sexp = torch.where(amax > 0, e - 1 - E4M3_EMAX, torch.full_like(e, -127)).clamp(-127, 127)
+    codes = torch.ldexp(xb, -sexp).clamp(-E4M3_MAX, E4M3_MAX).to(torch.float8_e4m3fn)
+    return (codes.view(torch.uint8).reshape(shp).numpy(),
+            (sexp + 127).to(torch.uint8).squeeze(-1).numpy())
+
+
+def _spread_blocks(g: torch.Generator, x: torch.Tensor, spread: int):
+    """Multiplies every 32-element block of the last axis by 2**r, r uniform in
+    [-spread, spread] (seeded), so that blocks of one vector differ in range."""
+    shp = x.shape
+    r = torch.randint(-spread, spread + 1, (*shp[:-1], shp[-1] // MX_BLOCK, 1), generator=g)
+    x.view(*shp[:-1], shp[-1] // MX_BLOCK, MX_BLOCK).mul_(torch.pow(2.0, r.to(torch.float32)))
 
 
 def _bf16_bits(x: torch.Tensor) -> np.ndarray:
@@ -215,6 +244,11 @@ def make(name_or_spec, seed: int = 0, **over) -> Workload:
     if sp.idx_dtype == "e4m3":
         k_i, k_i_scale = _quant_rows_e4m3(k_f)
         q_i, q_i_scale = _quant_rows_e4m3(q_f)
+    elif sp.idx_dtype == "mx_e4m3":
+        _spread_blocks(g, k_f, sp.mx_block_spread)
+        _spread_blocks(g, q_f, sp.mx_block_spread)
+        k_i, k_i_scale = _quant_blocks_mx(k_f)
+        q_i, q_i_scale = _quant_blocks_mx(q_f)
     elif sp.idx_dtype == "f32":
         k_i, k_i_scale = k_f.numpy(), np.ones(cache_rows, np.float32)
         q_i, q_i_scale = q_f.numpy(), np.ones((T, sp.H_I), np.float32)
@@ -255,9 +289,9 @@ def make(name_or_spec, seed: int = 0, **over) -> Workload:
         seq_lens=np.asarray(ctx, dtype=np.int32), block_table=block_table,
         cache_rows=cache_rows,
         idx_dtype=sp.idx_dtype, H_I=sp.H_I, D_I=sp.D_I, q_i=q_i,
-        q_i_scale=np.ascontiguousarray(q_i_scale, dtype=np.float32),
+        q_i_scale=np.ascontiguousarray(q_i_scale, dtype=np.uint8 if sp.idx_dtype == "mx_e4m3" else np.float32),
         w=np.ascontiguousarray(w, dtype=np.float32), k_i=k_i,
-        k_i_scale=np.ascontiguousarray(k_i_scale, dtype=np.float32),
+        k_i_scale=np.ascontiguousarray(k_i_scale, dtype=np.uint8 if sp.idx_dtype == "mx_e4m3" else np.float32),
         mla_dtype=sp.mla_dtype, H=sp.H, d_latent=sp.d_latent, d_rope=sp.d_rope,
         q=q, kv=kv, row_bytes=row_bytes, softmax_scale=float(sp.softmax_scale),
     )
@@ -283,6 +317,8 @@ def device_tensors(wl: Workload, device, copies: int = 1) -> dict:
                    q_per_seq=wl.q_per_seq)
         idx = dict(q=t(wl.q_i), w=t(wl.w), k_cache=t(wl.k_i), q_scale=t(wl.q_i_scale),
                    k_scale=t(wl.k_i_scale))
+        if wl.idx_dtype == "mx_e4m3":
+            idx["dtype"] = 3  # MXFP8: E4M3 codes + one E8M0 scale byte per 32 elements
         if wl.mla_dtype == "bf16":
             q, kv = t(wl.q.view(np.int16), torch.bfloat16), t(wl.kv.view(np.int16), torch.bfloat16)
             dt = None

@@ -15,7 +15,11 @@ the method states it:
    Top-K; page "Large Language Model Inference Acceleration in Practice",
    section 1.2 "DSA", LI sub-module).  Per the spec definition:
        I[t, s] = sum_h w[t, h] * ReLU(q_I[t, h] . k_I[s])
-   with q_I, k_I the dequantised FP8 values (code * scale).
+   with q_I, k_I the dequantised FP8 values (code * scale): one fp32 scale per
+   key and per (query, head), or -- the pages' MXFP8 variant ("Day0 ... Kimi
+   K3.1 Pro", section 4; "Large Language Model Inference Acceleration in
+   Practice", section 4) -- one power-of-two E8M0 scale per 32 consecutive
+   elements (OCP Microscaling formats: shared exponent floor(log2 amax) - 8).
 2. per-query Top-K over the causal history s in [0, q_pos[t]], ties to the
    lower index (same page, section 1.2, "selects the Top-K most relevant
    positions").
@@ -108,6 +112,36 @@ def e4m3_encode(x) -> np.ndarray:
     return (sign | mag_code).astype(np.uint8)
 
 
+def decode_e8m0(e) -> np.ndarray:
+    """OCP E8M0 scale byte -> float64: 2**(e - 127) for e in 0..254; 255 is NaN."""
+    e = np.asarray(e, dtype=np.int64)
+    return np.where(e == 255, math.nan, np.ldexp(1.0, e - 127))
+
+
+def quantize_mx_e4m3(x, block: int = 32) -> tuple:
+    """OCP MXFP8 (E4M3 elements, E8M0 shared scales) along the last axis: for each
+    block of `block` consecutive values, shared exponent = floor(log2(amax)) - 8
+    (8 = exponent of E4M3's largest normal, 448 = 1.75 * 2**8; -127 for an
+    all-zero block), scale byte = exponent + 127, element codes = e4m3_encode of
+    x / 2**exponent (an exact power-of-two quotient; saturates at 448).
+    Returns (uint8 codes, uint8 scale bytes with the block axis last)."""
+    x = np.asarray(x, dtype=np.float32)
+    xb = x.reshape(*x.shape[:-1], x.shape[-1] // block, block)
+    amax = np.max(np.abs(xb), axis=-1, keepdims=True).astype(np.float64)
+    with np.errstate(divide="ignore"):
+        exp = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - 8, -127)
+    exp = np.clip(exp, -127, 127).astype(np.int64)
+    codes = e4m3_encode(np.ldexp(xb.astype(np.float64), -exp).astype(np.float32))
+    return codes.reshape(x.shape), (exp + 127).astype(np.uint8)[..., 0]
+
+
+def dequantize_mx_e4m3(codes, scales, block: int = 32) -> np.ndarray:
+    """float64 values of MXFP8 data: code value * 2**(e - 127) of its block."""
+    v = decode_e4m3(codes)
+    v = v.reshape(*v.shape[:-1], v.shape[-1] // block, block)
+    return (v * decode_e8m0(scales)[..., None]).reshape(np.asarray(codes).shape)
+
+
 def quantize_e4m3_row(x) -> tuple:
     """One token's vector -> (uint8 codes, float32 scale): scale = amax / 448 in
     float32 (1 when the row is all zero), codes = e4m3_encode(x / scale) with the
@@ -129,16 +163,22 @@ def physical_rows(block_table_row: np.ndarray, page_size: int, pos: np.ndarray) 
 
 
 def indexer_keys(wl, rows: np.ndarray) -> np.ndarray:
-    """Dequantised indexer keys k_I[row] = code * k_scale[row] (float64)."""
+    """Dequantised indexer keys (float64): code * k_scale[row] for per-token
+    scales, code * 2**(e - 127) of the element's 32-value block for MXFP8."""
     if wl.idx_dtype == "e4m3":
         return decode_e4m3(wl.k_i[rows]) * wl.k_i_scale[rows].astype(np.float64)[:, None]
+    if wl.idx_dtype == "mx_e4m3":
+        return dequantize_mx_e4m3(wl.k_i[rows], wl.k_i_scale[rows])
     return wl.k_i[rows].astype(np.float64)
 
 
 def indexer_query(wl, t: int) -> np.ndarray:
-    """Dequantised indexer query q_I[t, h] = code * q_scale[t, h] (float64 [H_I, D_I])."""
+    """Dequantised indexer query q_I[t, h] (float64 [H_I, D_I]): code * q_scale[t, h],
+    or code * 2**(e - 127) of its 32-value block for MXFP8."""
     if wl.idx_dtype == "e4m3":
         return decode_e4m3(wl.q_i[t]) * wl.q_i_scale[t].astype(np.float64)[:, None]
+    if wl.idx_dtype == "mx_e4m3":
+        return dequantize_mx_e4m3(wl.q_i[t], wl.q_i_scale[t])
     return wl.q_i[t].astype(np.float64)
 
 

@@ -71,12 +71,18 @@ def brute_scores(wl, t):
         if wl.idx_dtype == "e4m3":
             v = torch.tensor([wl.q_i[t, h, i]], dtype=torch.uint8).view(torch.float8_e4m3fn).item()
             return v * float(wl.q_i_scale[t, h])
+        if wl.idx_dtype == "mx_e4m3":   # block i // 32 carries the E8M0 exponent
+            v = torch.tensor([wl.q_i[t, h, i]], dtype=torch.uint8).view(torch.float8_e4m3fn).item()
+            return v * 2.0 ** (int(wl.q_i_scale[t, h, i // 32]) - 127)
         return float(wl.q_i[t, h, i])
 
     def deq_k(row, i):
         if wl.idx_dtype == "e4m3":
             v = torch.tensor([wl.k_i[row, i]], dtype=torch.uint8).view(torch.float8_e4m3fn).item()
             return v * float(wl.k_i_scale[row])
+        if wl.idx_dtype == "mx_e4m3":
+            v = torch.tensor([wl.k_i[row, i]], dtype=torch.uint8).view(torch.float8_e4m3fn).item()
+            return v * 2.0 ** (int(wl.k_i_scale[row, i // 32]) - 127)
         return float(wl.k_i[row, i])
 
     b = wl.q_seq[t]
@@ -95,11 +101,14 @@ def brute_scores(wl, t):
     return np.array(out)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "decode_b1", "decode_b64"])
+@pytest.mark.parametrize("name", ["tiny_fp32", "decode_b1", "decode_b64", "mx"])
 def test_indexer_brute_force(name):
     over = dict(ctx=[70], K=8, H_I=3, D_I=8)
     if name == "decode_b64":
         over = dict(ctx=None, ctx_range=(65, 130), B=2, K=8, H_I=3, D_I=8)
+    if name == "mx":   # MXFP8: blocks of 32 with their own power-of-two scales
+        name, over = "decode_b64", dict(ctx=None, ctx_range=(40, 70), B=2, K=8, H_I=2, D_I=64,
+                                        idx_dtype="mx_e4m3")
     wl = small(name, **over)
     for t in range(wl.T):
         ref = brute_scores(wl, t)
@@ -423,3 +432,67 @@ def test_cache_append_oracle_layout_and_untouched_rows():
     cacheb = O.latent_cache_append(block_table, page, q_seq, q_pos, bits, cacheb0, fp8_rows=False)
     assert np.array_equal(cacheb[other], cacheb0[other])
     assert all(np.array_equal(cacheb[r].view("<u2"), bits[t]) for t, r in enumerate(rows))
+
+
+# --------------------------------------------------------------------------- MXFP8 (OCP microscaling)
+
+def test_e8m0_all_codes():
+    """E8M0 byte e is 2**(e - 127); 255 is NaN (OCP Microscaling formats)."""
+    e = np.arange(256)
+    v = O.decode_e8m0(e)
+    assert np.isnan(v[255])
+    assert v[127] == 1.0 and v[0] == 2.0 ** -127 and v[254] == 2.0 ** 127
+    assert np.all(v[1:255] / v[0:254] == 2.0)
+
+
+def test_mx_quantizer_rule_and_torch_cast():
+    """Shared exponent = floor(log2 amax) - 8, so the block maximum lands in
+    [256, 512) before saturation at 448; elements agree with torch's E4M3 cast of
+    the power-of-two quotient (a library routine); an all-zero block gets byte 0."""
+    rng = np.random.default_rng(5)
+    x = (rng.normal(0, 1, (40, 128)) * np.repeat(np.exp2(rng.integers(-9, 9, (40, 4))), 32, axis=1)).astype(np.float32)
+    x[3, 32:64] = 0.0
+    codes, scales = O.quantize_mx_e4m3(x)
+    assert codes.shape == x.shape and scales.shape == (40, 4) and scales.dtype == np.uint8
+    assert scales[3, 1] == 0 and np.all(codes[3, 32:64] == 0)
+    xb = x.reshape(40, 4, 32).astype(np.float64)
+    amax = np.abs(xb).max(-1)
+    e = scales.astype(np.int64) - 127
+    nz = amax > 0
+    assert np.all(np.floor(np.log2(amax[nz])) - 8 == e[nz])
+    q = np.ldexp(xb, -e[..., None]).astype(np.float32)
+    ref = torch.from_numpy(np.clip(q, -448, 448)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(codes.reshape(40, 4, 32), ref)
+    back = O.dequantize_mx_e4m3(codes, scales)
+    # E4M3 has 3 mantissa bits: relative error <= 2**-4 below saturation
+    unsat = np.abs(q) <= 448
+    err = np.abs(back.reshape(40, 4, 32) - xb)
+    assert np.all(err[unsat] <= np.abs(xb[unsat]) * 2.0 ** -4 + np.ldexp(1.0, e[..., None] - 9).repeat(32, -1)[unsat])
+
+
+def test_mx_generator_matches_oracle_quantizer():
+    """The input generator's MXFP8 encoder (torch) and the oracle's (numpy,
+    nearest-value search) agree code for code."""
+    rng = np.random.default_rng(6)
+    x = (rng.normal(0, 1, (64, 128)) * np.repeat(np.exp2(rng.integers(-6, 6, (64, 4))), 32, axis=1)).astype(np.float32)
+    c0, e0 = O.quantize_mx_e4m3(x)
+    c1, e1 = W._quant_blocks_mx(torch.from_numpy(x))
+    assert np.array_equal(c0, c1) and np.array_equal(e0, e1)
+
+
+def test_mx_indexer_one_block_closed_form():
+    """H_I = 1, w = 1, the query nonzero only in element i of block b (code 1.0,
+    exponent byte 127 + a): I[s] = max(k_code[s, i] * 2**(ek[s, b] - 127) * 2**a, 0)."""
+    wl = small("decode_b64", ctx=None, ctx_range=(130, 131), B=1, H_I=1, D_I=64, idx_dtype="mx_e4m3")
+    i, b, a = 37, 1, 3
+    wl.q_i[:] = 0
+    wl.q_i[0, 0, i] = 0x38
+    wl.q_i_scale[0, 0, :] = 120            # other blocks hold zeros anyway
+    wl.q_i_scale[0, 0, b] = 127 + a
+    wl.w[0, 0] = 1.0
+    got = O.indexer_scores_row(wl, 0)
+    n = got.shape[0]
+    rows = O.physical_rows(wl.block_table[0], wl.page_size, np.arange(n))
+    kcode = torch.from_numpy(wl.k_i[rows, i].copy()).view(torch.float8_e4m3fn).double().numpy()
+    expect = np.maximum(kcode * np.exp2(wl.k_i_scale[rows, b].astype(np.float64) - 127) * 2.0 ** a, 0.0)
+    np.testing.assert_array_equal(got, expect.astype(np.float32))
