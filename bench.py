@@ -36,6 +36,10 @@ DESCRIPTIONS = {
                       "bf16 rope), indexer 64x128 e4m3, top-k 2048, MLA 128 heads",
     "prefill_16k": "prefill: 16384 causal tokens, indexer 64x128 e4m3, top-k 2048, MLA 128 heads, "
                    "bf16 512+64, inputs N(0,1) + rank-8 component",
+    "decode_b64_mx": "decode batch 64 as decode_b64, indexer keys and queries MXFP8 (e4m3 codes, one E8M0 "
+                     "scale per 32 elements, block magnitudes spread 2^-4..2^4)",
+    "decode_b4_long_mx": "decode batch 4 as decode_b4_long, indexer keys and queries MXFP8 (e4m3 codes, one "
+                         "E8M0 scale per 32 elements, block magnitudes spread 2^-4..2^4)",
 }
 
 
@@ -60,8 +64,9 @@ def algorithmic(wl):
     per_seq = {}
     for b, nn in zip(wl.q_seq, n):
         per_seq[int(b)] = max(per_seq.get(int(b), 0), int(nn))
-    key_bytes = sum(per_seq.values()) * (wl.D_I + 4)
-    qi_bytes = wl.T * wl.H_I * (wl.D_I + 8)
+    scale_bytes = wl.D_I // 32 if wl.idx_dtype == "mx_e4m3" else 4   # per key / per query head
+    key_bytes = sum(per_seq.values()) * (wl.D_I + scale_bytes)
+    qi_bytes = wl.T * wl.H_I * (wl.D_I + scale_bytes + 4)
     score_bytes = int(n.sum()) * 4
     gather = int(m.sum()) * (656 if wl.mla_dtype == "e4m3" else wl.d_qk * 2)
     q_bytes = wl.T * wl.H * wl.d_qk * 2
@@ -309,7 +314,8 @@ def main():
         return profile_stage(torch, dsa, W, wl, dev, args.stage, args.reps)
     alg = algorithmic(wl)
     copies_n = max(1, min(64, math.ceil(2 * L2_BYTES / max(alg["step_bytes"], 1)) + 1))
-    default_steps = {"decode_b1": 20000, "decode_b64": 2000, "decode_b4_long": 5000, "prefill_16k": 10}
+    default_steps = {"decode_b1": 20000, "decode_b64": 2000, "decode_b4_long": 5000, "prefill_16k": 10,
+                     "decode_b64_mx": 2000, "decode_b4_long_mx": 5000}
     steps = args.steps or default_steps[args.workload]
     warmup = max(3, args.warmup)
 

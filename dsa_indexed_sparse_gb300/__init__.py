@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libdsa.so")
 DSA_OK = 0
 STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
                 4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_DEVICE_CHECK"}
-DSA_F32, DSA_BF16, DSA_E4M3 = 0, 1, 2
+DSA_F32, DSA_BF16, DSA_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2, 3
 
 EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_plan",
             "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn_workspace_size",
@@ -168,12 +168,14 @@ class Indexer(_CachedDesc):
     q: torch.Tensor                    # [T, H_I, D_I] e4m3 codes (uint8) or fp32
     w: torch.Tensor                    # [T, H_I] fp32
     k_cache: torch.Tensor              # [cache_rows, D_I]
-    q_scale: Optional[torch.Tensor] = None
-    k_scale: Optional[torch.Tensor] = None
+    q_scale: Optional[torch.Tensor] = None   # fp32 [T, H_I], or uint8 E8M0 [T, H_I, D_I/32] (MXFP8)
+    k_scale: Optional[torch.Tensor] = None   # fp32 [cache_rows], or uint8 E8M0 [cache_rows, D_I/32] (MXFP8)
+    dtype: Optional[int] = None              # DSA_MXFP8_E4M3 for MXFP8 codes; else from k_cache
 
     def _build_desc(self) -> IndexerDesc:
         _, H_I, D_I = self.q.shape
-        return IndexerDesc(H_I, D_I, _dtype_code(self.k_cache), _ptr(self.q), _ptr(self.q_scale),
+        dt = self.dtype if self.dtype is not None else _dtype_code(self.k_cache)
+        return IndexerDesc(H_I, D_I, dt, _ptr(self.q), _ptr(self.q_scale),
                            _ptr(self.w), _ptr(self.k_cache), _ptr(self.k_scale))
 
 

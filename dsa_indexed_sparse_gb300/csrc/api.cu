@@ -80,17 +80,21 @@ dsa_status_t check_indexer(const dsa_seq_desc_t* s, const dsa_indexer_desc_t* x,
                            int64_t ld, dsa::IndexerArgs* out) {
   if (!x) return fail(DSA_ERR_INVALID_ARG, "indexer descriptor is NULL");
   if (x->H_I < 1 || x->D_I < 1) return fail(DSA_ERR_INVALID_ARG, "H_I and D_I must be >= 1");
-  if (x->dtype != DSA_E4M3 && x->dtype != DSA_F32)
-    return fail(DSA_ERR_UNSUPPORTED, "indexer dtype must be DSA_E4M3 or DSA_F32");
+  if (x->dtype != DSA_E4M3 && x->dtype != DSA_F32 && x->dtype != DSA_MXFP8_E4M3)
+    return fail(DSA_ERR_UNSUPPORTED, "indexer dtype must be DSA_E4M3, DSA_MXFP8_E4M3 or DSA_F32");
+  const bool mx = x->dtype == DSA_MXFP8_E4M3;
+  if (mx && x->D_I % 32 != 0) return fail(DSA_ERR_UNSUPPORTED, "MXFP8 index keys need D_I a multiple of 32");
   if (s->T > 0 && (!x->q || !x->w || !x->k_cache))
     return fail(DSA_ERR_INVALID_ARG, "indexer q, w and k_cache must be non-NULL");
+  if (s->T > 0 && mx && (!x->q_scale || !x->k_scale))
+    return fail(DSA_ERR_INVALID_ARG, "MXFP8 index keys need q_scale and k_scale");
   if (!aligned16(x->q) || !aligned16(x->k_cache) || !aligned16(x->w) || !aligned16(x->q_scale) ||
       !aligned16(x->k_scale))
     return fail(DSA_ERR_INVALID_ARG, "indexer pointers must be 16-byte aligned");
   if (ld < s->max_ctx || ld % 4 != 0) return fail(DSA_ERR_INVALID_ARG, "ld must be >= max_ctx and a multiple of 4");
   if (s->T > 0 && (!scores || !aligned16(scores)))
     return fail(DSA_ERR_INVALID_ARG, "scores must be non-NULL and 16-byte aligned");
-  *out = dsa::IndexerArgs{x->H_I, x->D_I, x->dtype == DSA_E4M3, x->q, x->q_scale, x->w,
+  *out = dsa::IndexerArgs{x->H_I, x->D_I, x->dtype != DSA_F32, mx, x->q, x->q_scale, x->w,
                           x->k_cache, x->k_scale, const_cast<float*>(scores), ld};
   return DSA_OK;
 }

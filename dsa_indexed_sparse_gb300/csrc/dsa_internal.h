@@ -23,12 +23,13 @@ struct SeqArgs {
 
 struct IndexerArgs {
   int32_t H_I, D_I;
-  bool e4m3;  // else fp32
+  bool e4m3;  // e4m3 codes (else fp32 values)
+  bool mx;    // e4m3 codes with E8M0 scales per 32 elements (q_scale/k_scale uint8)
   const void* q;
-  const float* q_scale;  // may be null
+  const void* q_scale;  // fp32 [T, H_I] (may be null) or uint8 [T, H_I, D_I/32] (mx)
   const float* w;
   const void* k;
-  const float* k_scale;  // may be null
+  const void* k_scale;  // fp32 [rows] (may be null) or uint8 [rows, D_I/32] (mx)
   float* scores;
   int64_t ld;
 };

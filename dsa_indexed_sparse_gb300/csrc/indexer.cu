@@ -37,13 +37,17 @@ namespace {
 // =============================================================== generic kernel
 constexpr int kGenThreads = 256;
 
-template <bool kE4M3>
+// kFmt: 0 fp32 values, 1 e4m3 codes with fp32 per-token / per-head scales,
+// 2 MXFP8 (e4m3 codes, E8M0 scale per 32 elements: the query is dequantised
+// into shared memory and each key element is dequantised as it is read; both
+// are exact in fp32).
+template <int kFmt>
 __global__ void __launch_bounds__(kGenThreads)
     indexer_generic_kernel(SeqArgs seq, IndexerArgs a) {
   grid_dep_wait();
   extern __shared__ float sm_gen[];
-  float* qf = sm_gen;                   // [H_I * D_I] query codes (as float)
-  float* wq = sm_gen + a.H_I * a.D_I;  // [H_I] w * q_scale
+  float* qf = sm_gen;                   // [H_I * D_I] query values (codes for kFmt 1)
+  float* wq = sm_gen + a.H_I * a.D_I;  // [H_I] w * q_scale (w for MXFP8)
   const int t = blockIdx.y;
   const int qpos = __ldg(seq.q_pos + t);
   const int b = __ldg(seq.q_seq + t);
@@ -52,14 +56,24 @@ __global__ void __launch_bounds__(kGenThreads)
     return;
   }
   const int HD = a.H_I * a.D_I;
+  const int nb = a.D_I / 32;            // MXFP8 blocks per vector
   for (int i = threadIdx.x; i < HD; i += blockDim.x) {
-    if (kE4M3)
-      qf[i] = e4m3_to_float(static_cast<const uint8_t*>(a.q)[static_cast<int64_t>(t) * HD + i]);
-    else
+    if (kFmt == 0) {
       qf[i] = static_cast<const float*>(a.q)[static_cast<int64_t>(t) * HD + i];
+    } else {
+      float v = e4m3_to_float(static_cast<const uint8_t*>(a.q)[static_cast<int64_t>(t) * HD + i]);
+      if (kFmt == 2) {
+        const int h = i / a.D_I, blk = (i % a.D_I) / 32;
+        const int e = static_cast<const uint8_t*>(a.q_scale)[(static_cast<int64_t>(t) * a.H_I + h) * nb + blk];
+        v = ldexpf(v, e - 127);
+      }
+      qf[i] = v;
+    }
   }
   for (int h = threadIdx.x; h < a.H_I; h += blockDim.x) {
-    const float sq = a.q_scale ? __ldg(a.q_scale + static_cast<int64_t>(t) * a.H_I + h) : 1.f;
+    const float sq = (kFmt != 2 && a.q_scale)
+                         ? __ldg(static_cast<const float*>(a.q_scale) + static_cast<int64_t>(t) * a.H_I + h)
+                         : 1.f;
     wq[h] = __ldg(a.w + static_cast<int64_t>(t) * a.H_I + h) * sq;
   }
   __syncthreads();
@@ -71,16 +85,21 @@ __global__ void __launch_bounds__(kGenThreads)
   float acc = 0.f;
   for (int h = 0; h < a.H_I; ++h) {
     float d = 0.f;
-    if (kE4M3) {
+    if (kFmt == 0) {
+      const float* kr = static_cast<const float*>(a.k) + row * a.D_I;
+      for (int i = 0; i < a.D_I; ++i) d = fmaf(qf[h * a.D_I + i], kr[i], d);
+    } else if (kFmt == 1) {
       const uint8_t* kr = static_cast<const uint8_t*>(a.k) + row * a.D_I;
       for (int i = 0; i < a.D_I; ++i) d = fmaf(qf[h * a.D_I + i], e4m3_to_float(kr[i]), d);
     } else {
-      const float* kr = static_cast<const float*>(a.k) + row * a.D_I;
-      for (int i = 0; i < a.D_I; ++i) d = fmaf(qf[h * a.D_I + i], kr[i], d);
+      const uint8_t* kr = static_cast<const uint8_t*>(a.k) + row * a.D_I;
+      const uint8_t* ke = static_cast<const uint8_t*>(a.k_scale) + row * nb;
+      for (int i = 0; i < a.D_I; ++i)
+        d = fmaf(qf[h * a.D_I + i], ldexpf(e4m3_to_float(kr[i]), static_cast<int>(ke[i / 32]) - 127), d);
     }
     acc = fmaf(wq[h], fmaxf(d, 0.f), acc);
   }
-  const float sk = a.k_scale ? __ldg(a.k_scale + row) : 1.f;
+  const float sk = (kFmt != 2 && a.k_scale) ? __ldg(static_cast<const float*>(a.k_scale) + row) : 1.f;
   a.scores[static_cast<int64_t>(t) * a.ld + s] = acc * sk;
 }
 
@@ -93,23 +112,36 @@ constexpr int kTcStages = 6;       // key-tile ring depth (16 KB each)
 // warp 0 TMA, warp 1 MMA, then the epilogue: one warp per (query of the group,
 // TMEM lane quarter), so 4*G warps.  The ReLU-weighted head sums (two CUDA-core
 // operations per key, query and head) cost about as much issue time as the
-// MMAs' tensor time, so they get every warp slot the register budget allows.
+// MMAs' tensor time at prefill, so they get every warp slot the register
+// budget allows.  (Splitting a single query's heads over two warps per quarter
+// made the decode configurations slower.)
 template <int G>
 struct TcWarps {
   static constexpr int kEpiWarps = 4 * G;
   static constexpr int kThreads = 64 + 32 * kEpiWarps;
 };
 
-template <int G>
+// kMx: MXFP8 keys and queries (E8M0 scale per 32 elements).  The four 32-wide
+// blocks of the K = 128 dot product go to four separate accumulators (one
+// MMA each, no accumulation), which the epilogue scales by the two blocks'
+// power-of-two factors and sums: d = sum_b 2^(eq_b + ek_b - 254) * D_b.
+template <int G, bool kMx = false>
 struct TcCfg {
+  static_assert(!kMx || G == 1, "MXFP8 keys run one query per group");
   static constexpr int N = kTcHeads * G;                 // UMMA N
+  static constexpr int kBlocks = kMx ? kTcDim / 32 : 1;  // accumulators per tile
+  static constexpr int kAccCols = kBlocks * N;           // TMEM columns per tile
   static constexpr int kStageBytes = kTcKeys * kTcDim;   // 16384
   static constexpr int kQBytes = N * kTcDim;             // one query-group buffer
-  static constexpr uint32_t kTmemCols = (2 * N <= 128) ? 128u : ((2 * N <= 256) ? 256u : 512u);
+  static constexpr uint32_t kTmemCols = (2 * kAccCols <= 128) ? 128u : ((2 * kAccCols <= 256) ? 256u : 512u);
+  // per epilogue warp: w / 2 for its 64 heads, then (MXFP8) the query's block
+  // factors 2^(e - 127) as float [4][64]
+  static constexpr int kSlice = kTcHeads * (1 + (kMx ? kBlocks : 0));
   static constexpr int kOffStages = 0;
   static constexpr int kOffQ = kOffStages + kTcStages * kStageBytes;
-  static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [4G][64]: each epilogue warp's head weights
-  static constexpr int kOffScale = kOffWq + TcWarps<G>::kEpiWarps * kTcHeads * 4;  // float [stages][128] key scales
+  static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [4G][kSlice]: each epilogue warp's slice
+  // key scales: 4 bytes per key (an fp32 scale, or MXFP8's four E8M0 bytes)
+  static constexpr int kOffScale = kOffWq + TcWarps<G>::kEpiWarps * kSlice * 4;
   static constexpr int kOffValid = kOffScale + kTcStages * kTcKeys * 4;  // uint32 [stages]
   static constexpr int kOffBar = kOffValid + kTcStages * 4 + 8;
   // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2]
@@ -179,11 +211,11 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
   return tot;
 }
 
-template <int G>
+template <int G, bool kMx>
 __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap qmap, TcParams p) {
-  using C = TcCfg<G>;
+  using C = TcCfg<G, kMx>;
   constexpr int kTcThreads = TcWarps<G>::kThreads;
   constexpr int kEpiWarps = TcWarps<G>::kEpiWarps;
   static_assert(4 + kTcThreads / 32 <= 64, "misc area holds one int per warp");
@@ -252,7 +284,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   // ---- barriers and TMEM -------------------------------------------------
   if (threadIdx.x == 0) {
     // full: the producer's expect_tx arrival, plus one cp.async arrival per lane
-    // of the producer warp when the keys carry scales
+    // of the producer warp when the keys carry scales (always for MXFP8)
     const uint32_t full_count = 1u + (p.a.k_scale != nullptr ? 32u : 0u);
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&full[i], full_count);
@@ -349,7 +381,8 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         const int32_t pid = half ? pid1 : pid0;
         if (pid >= 0)
           cp_async16(smem_u32(scale_s + st * kTcKeys + half * kTcPage + (lane & 15) * 4),
-                     p.a.k_scale + static_cast<int64_t>(pid) * kTcPage + (lane & 15) * 4);
+                     static_cast<const uint8_t*>(p.a.k_scale) +
+                         (static_cast<int64_t>(pid) * kTcPage + (lane & 15) * 4) * 4);
         cp_async_mbar_arrive(&full[st]);
       }
     }
@@ -383,11 +416,16 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       // the start-address field; one elected lane issues the block
       const uint64_t da = make_sdesc(smem_u32(sm + C::kOffStages + st * C::kStageBytes), 16, 1024, kLayoutSw128);
       const uint64_t db = make_sdesc(smem_u32(sm + C::kOffQ + qb * C::kQBytes), 16, 1024, kLayoutSw128);
-      const uint32_t dcol = tmem + ab * C::N;
+      const uint32_t dcol = tmem + ab * C::kAccCols;
       if (elect_one()) {
 #pragma unroll
-        for (int k = 0; k < kTcDim / 32; ++k)
-          umma_f8(dcol, da + static_cast<uint64_t>(2 * k), db + static_cast<uint64_t>(2 * k), C::kIdesc, k > 0 ? 1u : 0u);
+        for (int k = 0; k < kTcDim / 32; ++k) {
+          if (kMx)   // block k into its own accumulator
+            umma_f8(dcol + k * C::N, da + static_cast<uint64_t>(2 * k), db + static_cast<uint64_t>(2 * k), C::kIdesc, 0u);
+          else
+            umma_f8(dcol, da + static_cast<uint64_t>(2 * k), db + static_cast<uint64_t>(2 * k), C::kIdesc,
+                    k > 0 ? 1u : 0u);
+        }
         umma_commit(&empty[st]);
         umma_commit(&accfull[ab]);
       }
@@ -402,10 +440,11 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     // global-memory round trip.
     const int e = warp - 2;
     const int quarter = warp & 3;
-    const int j = e >> 2;
+    const int j = e >> 2;                     // query of the group
     const int row = quarter * 32 + lane;          // key within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    float* wq = wq_s + e * kTcHeads;
+    float* wq = wq_s + e * C::kSlice;
+    float* cq = wq + kTcHeads;   // MXFP8: the query's block factors [4][64]
     TileWalker<G> w;
     w.init(p, g_start, kt_start);
     int cur_g = -1, qp = -1;
@@ -416,6 +455,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     // and position, and lanes' two head weights and query scales
     int pf_g = -1, pf_b = 0, pf_qs = 0, pf_qp = -1;
     float pf_w0 = 0.f, pf_w1 = 0.f, pf_s0 = 1.f, pf_s1 = 1.f;
+    uint32_t pf_e0 = 0x7F7F7F7Fu, pf_e1 = 0x7F7F7F7Fu;   // MXFP8: the two heads' four E8M0 bytes
     auto prefetch = [&](int g) {
       pf_g = g;
       const int t = g * G + j;
@@ -430,9 +470,12 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         const int64_t o = static_cast<int64_t>(t) * kTcHeads + 2 * lane;
         pf_w0 = __ldg(p.a.w + o);
         pf_w1 = __ldg(p.a.w + o + 1);
-        if (p.a.q_scale) {
-          pf_s0 = __ldg(p.a.q_scale + o);
-          pf_s1 = __ldg(p.a.q_scale + o + 1);
+        if (kMx) {
+          pf_e0 = __ldg(static_cast<const uint32_t*>(p.a.q_scale) + o);
+          pf_e1 = __ldg(static_cast<const uint32_t*>(p.a.q_scale) + o + 1);
+        } else if (p.a.q_scale) {
+          pf_s0 = __ldg(static_cast<const float*>(p.a.q_scale) + o);
+          pf_s1 = __ldg(static_cast<const float*>(p.a.q_scale) + o + 1);
         }
       }
     };
@@ -453,6 +496,13 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         // max on the half-rate ALU pipe.
         wq[2 * lane] = 0.5f * (pf_w0 * pf_s0);
         wq[2 * lane + 1] = 0.5f * (pf_w1 * pf_s1);
+        if (kMx) {
+#pragma unroll
+          for (int bk = 0; bk < C::kBlocks; ++bk) {
+            cq[bk * kTcHeads + 2 * lane] = ldexpf(1.f, static_cast<int>((pf_e0 >> (8 * bk)) & 0xFFu) - 127);
+            cq[bk * kTcHeads + 2 * lane + 1] = ldexpf(1.f, static_cast<int>((pf_e1 >> (8 * bk)) & 0xFFu) - 127);
+          }
+        }
         __syncwarp();
         cur_g = w.g;
         if (w.g + 1 < p.n_groups) prefetch(w.g + 1);
@@ -471,38 +521,85 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       asm volatile("ld.shared.u32 %0, [%1];" : "=r"(vmask) : "r"(valid_addr + st * 4) : "memory");
       const bool key_ok = s < w.nhist && ((vmask >> (row >> 6)) & 1u);
       float sk = 1.f;
-      if (p.a.k_scale)
+      uint32_t ek = 0;   // MXFP8: this key's four E8M0 bytes
+      if (kMx)
+        asm volatile("ld.shared.u32 %0, [%1];" : "=r"(ek) : "r"(scale_addr + st * (kTcKeys * 4)) : "memory");
+      else if (p.a.k_scale)
         asm volatile("ld.shared.f32 %0, [%1];" : "=f"(sk) : "r"(scale_addr + st * (kTcKeys * 4)) : "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      // the 64 heads in two halves of 32 columns (fewer live registers: 18 warps
-      // leave 96 a thread); head weights as 16-byte broadcast loads
-      const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
       const float4* w4 = reinterpret_cast<const float4*>(wq);
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if constexpr (kMx) {
+        // d[h] = sum_b D_b[h] * 2^(eq_b[h] - 127) * 2^(ek_b - 127), 32 heads at a time
+        const uint32_t col = tmem + lane_off + ab * C::kAccCols;
+        float kx[C::kBlocks];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t v[32];
-        tmem_ld32(col + 32 * hh, v);
-        tmem_ld_wait();
-        if (hh == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&accempty[ab]);   // the accumulator is in registers
-        }
-        // x + |x| per head, then packed fmas over head pairs: eight running sums
+        for (int bk = 0; bk < C::kBlocks; ++bk) kx[bk] = ldexpf(1.f, static_cast<int>((ek >> (8 * bk)) & 0xFFu) - 127);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float4 wv = w4[8 * hh + i];
-          const int a = 4 * (i & 1);
-          float y[4];
+        for (int hh = 0; hh < 2; ++hh) {
+          float d[32];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float x = __uint_as_float(v[4 * i + k]);
-            y[k] = x + fabsf(x);
+          for (int i = 0; i < 32; ++i) d[i] = 0.f;
+#pragma unroll
+          for (int bk = 0; bk < C::kBlocks; ++bk) {
+            uint32_t v[32];
+            tmem_ld32(col + bk * C::N + 32 * hh, v);
+            tmem_ld_wait();
+            if (hh == 1 && bk == C::kBlocks - 1) {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(&accempty[ab]);   // the accumulators are in registers
+            }
+            // packed over head pairs: f = query factor * key factor, d += D * f
+            const float4* c4 = reinterpret_cast<const float4*>(cq + bk * kTcHeads + 32 * hh);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float4 cv = c4[i];
+              float f0, f1, f2, f3;
+              mul2(f0, f1, cv.x, cv.y, kx[bk], kx[bk]);
+              mul2(f2, f3, cv.z, cv.w, kx[bk], kx[bk]);
+              fma2(d[4 * i], d[4 * i + 1], __uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]), f0, f1);
+              fma2(d[4 * i + 2], d[4 * i + 3], __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]), f2, f3);
+            }
           }
-          fma2(acc[a], acc[a + 1], wv.x, wv.y, y[0], y[1]);
-          fma2(acc[a + 2], acc[a + 3], wv.z, wv.w, y[2], y[3]);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 wv = w4[8 * hh + i];
+            const int a = 4 * (i & 1);
+            fma2(acc[a], acc[a + 1], wv.x, wv.y, d[4 * i] + fabsf(d[4 * i]), d[4 * i + 1] + fabsf(d[4 * i + 1]));
+            fma2(acc[a + 2], acc[a + 3], wv.z, wv.w, d[4 * i + 2] + fabsf(d[4 * i + 2]),
+                 d[4 * i + 3] + fabsf(d[4 * i + 3]));
+          }
+        }
+      } else {
+        // the 64 heads in two halves of 32 columns (fewer live registers: 18 warps
+        // leave 96 a thread); head weights as 16-byte broadcast loads
+        const uint32_t col = tmem + lane_off + ab * C::N + j * kTcHeads;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tmem_ld32(col + 32 * hh, v);
+          tmem_ld_wait();
+          if (hh == 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[ab]);   // the accumulator is in registers
+          }
+          // x + |x| per head, then packed fmas over head pairs: eight running sums
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float4 wv = w4[8 * hh + i];
+            const int a = 4 * (i & 1);
+            float y[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const float x = __uint_as_float(v[4 * i + k]);
+              y[k] = x + fabsf(x);
+            }
+            fma2(acc[a], acc[a + 1], wv.x, wv.y, y[0], y[1]);
+            fma2(acc[a + 2], acc[a + 3], wv.z, wv.w, y[2], y[3]);
+          }
         }
       }
       const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
@@ -519,10 +616,10 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   }
 }
 
-template <int G>
+template <int G, bool kMx = false>
 cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
                       std::string* plan, bool* unsupported, std::string* why) {
-  using C = TcCfg<G>;
+  using C = TcCfg<G, kMx>;
   alignas(64) CUtensorMap kmap, qmap;
   if (!encode_tmap_2d_u8(&kmap, a.k, kTcDim, static_cast<uint64_t>(seq.cache_rows), kTcDim,
                          kTcDim, kTcPage, why) ||
@@ -538,16 +635,16 @@ cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv&
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(indexer_tc_kernel<G>,
+    attr_err = cudaFuncSetAttribute(indexer_tc_kernel<G, kMx>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  const cudaError_t le = launch_kernel(indexer_tc_kernel<G>, dim3(grid), dim3(TcWarps<G>::kThreads), C::kSmemBytes,
+  const cudaError_t le = launch_kernel(indexer_tc_kernel<G, kMx>, dim3(grid), dim3(TcWarps<G>::kThreads), C::kSmemBytes,
                                        env.stream, true, 1,
                                     kmap, qmap, p);
   if (le != cudaSuccess) return le;
   char buf[160];
-  snprintf(buf, sizeof(buf), "indexer_tc<G=%d>[grid=%d,tiles<=%lld]", G, grid,
+  snprintf(buf, sizeof(buf), "indexer_tc<G=%d%s>[grid=%d,tiles<=%lld]", G, kMx ? ",mxfp8" : "", grid,
            static_cast<long long>(tiles_ub));
   *plan += buf;
   return cudaGetLastError();
@@ -566,6 +663,7 @@ cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const Launc
                      (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(a.q) % 16 == 0);
   if (tc_ok) {
+    if (a.mx) return launch_tc<1, true>(seq, a, env, plan, unsupported, why);
     const int qps = seq.q_per_seq;
     if (qps > 0 && qps % 4 == 0) return launch_tc<4>(seq, a, env, plan, unsupported, why);
     if (qps > 0 && qps % 2 == 0) return launch_tc<2>(seq, a, env, plan, unsupported, why);
@@ -578,20 +676,13 @@ cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const Launc
     return cudaSuccess;
   }
   dim3 grid((seq.max_ctx + kGenThreads - 1) / kGenThreads, seq.T);
-  if (a.e4m3) {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(indexer_generic_kernel<true>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    const cudaError_t le = launch_kernel(indexer_generic_kernel<true>, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
-    if (le != cudaSuccess) return le;
-  } else {
-    if (smem > 48 * 1024)
-      cudaFuncSetAttribute(indexer_generic_kernel<false>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    const cudaError_t le = launch_kernel(indexer_generic_kernel<false>, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
-    if (le != cudaSuccess) return le;
-  }
-  *plan += a.e4m3 ? "indexer_generic<e4m3>" : "indexer_generic<f32>";
+  const int fmt = a.mx ? 2 : (a.e4m3 ? 1 : 0);
+  void (*kern)(SeqArgs, IndexerArgs) = fmt == 2 ? indexer_generic_kernel<2>
+                                       : (fmt == 1 ? indexer_generic_kernel<1> : indexer_generic_kernel<0>);
+  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  const cudaError_t le = launch_kernel(kern, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
+  if (le != cudaSuccess) return le;
+  *plan += fmt == 2 ? "indexer_generic<mxfp8>" : (fmt == 1 ? "indexer_generic<e4m3>" : "indexer_generic<f32>");
   return cudaGetLastError();
 }
 

@@ -130,6 +130,11 @@ def spec(name: str, **over) -> Spec:
         "prefill_16k": dict(ctx=[16384], q_len=16384, K=2048, low_rank=8),
         # 4 x 131072 context, FP8 latent cache with per-token fp32 scale
         "decode_b4_long": dict(ctx=[131072] * 4, B=4, q_len=1, K=2048, mla_dtype="e4m3"),
+        # the same two decode shapes with MXFP8 index keys and queries (E8M0 per 32)
+        "decode_b64_mx": dict(ctx=None, ctx_range=(2048, 8192), B=64, q_len=1, K=2048,
+                              shuffle_pages=True, idx_dtype="mx_e4m3"),
+        "decode_b4_long_mx": dict(ctx=[131072] * 4, B=4, q_len=1, K=2048, mla_dtype="e4m3",
+                                  idx_dtype="mx_e4m3"),
     }[name]
     base.update(over)
     if base.get("ctx") is not None:

@@ -59,7 +59,10 @@ typedef enum dsa_status {
 typedef enum dsa_dtype {
   DSA_F32 = 0,
   DSA_BF16 = 1,
-  DSA_E4M3 = 2               /* OCP FP8 E4M3 codes (bias 7, max 448, no inf)      */
+  DSA_E4M3 = 2,              /* OCP FP8 E4M3 codes (bias 7, max 448, no inf)      */
+  DSA_MXFP8_E4M3 = 3         /* OCP MXFP8: E4M3 codes, one E8M0 scale byte         */
+                             /* 2**(e - 127) per 32 consecutive elements (indexer  */
+                             /* only)                                              */
 } dsa_dtype_t;
 
 typedef void* dsa_stream_t;  /* cudaStream_t */
@@ -87,16 +90,27 @@ typedef struct dsa_seq_desc {
                              /* page_size                                          */
 } dsa_seq_desc_t;
 
-/* Lightning indexer inputs (dequantised value = code * scale). */
+/* Lightning indexer inputs (dequantised value = code * scale).
+ * "Day0 Inference Adaptation and Performance Optimization for Kimi K3.1 Pro",
+ * section 4, and "Large Language Model Inference Acceleration in Practice",
+ * section 4: FP8 index keys and queries, with MXFP8 (blocks of 32 sharing a
+ * power-of-two scale) as the pages' own granularity.
+ *   DSA_E4M3:       q_scale fp32 [T, H_I] (per query head), k_scale fp32
+ *                   [cache_rows] (per key); either may be NULL for all-ones.
+ *   DSA_MXFP8_E4M3: q_scale uint8 [T, H_I, D_I/32], k_scale uint8
+ *                   [cache_rows, D_I/32]: E8M0 exponents, element i of a vector
+ *                   is code * 2**(scale[i / 32] - 127); both required; D_I a
+ *                   multiple of 32.
+ *   DSA_F32:        q and k_cache hold fp32 values; scales as for DSA_E4M3. */
 typedef struct dsa_indexer_desc {
   int32_t H_I;               /* indexer heads                                      */
   int32_t D_I;               /* indexer head dim                                   */
-  dsa_dtype_t dtype;         /* DSA_E4M3 or DSA_F32, for both q and k_cache        */
+  dsa_dtype_t dtype;         /* DSA_E4M3, DSA_MXFP8_E4M3 or DSA_F32 (q and k_cache) */
   const void* q;             /* device [T, H_I, D_I]                               */
-  const float* q_scale;      /* device fp32 [T, H_I], or NULL for all-ones         */
+  const void* q_scale;       /* device query scales (layout by dtype, above)       */
   const float* w;            /* device fp32 [T, H_I] head weights                  */
   const void* k_cache;       /* device [cache_rows, D_I]                           */
-  const float* k_scale;      /* device fp32 [cache_rows] per-token, or NULL        */
+  const void* k_scale;       /* device key scales (layout by dtype, above)         */
 } dsa_indexer_desc_t;
 
 /* MLA latent attention inputs (MQA form: one latent row per position, shared by

@@ -1,6 +1,7 @@
 """GPU parity at the full benchmark sizes (decode batch 1 at 32768 positions,
 decode batch 64 over ragged shuffled pages, long-context batch 4 with the FP8
-latent cache, and the 16384-token causal prefill), in the launch configuration
+latent cache -- also with MXFP8 index keys -- and the 16384-token causal
+prefill), in the launch configuration
 the benchmark times: one ``dsa_decode_step`` over the whole batch.
 
 The oracle is too slow for every output at these sizes, so each test samples
@@ -36,6 +37,7 @@ SIZES = {
     "decode_b64": 4,
     "decode_b4_long": 0,
     "prefill_16k": 3,
+    "decode_b4_long_mx": 0,   # MXFP8 index keys at the long-context size
 }
 
 

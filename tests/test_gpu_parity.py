@@ -34,6 +34,13 @@ CASES = {
     "qlen8_b3_shuffled": ("decode_b64", dict(ctx_range=(300, 2500), B=3, q_len=8, K=256)),
     # FP8 cache at a batch where every query gets one row slice: 64 tiles per CTA
     "fp8_b80_single_slice": ("decode_b4_long", dict(ctx=[2100] * 80, B=80, K=2048)),
+    # MXFP8 index keys and queries (E8M0 scale per 32 elements; block magnitudes
+    # spread over 2**-4..2**4): ragged shuffled batch, several query tokens per
+    # sequence, a causal prefill, and with the FP8 latent cache
+    "mx_b5_shuffled": ("decode_b64", dict(ctx_range=(100, 3000), B=5, K=256, idx_dtype="mx_e4m3")),
+    "mx_qlen4": ("decode_b1", dict(ctx=[900], q_len=4, K=128, idx_dtype="mx_e4m3")),
+    "mx_prefill_300": ("prefill_16k", dict(ctx=[300], q_len=300, K=64, idx_dtype="mx_e4m3")),
+    "mx_fp8_b2": ("decode_b4_long", dict(ctx=[3000, 4100], B=2, K=2048, idx_dtype="mx_e4m3")),
 }
 
 
@@ -118,6 +125,21 @@ def test_generic_indexer_e4m3_matches_oracle(dev):
     g, plan = run.scores()
     assert plan == "indexer_generic<e4m3>"
     P.check_scores(g, O.indexer_scores(wl), wl.q_pos)
+
+
+def test_generic_indexer_mxfp8_matches_oracle(dev):
+    """MXFP8 with dims the tensor-core path does not cover (H_I = 6, D_I = 64)."""
+    wl = W.make("decode_b64", seed=4, ctx_range=(300, 900), B=2, K=64, H_I=6, D_I=64, idx_dtype="mx_e4m3")
+    run = P.Run(wl, dev)
+    g, plan = run.scores()
+    assert plan == "indexer_generic<mxfp8>"
+    P.check_scores(g, O.indexer_scores(wl), wl.q_pos)
+
+
+def test_mxfp8_tensor_core_plan(dev):
+    wl = W.make("decode_b64", seed=5, ctx_range=(200, 400), B=3, K=64, q_len=2, idx_dtype="mx_e4m3")
+    _, plan = P.Run(wl, dev).scores()
+    assert plan.startswith("indexer_tc<G=1,mxfp8>"), plan
 
 
 # --------------------------------------------------------------------------- top-k edges
