@@ -67,7 +67,7 @@ class Workload:
     k_i: np.ndarray
     k_i_scale: np.ndarray        # float32 [cache_rows]
     # MLA latent attention
-    mla_dtype: str               # "bf16" | "e4m3" | "f32"
+    mla_dtype: str               # "bf16" | "e4m3" (per-token scale) | "e4m3_t128" (scale per 128 latent dims) | "f32"
     H: int
     d_latent: int
     d_rope: int
@@ -135,6 +135,8 @@ def spec(name: str, **over) -> Spec:
                               shuffle_pages=True, idx_dtype="mx_e4m3"),
         "decode_b4_long_mx": dict(ctx=[131072] * 4, B=4, q_len=1, K=2048, mla_dtype="e4m3",
                                   idx_dtype="mx_e4m3"),
+        # long decode with the FP8 latent cache scaled per 128-dim tile
+        "decode_b4_long_t128": dict(ctx=[131072] * 4, B=4, q_len=1, K=2048, mla_dtype="e4m3_t128"),
     }[name]
     base.update(over)
     if base.get("ctx") is not None:
@@ -154,14 +156,14 @@ MX_BLOCK = 32        # elements sharing one E8M0 scale (OCP MXFP8)
 E4M3_EMAX = 8        # exponent of the largest normal E4M3 value (448 = 1.75 * 2**8)
 
 
-def _quant_blocks_mx(x: torch.Tensor):
-    """OCP MXFP8 along the last axis: blocks of 32 elements share an E8M0 scale
-    2**(e - 127) with e - 127 = floor(log2(amax of the block)) - 8 (-127 for an
-    all-zero block); elements are the E4M3 values nearest to x / scale (ties to
-    even), clamped to +-448.  Returns (uint8 codes, uint8 E8M0 exponents with
-    the block axis last)."""
+def _quant_blocks_mx(x: torch.Tensor, block: int = MX_BLOCK):
+    """OCP MXFP8 along the last axis: blocks of `block` (32) elements share an
+    E8M0 scale 2**(e - 127) with e - 127 = floor(log2(amax of the block)) - 8
+    (-127 for an all-zero block); elements are the E4M3 values nearest to
+    x / scale (ties to even), clamped to +-448.  Returns (uint8 codes, uint8 E8M0
+    exponents with the block axis last)."""
     shp = x.shape
-    xb = x.reshape(*shp[:-1], shp[-1] // MX_BLOCK, MX_BLOCK)
+    xb = x.reshape(*shp[:-1], shp[-1] // block, block)
     amax = xb.abs().amax(dim=-1, keepdim=True)
     _, e = torch.frexp(amax)                          # amax = m * 2**e, m in [0.5, 1)
     sexp = torch.where(amax > 0, e - 1 - E4M3_EMAX, torch.full_like(e, -127)).clamp(-127, 127)
@@ -170,12 +172,12 @@ def _quant_blocks_mx(x: torch.Tensor):
             (sexp + 127).to(torch.uint8).squeeze(-1).numpy())
 
 
-def _spread_blocks(g: torch.Generator, x: torch.Tensor, spread: int):
-    """Multiplies every 32-element block of the last axis by 2**r, r uniform in
-    [-spread, spread] (seeded), so that blocks of one vector differ in range."""
+def _spread_blocks(g: torch.Generator, x: torch.Tensor, spread: int, block: int = MX_BLOCK):
+    """Multiplies every `block`-element block of the last axis by 2**r, r uniform
+    in [-spread, spread] (seeded), so that blocks of one vector differ in range."""
     shp = x.shape
-    r = torch.randint(-spread, spread + 1, (*shp[:-1], shp[-1] // MX_BLOCK, 1), generator=g)
-    x.view(*shp[:-1], shp[-1] // MX_BLOCK, MX_BLOCK).mul_(torch.pow(2.0, r.to(torch.float32)))
+    r = torch.randint(-spread, spread + 1, (*shp[:-1], shp[-1] // block, 1), generator=g)
+    x.view(*shp[:-1], shp[-1] // block, block).mul_(torch.pow(2.0, r.to(torch.float32)))
 
 
 def _bf16_bits(x: torch.Tensor) -> np.ndarray:
@@ -276,6 +278,19 @@ def make(name_or_spec, seed: int = 0, **over) -> Workload:
         kv[:, FP8_SCALE_OFFSET:FP8_SCALE_OFFSET + 4] = scale.astype("<f4").view(np.uint8).reshape(-1, 4)
         kv[:, FP8_ROPE_OFFSET:] = _bf16_bits(kv_f[:, sp.d_latent:]).view(np.uint8).reshape(cache_rows, -1)
         row_bytes = FP8_ROW_BYTES
+    elif sp.mla_dtype == "e4m3_t128":
+        # the same 656-byte row with four scales, one per 128 latent dims, each a
+        # power of two (the shared-exponent rule of the MX formats on 128-blocks)
+        assert sp.d_latent == 512 and sp.d_rope == 64
+        lat = kv_f[:, :sp.d_latent].contiguous()
+        _spread_blocks(g, lat, 2, block=128)
+        codes, exps = _quant_blocks_mx(lat, block=128)
+        scales = np.ldexp(np.float32(1.0), exps.astype(np.int32) - 127).astype("<f4")   # [rows, 4]
+        kv = np.zeros((cache_rows, FP8_ROW_BYTES), dtype=np.uint8)
+        kv[:, :512] = codes
+        kv[:, FP8_SCALE_OFFSET:FP8_SCALE_OFFSET + 16] = scales.view(np.uint8).reshape(-1, 16)
+        kv[:, FP8_ROPE_OFFSET:] = _bf16_bits(kv_f[:, sp.d_latent:]).view(np.uint8).reshape(cache_rows, -1)
+        row_bytes = FP8_ROW_BYTES
     elif sp.mla_dtype == "f32":
         kv = kv_f.numpy()
         row_bytes = dk * 4
@@ -330,6 +345,9 @@ def device_tensors(wl: Workload, device, copies: int = 1) -> dict:
         elif wl.mla_dtype == "e4m3":
             q, kv = t(wl.q.view(np.int16), torch.bfloat16), t(wl.kv)
             dt = 2  # FP8 row format
+        elif wl.mla_dtype == "e4m3_t128":
+            q, kv = t(wl.q.view(np.int16), torch.bfloat16), t(wl.kv)
+            dt = 4  # FP8 rows with a power-of-two scale per 128 latent dims
         else:
             q, kv = t(wl.q), t(wl.kv)
             dt = None

@@ -28,6 +28,12 @@ the method states it:
    (same page, section 1.2, SFA sub-module; section 3.1 on reading the selected
    rows from the paged KV cache).
 
+The FP8 latent cache comes in two granularities: one fp32 scale per token
+(656-byte rows, scale at byte 512), or -- the pages' per-token-tile-128 variant
+("Large Language Model Inference Acceleration in Practice", section 4;
+"Day0 ... Kimi K3.1 Pro", section 4) -- four fp32 scales per token at bytes
+[512, 528), one per 128 latent dims.
+
 Readings taken where the pages are silent (each also listed in the design doc):
 * a query at position p sees s in [0, p] inclusive (its own key is cached);
 * scores are formed in float64 and then rounded to float32 once -- the Top-K
@@ -189,8 +195,14 @@ def latent_rows(wl, rows: np.ndarray) -> np.ndarray:
         return decode_bf16(wl.kv[rows])
     if wl.mla_dtype == "f32":
         return wl.kv[rows].astype(np.float64)
-    # 656-byte FP8 row: [0,512) e4m3 latent, [512,516) fp32 scale, [528,656) bf16 rope
     raw = wl.kv[rows]
+    if wl.mla_dtype == "e4m3_t128":
+        # 656-byte FP8 row with four fp32 scales at [512,528), one per 128 latent dims
+        scales = raw[:, 512:528].copy().view("<f4").astype(np.float64)   # [n, 4]
+        latent = decode_e4m3(raw[:, :512]) * np.repeat(scales, 128, axis=1)
+        rope = decode_bf16(raw[:, 528:656].copy().view("<u2"))
+        return np.concatenate([latent, rope], axis=1)
+    # 656-byte FP8 row: [0,512) e4m3 latent, [512,516) fp32 scale, [528,656) bf16 rope
     scale = raw[:, 512:516].copy().view("<f4").astype(np.float64)  # [n, 1]
     latent = decode_e4m3(raw[:, :512]) * scale
     rope = decode_bf16(raw[:, 528:656].copy().view("<u2"))

@@ -496,3 +496,20 @@ def test_mx_indexer_one_block_closed_form():
     kcode = torch.from_numpy(wl.k_i[rows, i].copy()).view(torch.float8_e4m3fn).double().numpy()
     expect = np.maximum(kcode * np.exp2(wl.k_i_scale[rows, b].astype(np.float64) - 127) * 2.0 ** a, 0.0)
     np.testing.assert_array_equal(got, expect.astype(np.float32))
+
+
+def test_fp8_tile128_latent_row_decode():
+    """656-byte rows with one scale per 128 latent dims: latent = code * scale of
+    its tile (decoded with torch's E4M3 view), rope = bf16; the generator's tile
+    scales are powers of two (so bf16 holds code * scale exactly)."""
+    wl = small("decode_b4_long", ctx=[300], K=64, mla_dtype="e4m3_t128")
+    row = wl.kv[7]
+    scales = row[512:528].copy().view("<f4").astype(np.float64)
+    assert np.all(np.log2(scales) == np.round(np.log2(scales)))
+    lat = torch.from_numpy(row[:512].copy()).view(torch.float8_e4m3fn).double().numpy() * np.repeat(scales, 128)
+    rope = torch.from_numpy(row[528:656].copy()).view(torch.bfloat16).double().numpy()
+    got = O.latent_rows(wl, np.array([7]))[0]
+    assert np.array_equal(got[:512], lat) and np.array_equal(got[512:], rope)
+    # exact in bf16: widening code * scale to bf16 loses nothing
+    b = torch.from_numpy(lat).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(b, lat)
