@@ -40,6 +40,8 @@ DESCRIPTIONS = {
                      "scale per 32 elements, block magnitudes spread 2^-4..2^4)",
     "decode_b4_long_mx": "decode batch 4 as decode_b4_long, indexer keys and queries MXFP8 (e4m3 codes, one "
                          "E8M0 scale per 32 elements, block magnitudes spread 2^-4..2^4)",
+    "decode_b4_long_t128": "decode batch 4 as decode_b4_long, FP8 latent rows with one power-of-two scale per "
+                           "128 latent dims (tile magnitudes scaled by 2^{0,-1,-2})",
 }
 
 
@@ -68,7 +70,7 @@ def algorithmic(wl):
     key_bytes = sum(per_seq.values()) * (wl.D_I + scale_bytes)
     qi_bytes = wl.T * wl.H_I * (wl.D_I + scale_bytes + 4)
     score_bytes = int(n.sum()) * 4
-    gather = int(m.sum()) * (656 if wl.mla_dtype == "e4m3" else wl.d_qk * 2)
+    gather = int(m.sum()) * (656 if wl.mla_dtype in ("e4m3", "e4m3_t128") else wl.d_qk * 2)
     q_bytes = wl.T * wl.H * wl.d_qk * 2
     out_bytes = wl.T * wl.H * (wl.d_v * 2 + 4)
     idx_bytes = wl.T * wl.K * 4
@@ -315,7 +317,7 @@ def main():
     alg = algorithmic(wl)
     copies_n = max(1, min(64, math.ceil(2 * L2_BYTES / max(alg["step_bytes"], 1)) + 1))
     default_steps = {"decode_b1": 20000, "decode_b64": 2000, "decode_b4_long": 5000, "prefill_16k": 10,
-                     "decode_b64_mx": 2000, "decode_b4_long_mx": 5000}
+                     "decode_b64_mx": 2000, "decode_b4_long_mx": 5000, "decode_b4_long_t128": 5000}
     steps = args.steps or default_steps[args.workload]
     warmup = max(3, args.warmup)
 

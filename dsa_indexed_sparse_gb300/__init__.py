@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libdsa.so")
 DSA_OK = 0
 STATUS_NAMES = {0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED", 3: "DSA_ERR_WORKSPACE",
                 4: "DSA_ERR_CUDA", 5: "DSA_ERR_TIMEOUT", 6: "DSA_ERR_DEVICE_CHECK"}
-DSA_F32, DSA_BF16, DSA_E4M3, DSA_MXFP8_E4M3 = 0, 1, 2, 3
+DSA_F32, DSA_BF16, DSA_E4M3, DSA_MXFP8_E4M3, DSA_E4M3_T128 = 0, 1, 2, 3, 4
 
 EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_plan",
             "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn_workspace_size",

@@ -117,6 +117,12 @@ dsa_status_t check_mla_shape(const dsa_mla_desc_t* m, int32_t K, dsa::MlaArgs* a
       kind = dsa::MlaKind::kFP8Row;
       min_row = 656;
       break;
+    case DSA_E4M3_T128:
+      if (m->d_latent != 512 || m->d_rope != 64)
+        return fail(DSA_ERR_UNSUPPORTED, "FP8 latent rows are defined for 512 + 64 dims only");
+      kind = dsa::MlaKind::kFP8Tile;
+      min_row = 656;
+      break;
     default: return fail(DSA_ERR_UNSUPPORTED, "unknown MLA cache dtype");
   }
   if (m->row_bytes < min_row) return fail(DSA_ERR_INVALID_ARG, "row_bytes smaller than one row");
@@ -408,6 +414,8 @@ dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_de
     dsa_status_t st = check_seq(seq, &s);
     if (st != DSA_OK) return st;
     if ((st = check_mla_shape(mla, 1, &a)) != DSA_OK) return st;
+    if (a.kind == dsa::MlaKind::kFP8Tile)
+      return fail(DSA_ERR_UNSUPPORTED, "latent append writes bf16, fp32 or per-token FP8 rows");
     if (a.kind != dsa::MlaKind::kFP8Row) {
       const int64_t row_in = static_cast<int64_t>(a.d_latent + a.d_rope) * (a.kind == dsa::MlaKind::kF32 ? 4 : 2);
       if (row_in % 16 != 0 || a.row_bytes % 16 != 0)

@@ -49,7 +49,9 @@ __device__ __forceinline__ float load_elem(MlaKind kind, const uint8_t* row, int
     case MlaKind::kBF16:
       return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row)[d]);
     default: {  // 656-byte FP8 row
-      if (d < 512) return e4m3_to_float(row[d]) * *reinterpret_cast<const float*>(row + 512);
+      // per-token scale at byte 512, or (per-128-tile rows) scale d / 128 at 512 + 4 (d / 128)
+      const int si = kind == MlaKind::kFP8Tile ? d / 128 : 0;
+      if (d < 512) return e4m3_to_float(row[d]) * reinterpret_cast<const float*>(row + 512)[si];
       return bf16_bits_to_float(reinterpret_cast<const uint16_t*>(row + 528)[d - 512]);
     }
   }
@@ -273,7 +275,9 @@ __device__ __forceinline__ void t48_issue_s(uint32_t tmem, uint64_t dq0, uint64_
   }
 }
 
-template <bool kFp8>
+// kTile: FP8 rows with one power-of-two scale per 128 latent dims, widened to
+// bf16 as code * scale by the producers (exact); the rest runs the bf16 plan.
+template <bool kFp8, bool kTile = false>
 __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams p) {
   using C = T48<kFp8>;
   constexpr int S = C::kStages;
@@ -425,17 +429,27 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       for (int rr = 0; rr < kRows; ++rr) rows[rr] = __shfl_sync(0xffffffffu, static_cast<int32_t>(my_row), rr);
       // FP8 rows: the codes (16 per lane and row) and the row scales are loaded
       // into registers while the stage may still be busy
-      uint4 raw[kFp8 ? kRows : 1];
+      uint4 raw[(kFp8 || kTile) ? kRows : 1];
+      float tsc[kTile ? kRows : 1];   // per-128-tile rows: the scale of this lane's tile (lane / 8)
       float my_scale = 0.f;
-      if constexpr (kFp8) {
+      if constexpr (kFp8 || kTile) {
 #pragma unroll
         for (int rr = 0; rr < kRows; ++rr)
           raw[rr] = rows[rr] >= 0 ? ld_global_nc_v4(kv + static_cast<int64_t>(rows[rr]) * p.a.row_bytes + lane * 16)
                                   : make_uint4(0u, 0u, 0u, 0u);
+      }
+      if constexpr (kFp8) {
         if (my_row >= 0) my_scale = __ldg(reinterpret_cast<const float*>(kv + my_row * p.a.row_bytes + kDv));
       }
+      if constexpr (kTile) {
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr)
+          tsc[rr] = rows[rr] >= 0 ? __ldg(reinterpret_cast<const float*>(kv + static_cast<int64_t>(rows[rr]) *
+                                                                                   p.a.row_bytes + kDv) + (lane >> 3))
+                                  : 0.f;
+      }
       if (j >= S) {
-        if constexpr (!kFp8) {
+        if constexpr (!kFp8 && !kTile) {
           // the stage is still busy: have L2 fetch this warp's rows (9 lines of 128 B each) meanwhile
 #pragma unroll
           for (int k = 0; k < (kRows * 9 + 31) / 32; ++k) {
@@ -449,7 +463,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       }
       if (lane == 0) mask16[st * C::kProducers + pw] = static_cast<uint16_t>(bits);
       if (kFp8 && lane < kRows) row_scale[st * kBR48 + pw * kRows + lane] = my_scale;
-      if constexpr (!kFp8) {
+      if constexpr (!kFp8 && !kTile) {
 #pragma unroll
         for (int rr = 0; rr < kRows; ++rr) {
           const int r = pw * kRows + rr;                       // row within the tile
@@ -492,13 +506,14 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
               st_shared_v4(dst, 0u, 0u, 0u, 0u);
           }
           const uint32_t w[4] = {raw[rr].x, raw[rr].y, raw[rr].z, raw[rr].w};
+          const float sc = kTile ? tsc[rr] : 1.f;   // per-token rows: the scale goes to the logits and P
           uint32_t o[8];
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const float2 lo = e4m3x2_to_float2(static_cast<uint16_t>(w[k] & 0xFFFFu));
             const float2 hi = e4m3x2_to_float2(static_cast<uint16_t>(w[k] >> 16));
-            o[2 * k] = pack_bf16x2(lo.x, lo.y);
-            o[2 * k + 1] = pack_bf16x2(hi.x, hi.y);
+            o[2 * k] = pack_bf16x2(lo.x * sc, lo.y * sc);
+            o[2 * k + 1] = pack_bf16x2(hi.x * sc, hi.y * sc);
           }
           // chunk ch = 2*lane + e of row r: atom ch >> 3, swizzled position (ch & 7) ^ (r & 7)
 #pragma unroll
@@ -814,7 +829,7 @@ bool tc_supported(const SeqArgs& seq, const MlaArgs& a) {
   if (a.H != kH || a.d_latent != kDv || a.d_rope != kDqk - kDv) return false;
   if (a.kind == MlaKind::kF32) return false;
   if (a.kind == MlaKind::kBF16 && a.row_bytes % 16 != 0) return false;
-  if (a.kind == MlaKind::kFP8Row && a.row_bytes % 16 != 0) return false;
+  if ((a.kind == MlaKind::kFP8Row || a.kind == MlaKind::kFP8Tile) && a.row_bytes % 16 != 0) return false;
   if (reinterpret_cast<uintptr_t>(a.kv) % 16 || reinterpret_cast<uintptr_t>(a.q) % 16 ||
       reinterpret_cast<uintptr_t>(a.out) % 16)
     return false;
@@ -856,6 +871,7 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
   }
   if (tc_supported(seq, a)) {
     const bool fp8 = a.kind == MlaKind::kFP8Row;
+    const bool tile = a.kind == MlaKind::kFP8Tile;
     const int tile_rows = kBR48;
     int split = choose_split(seq, a, env.num_sms);
     if (split > 1 && (workspace == nullptr || ws_bytes < attn_workspace_bytes(seq, a, env.num_sms)))
@@ -876,12 +892,19 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
       if (attr_err == cudaSuccess)
         attr_err = cudaFuncSetAttribute(attn_tc48_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         kT48SmemBytes);
+      if (attr_err == cudaSuccess)
+        attr_err = cudaFuncSetAttribute(attn_tc48_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kT48SmemBytes);
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = seq.T * split * 2;
     if (fp8) {
       const cudaError_t le =
           launch_kernel(attn_tc48_kernel<true>, dim3(grid), dim3(kT48Threads), kT48SmemBytes, env.stream, true, 1, p);
+      if (le != cudaSuccess) return le;
+    } else if (tile) {
+      const cudaError_t le = launch_kernel(attn_tc48_kernel<false, true>, dim3(grid), dim3(kT48Threads), kT48SmemBytes,
+                                           env.stream, true, 1, p);
       if (le != cudaSuccess) return le;
     } else {
       const cudaError_t le =
@@ -891,7 +914,8 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     char buf[128];
-    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8x48" : "bf16x48", split, grid);
+    snprintf(buf, sizeof(buf), "attn_tc<%s>[split=%d,grid=%d]", fp8 ? "fp8x48" : (tile ? "fp8t128x48" : "bf16x48"),
+             split, grid);
     *plan += buf;
     if (split > 1) {
       e = launch_kernel(attn_combine_kernel, dim3(seq.T, kH / kCombineHeads), dim3(32 * kCombineHeads), 0, env.stream,

@@ -34,7 +34,7 @@ struct IndexerArgs {
   int64_t ld;
 };
 
-enum class MlaKind { kF32 = 0, kBF16 = 1, kFP8Row = 2 };
+enum class MlaKind { kF32 = 0, kBF16 = 1, kFP8Row = 2, kFP8Tile = 3 };   // kFP8Tile: scale per 128 latent dims
 
 struct MlaArgs {
   int32_t H, d_latent, d_rope;

@@ -172,11 +172,13 @@ def _quant_blocks_mx(x: torch.Tensor, block: int = MX_BLOCK):
             (sexp + 127).to(torch.uint8).squeeze(-1).numpy())
 
 
-def _spread_blocks(g: torch.Generator, x: torch.Tensor, spread: int, block: int = MX_BLOCK):
+def _spread_blocks(g: torch.Generator, x: torch.Tensor, spread: int, block: int = MX_BLOCK, top: int = None):
     """Multiplies every `block`-element block of the last axis by 2**r, r uniform
-    in [-spread, spread] (seeded), so that blocks of one vector differ in range."""
+    in [-spread, top] (top = spread unless given; seeded), so that blocks of one
+    vector differ in range."""
     shp = x.shape
-    r = torch.randint(-spread, spread + 1, (*shp[:-1], shp[-1] // block, 1), generator=g)
+    top = spread if top is None else top
+    r = torch.randint(-spread, top + 1, (*shp[:-1], shp[-1] // block, 1), generator=g)
     x.view(*shp[:-1], shp[-1] // block, block).mul_(torch.pow(2.0, r.to(torch.float32)))
 
 
@@ -283,7 +285,7 @@ def make(name_or_spec, seed: int = 0, **over) -> Workload:
         # power of two (the shared-exponent rule of the MX formats on 128-blocks)
         assert sp.d_latent == 512 and sp.d_rope == 64
         lat = kv_f[:, :sp.d_latent].contiguous()
-        _spread_blocks(g, lat, 2, block=128)
+        _spread_blocks(g, lat, 2, block=128, top=0)   # tiles shrunk by 2**{0,-1,-2}
         codes, exps = _quant_blocks_mx(lat, block=128)
         scales = np.ldexp(np.float32(1.0), exps.astype(np.int32) - 127).astype("<f4")   # [rows, 4]
         kv = np.zeros((cache_rows, FP8_ROW_BYTES), dtype=np.uint8)

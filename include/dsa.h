@@ -60,9 +60,11 @@ typedef enum dsa_dtype {
   DSA_F32 = 0,
   DSA_BF16 = 1,
   DSA_E4M3 = 2,              /* OCP FP8 E4M3 codes (bias 7, max 448, no inf)      */
-  DSA_MXFP8_E4M3 = 3         /* OCP MXFP8: E4M3 codes, one E8M0 scale byte         */
+  DSA_MXFP8_E4M3 = 3,        /* OCP MXFP8: E4M3 codes, one E8M0 scale byte         */
                              /* 2**(e - 127) per 32 consecutive elements (indexer  */
                              /* only)                                              */
+  DSA_E4M3_T128 = 4          /* MLA cache only: 656-byte FP8 rows with one fp32    */
+                             /* scale per 128 latent dims (layout below)           */
 } dsa_dtype_t;
 
 typedef void* dsa_stream_t;  /* cudaStream_t */
@@ -125,6 +127,14 @@ typedef struct dsa_mla_desc {
                              /*  DSA_E4M3: 656-byte row (d_latent 512, d_rope 64): */
                              /*   [0,512) e4m3 latent codes, [512,516) fp32 scale, */
                              /*   [516,528) reserved, [528,656) 64 bf16 rope       */
+                             /*  DSA_E4M3_T128: the same 656-byte row with four    */
+                             /*   fp32 scales at [512,528), scale i for latent     */
+                             /*   dims [128 i, 128 i + 128) ("per-token-tile-128", */
+                             /*   "Large Language Model Inference Acceleration in  */
+                             /*   Practice" section 4).  The tensor-core path      */
+                             /*   widens code * scale to bf16: exact when every    */
+                             /*   scale is a power of two (as the cache writer     */
+                             /*   produces them), rounded to bf16 otherwise.       */
                              /*  DSA_F32 : row = d_latent+d_rope fp32 values       */
   const void* q;             /* device [T, H, d_latent+d_rope]: bf16, or fp32 when */
                              /* dtype == DSA_F32                                   */

@@ -68,6 +68,19 @@ def test_host_validation_rejects_bad_arguments(dsa):
     # decode step without a workspace
     assert lib.dsa_decode_step(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), 32, 16, None, None,
                                None, 0, None) == 3
+    # MXFP8 index keys: D_I a multiple of 32, both scale arrays required
+    x = dsa.IndexerDesc(H_I=4, D_I=48, dtype=dsa.DSA_MXFP8_E4M3, q=16, q_scale=16, w=16, k_cache=16, k_scale=16)
+    assert lib.dsa_indexer_scores(ctypes.byref(s), ctypes.byref(x), 16, 1024, None) == 2
+    assert "multiple of 32" in dsa.last_error()
+    x = dsa.IndexerDesc(H_I=4, D_I=64, dtype=dsa.DSA_MXFP8_E4M3, q=16, q_scale=None, w=16, k_cache=16, k_scale=16)
+    assert lib.dsa_indexer_scores(ctypes.byref(s), ctypes.byref(x), 16, 1024, None) == 1
+    # per-128-tile FP8 rows: 512 + 64 dims only; the latent writer does not produce them
+    m = dsa.MlaDesc(H=4, d_latent=64, d_rope=16, dtype=dsa.DSA_E4M3_T128, q=16, kv_cache=16, row_bytes=656,
+                    softmax_scale=0.1)
+    assert lib.dsa_sparse_mla_attn(ctypes.byref(s), ctypes.byref(m), 16, 32, 16, None, None, 0, None) == 2
+    m = dsa.MlaDesc(H=128, d_latent=512, d_rope=64, dtype=dsa.DSA_E4M3_T128, q=16, kv_cache=16, row_bytes=656,
+                    softmax_scale=0.1)
+    assert lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), 16, 16, None) == 2
 
 
 def test_product_package_does_not_touch_the_oracle():

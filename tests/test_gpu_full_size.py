@@ -38,6 +38,7 @@ SIZES = {
     "decode_b4_long": 0,
     "prefill_16k": 3,
     "decode_b4_long_mx": 0,   # MXFP8 index keys at the long-context size
+    "decode_b4_long_t128": 0,  # FP8 latent rows scaled per 128 dims, long context
 }
 
 

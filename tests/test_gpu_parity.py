@@ -41,6 +41,10 @@ CASES = {
     "mx_qlen4": ("decode_b1", dict(ctx=[900], q_len=4, K=128, idx_dtype="mx_e4m3")),
     "mx_prefill_300": ("prefill_16k", dict(ctx=[300], q_len=300, K=64, idx_dtype="mx_e4m3")),
     "mx_fp8_b2": ("decode_b4_long", dict(ctx=[3000, 4100], B=2, K=2048, idx_dtype="mx_e4m3")),
+    # FP8 latent rows with one power-of-two scale per 128 latent dims (the tiles
+    # of one row scaled by 2**{0,-1,-2})
+    "t128_b2": ("decode_b4_long", dict(ctx=[3000, 4100], B=2, K=2048, mla_dtype="e4m3_t128")),
+    "t128_prefill_400": ("prefill_16k", dict(ctx=[400], q_len=400, K=64, mla_dtype="e4m3_t128")),
 }
 
 
