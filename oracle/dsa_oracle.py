@@ -328,28 +328,35 @@ def decode_step(wl, ts=None):
 # ---------------------------------------------------------------------------
 
 
-def index_cache_append(block_table, page_size, q_seq, q_pos, k_new, k_cache, k_scale):
+def index_cache_append(block_table, page_size, q_seq, q_pos, k_new, k_cache, k_scale, mx: bool = False):
     """Quantise k_new[t] (float32 [T, D]) and store it at the cache row of
     position q_pos[t] of sequence q_seq[t].  Returns updated copies of k_cache
-    (uint8 [rows, D]) and k_scale (float32 [rows])."""
+    (uint8 [rows, D]) and k_scale: float32 [rows] (one scale per key), or with
+    mx, uint8 [rows, D / 32] E8M0 bytes (quantize_mx_e4m3)."""
     k_cache = np.array(k_cache, dtype=np.uint8, copy=True)
-    k_scale = np.array(k_scale, dtype=np.float32, copy=True)
+    k_scale = np.array(k_scale, dtype=np.uint8 if mx else np.float32, copy=True)
     for t in range(len(q_pos)):
         row = int(physical_rows(block_table[int(q_seq[t])], page_size, np.array([q_pos[t]]))[0])
-        codes, scale = quantize_e4m3_row(k_new[t])
+        if mx:
+            codes, scale = quantize_mx_e4m3(k_new[t])
+        else:
+            codes, scale = quantize_e4m3_row(k_new[t])
         k_cache[row] = codes
         k_scale[row] = scale
     return k_cache, k_scale
 
 
 def latent_cache_append(block_table, page_size, q_seq, q_pos, kv_new_bits, cache, fp8_rows: bool,
-                        d_latent: int = 512, d_rope: int = 64):
+                        d_latent: int = 512, d_rope: int = 64, tile128: bool = False):
     """Store the new latent rows (bfloat16 bit patterns, uint16 [T, d_latent +
     d_rope]) at the cache rows of their positions.  `cache` is uint8 [rows,
     row_bytes].  bf16 cache: the row's bytes are the input's.  FP8 cache (656-byte
     rows): [0, 512) e4m3 codes of the latent part quantised as one vector,
     [512, 516) its float32 scale, [516, 528) zero, [528, 656) the rope part's bf16
-    bytes.  Returns an updated copy of the cache."""
+    bytes.  With tile128 the four 128-value tiles of the latent part are
+    quantised separately by the MX shared-exponent rule (quantize_mx_e4m3 with
+    128-element blocks: power-of-two scales) and their four float32 scales fill
+    [512, 528).  Returns an updated copy of the cache."""
     cache = np.array(cache, dtype=np.uint8, copy=True)
     bits = np.asarray(kv_new_bits, dtype=np.uint16)
     for t in range(len(q_pos)):
@@ -359,10 +366,17 @@ def latent_cache_append(block_table, page_size, q_seq, q_pos, kv_new_bits, cache
             cache[row, :len(b)] = np.frombuffer(b, dtype=np.uint8)
             continue
         latent = decode_bf16(bits[t, :d_latent]).astype(np.float32)
-        codes, scale = quantize_e4m3_row(latent)
-        cache[row, :d_latent] = codes
-        cache[row, d_latent:d_latent + 4] = np.frombuffer(np.float32(scale).astype("<f4").tobytes(), dtype=np.uint8)
-        cache[row, d_latent + 4:d_latent + 16] = 0
+        if tile128:
+            codes, exps = quantize_mx_e4m3(latent, block=128)
+            scales = np.ldexp(np.float32(1.0), exps.astype(np.int32) - 127).astype("<f4")
+            cache[row, :d_latent] = codes
+            cache[row, d_latent:d_latent + 16] = np.frombuffer(scales.tobytes(), dtype=np.uint8)
+        else:
+            codes, scale = quantize_e4m3_row(latent)
+            cache[row, :d_latent] = codes
+            cache[row, d_latent:d_latent + 4] = np.frombuffer(np.float32(scale).astype("<f4").tobytes(),
+                                                              dtype=np.uint8)
+            cache[row, d_latent + 4:d_latent + 16] = 0
         rope = bits[t, d_latent:d_latent + d_rope].astype("<u2").tobytes()
         cache[row, d_latent + 16:d_latent + 16 + len(rope)] = np.frombuffer(rope, dtype=np.uint8)
     return cache

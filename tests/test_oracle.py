@@ -513,3 +513,33 @@ def test_fp8_tile128_latent_row_decode():
     # exact in bf16: widening code * scale to bf16 loses nothing
     b = torch.from_numpy(lat).to(torch.bfloat16).double().numpy()
     assert np.array_equal(b, lat)
+
+
+def test_cache_append_oracle_mx_keys_and_tile128_rows():
+    """The writers' variants store exactly the oracle quantiser's output at the
+    token's row and leave every other row untouched."""
+    rng = np.random.default_rng(9)
+    bt = np.array([[3, 1, 0, 2]], dtype=np.int32)
+    k_new = (rng.normal(0, 1, (2, 128)) * np.repeat(np.exp2(rng.integers(-5, 5, (2, 4))), 32, axis=1)).astype(np.float32)
+    kc0 = rng.integers(0, 256, (256, 128)).astype(np.uint8)
+    ks0 = rng.integers(0, 256, (256, 4)).astype(np.uint8)
+    kc, ks = O.index_cache_append(bt, 64, np.array([0, 0]), np.array([5, 130]), k_new, kc0, ks0, mx=True)
+    for t, pos in enumerate([5, 130]):
+        row = int(bt[0, pos // 64]) * 64 + pos % 64
+        c, e = O.quantize_mx_e4m3(k_new[t])
+        assert np.array_equal(kc[row], c) and np.array_equal(ks[row], e)
+        kc0[row], ks0[row] = kc[row], ks[row]
+    assert np.array_equal(kc, kc0) and np.array_equal(ks, ks0)
+    x = torch.from_numpy(rng.normal(0, 1, (1, 576)).astype(np.float32)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    cache0 = rng.integers(0, 256, (128, 656)).astype(np.uint8)
+    out = O.latent_cache_append(bt, 64, np.array([0]), np.array([70]), bits, cache0, fp8_rows=True, tile128=True)
+    row = int(bt[0, 1]) * 64 + 6
+    lat = x.float().numpy()[0, :512]
+    c, e = O.quantize_mx_e4m3(lat, block=128)
+    assert np.array_equal(out[row, :512], c)
+    assert np.array_equal(out[row, 512:528].view("<f4"), np.ldexp(np.float32(1), e.astype(np.int32) - 127))
+    assert np.array_equal(out[row, 528:].view("<u2"), bits[0, 512:])
+    others = np.ones(128, bool)
+    others[row] = False
+    assert np.array_equal(out[others], cache0[others])
