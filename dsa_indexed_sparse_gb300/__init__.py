@@ -25,7 +25,8 @@ DSA_F32, DSA_BF16, DSA_E4M3, DSA_MXFP8_E4M3, DSA_E4M3_T128 = 0, 1, 2, 3, 4
 EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_plan",
             "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn_workspace_size",
             "dsa_sparse_mla_attn", "dsa_decode_workspace_size", "dsa_decode_step",
-            "dsa_decode_step_static_ws", "dsa_index_cache_append", "dsa_latent_cache_append",
+            "dsa_decode_step_static_ws", "dsa_index_cache_append", "dsa_index_cache_append_mx",
+            "dsa_latent_cache_append",
             "dsa_check_status")
 STATIC_WORKSPACE_BYTES = 32 << 20   # DSA_STATIC_WORKSPACE_BYTES
 
@@ -73,6 +74,7 @@ def _load() -> ctypes.CDLL:
         "dsa_decode_step": (C, [P, P, P, ctypes.c_int32, P, P, P, P, ctypes.c_size_t, P]),
         "dsa_decode_step_static_ws": (C, [P, P, P, ctypes.c_int32, P, P, P, P]),
         "dsa_index_cache_append": (C, [P, ctypes.c_int32, C, P, P, P, P]),
+        "dsa_index_cache_append_mx": (C, [P, ctypes.c_int32, C, P, P, P, P]),
         "dsa_latent_cache_append": (C, [P, P, P, P, P]),
         "dsa_check_status": (C, [P]),
     }
@@ -253,12 +255,15 @@ def decode_step_static_ws(seq: Seq, idx: Indexer, mla: Mla, K: int, out: torch.T
 
 
 def index_cache_append(seq: Seq, k_new: torch.Tensor, k_cache: torch.Tensor, k_scale: torch.Tensor,
-                       stream=None) -> None:
+                       stream=None, mx: bool = False) -> None:
     """Quantises the new tokens' index keys k_new [T, D_I] (fp32 or bf16) to e4m3
-    + per-token scale and writes them at their positions' cache rows."""
+    + per-token fp32 scale (k_scale [cache_rows]), or with mx to MXFP8 (k_scale
+    uint8 [cache_rows, D_I / 32] E8M0 bytes), and writes them at their
+    positions' cache rows."""
     s = seq.desc()
-    _check(_lib.dsa_index_cache_append(ctypes.byref(s), k_new.shape[1], _dtype_code(k_new), _ptr(k_new),
-                                       _ptr(k_cache), _ptr(k_scale), _stream(stream)))
+    fn = _lib.dsa_index_cache_append_mx if mx else _lib.dsa_index_cache_append
+    _check(fn(ctypes.byref(s), k_new.shape[1], _dtype_code(k_new), _ptr(k_new), _ptr(k_cache), _ptr(k_scale),
+              _stream(stream)))
 
 
 def latent_cache_append(seq: Seq, mla: Mla, kv_new: torch.Tensor, stream=None) -> None:

@@ -406,6 +406,32 @@ dsa_status_t dsa_index_cache_append(const dsa_seq_desc_t* seq, int32_t D_I, dsa_
   }
 }
 
+dsa_status_t dsa_index_cache_append_mx(const dsa_seq_desc_t* seq, int32_t D_I, dsa_dtype_t src_dtype,
+                                       const void* k_new, uint8_t* k_cache, uint8_t* k_exp, dsa_stream_t stream) {
+  try {
+    dsa::SeqArgs s;
+    dsa_status_t st = check_seq(seq, &s);
+    if (st != DSA_OK) return st;
+    if (D_I < 32 || D_I > 1024 || D_I % 32 != 0)
+      return fail(DSA_ERR_UNSUPPORTED, "MXFP8 index-key append needs D_I in [32, 1024], a multiple of 32");
+    if (src_dtype != DSA_F32 && src_dtype != DSA_BF16)
+      return fail(DSA_ERR_UNSUPPORTED, "new index keys must be DSA_F32 or DSA_BF16");
+    if (s.T > 0 && (!k_new || !k_cache || !k_exp))
+      return fail(DSA_ERR_INVALID_ARG, "k_new, k_cache and k_exp must be non-NULL");
+    if (!aligned16(k_new) || !aligned16(k_cache) || !aligned16(k_exp))
+      return fail(DSA_ERR_INVALID_ARG, "k_new, k_cache and k_exp must be 16-byte aligned");
+    dsa::LaunchEnv env;
+    if ((st = make_env(stream, &env)) != DSA_OK) return st;
+    std::string plan;
+    cudaError_t e = dsa::launch_index_append_mx(s, D_I, src_dtype == DSA_BF16, k_new, k_cache, k_exp, env, &plan);
+    if (e != cudaSuccess) return cuda_fail(e, "index-key append launch");
+    g_last_plan = plan;
+    return DSA_OK;
+  } catch (...) {
+    return fail(DSA_ERR_CUDA, "unexpected host exception");
+  }
+}
+
 dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, const void* kv_new,
                                      void* kv_cache, dsa_stream_t stream) {
   try {
@@ -414,9 +440,7 @@ dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_de
     dsa_status_t st = check_seq(seq, &s);
     if (st != DSA_OK) return st;
     if ((st = check_mla_shape(mla, 1, &a)) != DSA_OK) return st;
-    if (a.kind == dsa::MlaKind::kFP8Tile)
-      return fail(DSA_ERR_UNSUPPORTED, "latent append writes bf16, fp32 or per-token FP8 rows");
-    if (a.kind != dsa::MlaKind::kFP8Row) {
+    if (a.kind != dsa::MlaKind::kFP8Row && a.kind != dsa::MlaKind::kFP8Tile) {
       const int64_t row_in = static_cast<int64_t>(a.d_latent + a.d_rope) * (a.kind == dsa::MlaKind::kF32 ? 4 : 2);
       if (row_in % 16 != 0 || a.row_bytes % 16 != 0)
         return fail(DSA_ERR_UNSUPPORTED, "latent append copies 16-byte vectors: row and row_bytes must be multiples of 16");

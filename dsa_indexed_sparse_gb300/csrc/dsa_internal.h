@@ -109,6 +109,8 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 // Cache writers (the new tokens' index keys / latent rows into the paged caches).
 cudaError_t launch_index_append(const SeqArgs& seq, int32_t D, bool bf16_in, const void* k_new, uint8_t* k_cache,
                                 float* k_scale, const LaunchEnv& env, std::string* plan);
+cudaError_t launch_index_append_mx(const SeqArgs& seq, int32_t D, bool bf16_in, const void* k_new, uint8_t* k_cache,
+                                   uint8_t* k_exp, const LaunchEnv& env, std::string* plan);
 cudaError_t launch_latent_append(const SeqArgs& seq, const MlaArgs& a, const void* kv_new, void* kv_cache,
                                  const LaunchEnv& env, std::string* plan);
 

@@ -233,6 +233,16 @@ dsa_status_t dsa_decode_step_static_ws(const dsa_seq_desc_t* seq, const dsa_inde
  *   the formats dsa_indexer_scores reads.  4 <= D_I <= 1024, D_I % 4 == 0. */
 dsa_status_t dsa_index_cache_append(const dsa_seq_desc_t* seq, int32_t D_I, dsa_dtype_t src_dtype,
                                     const void* k_new, uint8_t* k_cache, float* k_scale, dsa_stream_t stream);
+/* MXFP8 index keys (the DSA_MXFP8_E4M3 format dsa_indexer_scores reads): as
+ *   above, but every block of 32 consecutive values b gets its own E8M0 byte
+ *   k_exp[row, b] = x_b + 127, x_b = floor(log2 max_i |k_new[t, 32 b + i]|) - 8
+ *   (8 is the exponent of E4M3's largest normal, 448 = 1.75 * 2**8; -127 for an
+ *   all-zero block; clamped to [-127, 127]), and code_i = the E4M3 value nearest
+ *   to k_new[t, i] * 2**-x_b (an exact quotient), ties to even, saturated to
+ *   +-448.  k_exp: device uint8 [cache_rows, D_I / 32].  32 <= D_I <= 1024,
+ *   D_I % 32 == 0; k_new, k_cache and k_exp 16-byte aligned. */
+dsa_status_t dsa_index_cache_append_mx(const dsa_seq_desc_t* seq, int32_t D_I, dsa_dtype_t src_dtype,
+                                       const void* k_new, uint8_t* k_cache, uint8_t* k_exp, dsa_stream_t stream);
 /* Latent rows: kv_new device [T, d_latent + d_rope], bf16 (fp32 when
  *   mla->dtype == DSA_F32); mla gives d_latent, d_rope, the cache dtype and
  *   row_bytes (its q and kv_cache fields are not used); the rows are written to
@@ -240,7 +250,12 @@ dsa_status_t dsa_index_cache_append(const dsa_seq_desc_t* seq, int32_t D_I, dsa_
  *    DSA_BF16 / DSA_F32: the row copied (its byte size and row_bytes multiples of 16);
  *    DSA_E4M3 (656-byte rows, 512 + 64): the 512 latent values quantised as one
  *      vector by the rule above into [0,512), the fp32 scale at [512,516), zero
- *      bytes at [516,528), the 64 bf16 rope values copied to [528,656). */
+ *      bytes at [516,528), the 64 bf16 rope values copied to [528,656);
+ *    DSA_E4M3_T128 (656-byte rows, 512 + 64): each 128-value tile i of the latent
+ *      part quantised with the exponent rule of dsa_index_cache_append_mx on
+ *      128-value blocks, its scale 2**x_i stored as fp32 at [512 + 4 i, 516 + 4 i)
+ *      (a power of two, so the attention kernel widens code * scale to bf16
+ *      exactly), the rope copied to [528,656). */
 dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, const void* kv_new,
                                      void* kv_cache, dsa_stream_t stream);
 

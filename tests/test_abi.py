@@ -80,7 +80,8 @@ def test_host_validation_rejects_bad_arguments(dsa):
     assert lib.dsa_sparse_mla_attn(ctypes.byref(s), ctypes.byref(m), 16, 32, 16, None, None, 0, None) == 2
     m = dsa.MlaDesc(H=128, d_latent=512, d_rope=64, dtype=dsa.DSA_E4M3_T128, q=16, kv_cache=16, row_bytes=656,
                     softmax_scale=0.1)
-    assert lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), 16, 16, None) == 2
+    # (the tile-128 writer exists; D_I rules for the MXFP8 key writer)
+    assert lib.dsa_index_cache_append_mx(ctypes.byref(s), 48, dsa.DSA_F32, 16, 16, 16, None) == 2
 
 
 def test_product_package_does_not_touch_the_oracle():

@@ -128,3 +128,49 @@ def test_append_flags_bad_position(dev):
     assert e.value.status == 6 and "bad_q_pos" in str(e.value)
     # the other tokens were written
     assert int((ks != 0).sum()) == wl.T - 1
+
+
+@pytest.mark.parametrize("src", ["f32", "bf16"])
+def test_index_cache_append_mx_bit_exact(dev, src):
+    wl = _layout(41)
+    rng = np.random.default_rng(42)
+    D = wl.D_I
+    k_new = (rng.normal(0, 1, (wl.T, D)) * np.repeat(np.exp2(rng.integers(-6, 6, (wl.T, D // 32))), 32, axis=1)
+             ).astype(np.float32)
+    k_new[1] = 0.0                               # all-zero blocks: exponent byte 0, codes 0
+    k_new[2, :32] = 0.0
+    k_new[3, 32:39] = [448.0, -1e-6, 3e-3, -2.5, 0.0, -0.0, 1e4]
+    t_new = torch.from_numpy(k_new)
+    if src == "bf16":
+        t_new = t_new.to(torch.bfloat16)
+        k_new = t_new.float().numpy()
+    kc0 = rng.integers(0, 256, (wl.cache_rows, D)).astype(np.uint8)
+    ke0 = rng.integers(0, 256, (wl.cache_rows, D // 32)).astype(np.uint8)
+    kc = torch.from_numpy(kc0.copy()).to(dev)
+    ke = torch.from_numpy(ke0.copy()).to(dev)
+    dsa.index_cache_append(_seq(wl, dev), t_new.to(dev), kc, ke, mx=True)
+    assert dsa.last_plan().startswith("index_append_mx")
+    dsa.check_status()
+    o_kc, o_ke = O.index_cache_append(wl.block_table, wl.page_size, wl.q_seq, wl.q_pos, k_new, kc0, ke0, mx=True)
+    assert np.array_equal(kc.cpu().numpy(), o_kc)
+    assert np.array_equal(ke.cpu().numpy(), o_ke)
+
+
+def test_latent_cache_append_tile128_rows(dev):
+    wl = _layout(43)
+    rng = np.random.default_rng(44)
+    x = rng.normal(0, 1, (wl.T, 576)).astype(np.float32)
+    x[:, :512] *= np.repeat(np.exp2(rng.integers(-3, 3, (wl.T, 4))), 128, axis=1)
+    x[0, 128:256] = 0.0                          # one all-zero tile
+    t_new = torch.from_numpy(x).to(torch.bfloat16)
+    bits = t_new.view(torch.int16).numpy().view(np.uint16)
+    q = torch.zeros((1, 128, 576), dtype=torch.bfloat16, device=dev)
+    cache0 = rng.integers(0, 256, (wl.cache_rows, 656)).astype(np.uint8)
+    cache = torch.from_numpy(cache0.copy()).to(dev)
+    mla = dsa.Mla(q=q, kv_cache=cache, d_latent=512, d_rope=64, softmax_scale=1.0, dtype=dsa.DSA_E4M3_T128)
+    dsa.latent_cache_append(_seq(wl, dev), mla, t_new.to(dev))
+    assert dsa.last_plan() == "latent_append<fp8_tile128>"
+    dsa.check_status()
+    want = O.latent_cache_append(wl.block_table, wl.page_size, wl.q_seq, wl.q_pos, bits, cache0, fp8_rows=True,
+                                 tile128=True)
+    assert np.array_equal(cache.cpu().numpy(), want)
