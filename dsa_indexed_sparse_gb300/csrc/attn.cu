@@ -177,18 +177,22 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
 // ---------------------------------------------------------------------------
 // 48-row tiles: three stages for bf16 rows, two for FP8 rows.
 //
-// Producers (warps 0-11): a group of warps owns one stage and loads every
-// S-th tile (bf16 rows: three groups of four warps, 12 rows per warp; a warp
-// issues cp.async copies at ~30 ns per instruction here, so the warps per tile
-// set how fast it lands).  Lanes resolve the rows (index -> page -> cache row)
-// as soon as the group's previous tile has landed and ask L2 to fetch them;
-// once the stage is free every lane copies its fixed 16-byte chunks of each row
-// with cp.async into the 128B-swizzled K-major tile; rows that select nothing
-// are zeroed.  (On this GPU a tile::gather4 TMA producer reached ~12 GB/s per
-// SM and cp.async gathers ~60 GB/s.)  FP8 rows: two groups of six warps, 8 rows
-// per warp; a lane loads 16 codes of each of its warp's rows into registers
-// before the stage is free, then widens them to bf16 into the tile; the rope
-// goes by cp.async.
+// Producers (warps 0-11), bf16 rows: all twelve warps load every tile, four rows
+// each (a warp issues cp.async copies at ~30 ns per instruction here, so the
+// warps per tile set how fast it lands).  Lanes resolve the rows (index -> page
+// -> cache row; the index is loaded one tile ahead) and, while the stage is
+// still busy, ask L2 to fetch them; once it is free every lane copies its fixed
+// 16-byte chunks of each row with cp.async into the 128B-swizzled K-major tile
+// and moves on to the next tile without waiting: the copies arrive on the
+// stage's barrier when they land (cp.async.mbarrier.arrive.noinc), so a warp
+// keeps up to three tiles in flight.  Rows that select nothing are zeroed.  (On
+// this GPU a tile::gather4 TMA producer reached ~12 GB/s per SM and cp.async
+// gathers ~60 GB/s.)  FP8 rows with per-128 tile scales share this plan; their
+// lanes load the codes into registers before the stage is free and widen them
+// into the tile.  FP8 rows with one scale per row: two groups of six warps, 8
+// rows per warp, each group owning one stage; a lane loads 16 codes of each of
+// its warp's rows into registers before the stage is free, then widens them to
+// bf16 into the tile; the rope goes by cp.async.
 //
 // MMA warps: warp 12 issues Q K^T_{j+1} (N = 48 rows) as soon as the softmax
 // has read S_j and tile j+1 has landed, so it runs during the softmax of tile
@@ -228,15 +232,24 @@ constexpr uint32_t kIdescS48 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, 
 template <bool kFp8>
 struct T48 {
   static constexpr int kStages = kFp8 ? 2 : 3;
-  static constexpr int kProducers = kFp8 ? 6 : 4;          // warps per stage group
+  // bf16 rows: the twelve producer warps all load every tile (four rows each) and
+  // run up to kStages tiles ahead, each lane's copies arriving on the stage's
+  // barrier as they land; FP8 rows: one group of six warps per stage, each warp
+  // converting its rows and waiting for its copies before it arrives
+  static constexpr int kGroups = kFp8 ? kStages : 1;
+  static constexpr bool kAsyncArrive = kGroups == 1;
+  static constexpr int kProducers = 12 / kGroups;          // warps per tile
   static constexpr int kRows = kBR48 / kProducers;         // tile rows per producer warp
+  // arrivals that complete a stage's barrier: one per warp (after its shared
+  // stores), plus one per lane when its copies land (asynchronous arrival)
+  static constexpr uint32_t kFullCount = kProducers * (kAsyncArrive ? 33 : 1);
   static constexpr int kQTmemDims = kFp8 ? 256 : 320;
   static constexpr int kQTmemSteps = kQTmemDims / 16;
   static constexpr int kQSmemAtoms = (kDqk - kQTmemDims) / 64;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQSmemAtoms * kH * 128;
   static constexpr int kOffMask = kOffKV + kStages * kTile48Bytes;     // uint16 [stages][producers]
-  static constexpr int kOffScale = kOffMask + 32;                       // float [stages][48] (FP8 rows)
+  static constexpr int kOffScale = kOffMask + 128;                      // float [stages][48] (FP8 rows)
   static constexpr int kOffBar = kOffScale + (kFp8 ? kStages * kBR48 * 4 : 0);
   // barriers: full[S], empty[S], sfull, sfree, pfull, pvdone, ofull
   static constexpr int kNumBars = 2 * kStages + 5;
@@ -250,8 +263,8 @@ struct T48 {
   static_assert(kColQ + kQTmemDims / 2 <= kColO, "TMEM plan");
   static_assert(kColP + kBR48 / 2 <= kColQ && kColS + kBR48 <= (kFp8 ? kColSr : kColP), "TMEM plan");
   static_assert(!kFp8 || kColSr + kBR48 <= kColP, "TMEM plan");
-  static_assert(kStages * kProducers * 2 <= 32 && kSlack >= 128, "shared memory budget");
-  static_assert(kStages * kProducers <= 12, "producer warps");
+  static_assert(kStages * kProducers * 2 <= 128 && kSlack >= 128, "shared memory budget");
+  static_assert(kGroups * kProducers == 12 && kProducers * kRows == kBR48, "producer warps");
 };
 
 // Q K^T of one 48-row tile (elected lane of the MMA warp).  FP8 rows: the 32
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], C::kProducers);
+      mbar_init(&full[i], C::kFullCount);
       mbar_init(&empty[i], 1);
     }
     mbar_init(sfull, 1);
@@ -388,9 +401,9 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     tc_fence_after();
   }
 
-  if (warp < C::kProducers * S) {
-    // ------------------------------------------------ producers: group g = warp / 4 loads tiles
-    // j = g mod S into stage g; warp w of the group copies tile rows [w*kRows, (w+1)*kRows)
+  if (warp < C::kProducers * C::kGroups) {
+    // ------------------------------------------------ producers: group g loads tiles j = g mod
+    // kGroups into stage j mod S; warp w of the group copies tile rows [w*kRows, (w+1)*kRows)
     grid_dep_wait();   // the selected indices come from the kernel before
     constexpr int kRows = C::kRows;
     const int grp = warp / C::kProducers, pw = warp % C::kProducers;
@@ -406,21 +419,24 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       dst_off[k] = static_cast<uint32_t>((ch >> 3) * kBR48 * 128);   // atom block
       src_off[k] = static_cast<uint32_t>(ch * 16);
     }
-    const int st = grp;
-    const uint32_t stage = smem_u32(sm + C::kOffKV + st * kTile48Bytes);
-    for (int j = grp; j < ntiles; j += S) {
+    // the selected position of this lane's row of tile j (lanes < kRows), or -1;
+    // loaded one tile ahead of its use
+    auto load_pos = [&](int j) -> int {
+      const int gi = r0 + j * kBR48 + pw * kRows + lane;
+      return (lane < kRows && gi < r1) ? __ldg(idx + gi) : -1;
+    };
+    int pos_next = load_pos(grp);
+    for (int j = grp; j < ntiles; j += C::kGroups) {
+      const int st = j % S;
+      const uint32_t stage = smem_u32(sm + C::kOffKV + st * kTile48Bytes);
+      const int pos = pos_next;
+      pos_next = load_pos(j + C::kGroups);
       int64_t my_row = -1;
-      if (lane < kRows) {
-        const int gi = r0 + j * kBR48 + pw * kRows + lane;
-        if (gi < r1) {
-          const int pos = __ldg(idx + gi);
-          if (pos >= 0) {
-            if (pos > qp)
-              atomicOr(&g_status_attn, kDevBadIndex);
-            else
-              my_row = phys_row(bt, pos, p.seq.page_size, p.seq.n_pages, &g_status_attn);
-          }
-        }
+      if (pos >= 0) {
+        if (pos > qp)
+          atomicOr(&g_status_attn, kDevBadIndex);
+        else
+          my_row = phys_row(bt, pos, p.seq.page_size, p.seq.n_pages, &g_status_attn);
       }
       const uint32_t bits = __ballot_sync(0xffffffffu, my_row >= 0) & ((1u << kRows) - 1u);
       // every row number first: a shuffle queues behind earlier cp.async copies
@@ -525,12 +541,24 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           }
         }
       }
-      cp_async_commit();
-      cp_async_wait<0>();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&full[st]);
+      if constexpr (C::kAsyncArrive) {
+        // each lane's copies arrive when they land; lane 0 arrives for the warp's
+        // shared stores (row mask, zeroed rows).  The MMA warps fence the async
+        // proxy after their waits.
+        cp_async_mbar_arrive(&full[st]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[st]);
+      } else {
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[st]);
+      }
     }
+    // nothing of this warp in flight when the CTA tears down
+    cp_async_commit();
+    cp_async_wait<0>();
   } else if (warp == kT48Mma || warp == kT48Pv) {
     // ------------------------------------------------ MMA issuers (whole warp, elected lane issues)
     // Bounded waits on the suspending try_wait: the issuing warps share their
@@ -564,6 +592,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         if (j >= 1 && !poll(sfree, (j - 1) & 1)) break;
         if (!poll(&full[j % S], (j / S) & 1)) break;
         tc_fence_after();
+        fence_proxy_async_smem();   // the copies that landed are visible to the tensor core
         if (elect_one()) {
           t48_issue_s<kFp8>(tmem, dq0, dk0 + static_cast<uint64_t>(((j % S) * kTile48Bytes) >> 4));
           umma_commit(sfull);
@@ -578,6 +607,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         // ofull marks every MMA of the CTA done.
         if (!poll(pfull, j & 1)) break;
         tc_fence_after();
+        fence_proxy_async_smem();
         const uint64_t dv = dv0 + static_cast<uint64_t>(((j % S) * kTile48Bytes) >> 4);
         if (elect_one()) {
 #pragma unroll
