@@ -156,7 +156,11 @@ constexpr int kDv = 512;
 constexpr int kDvHalf = 256;     // value dims per CTA = UMMA N of P V
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescPV = make_idesc(kFmtBF16, kFmtBF16, false, true, kH, kDvHalf);
-constexpr float kRescaleThreshold = 8.0f;          // log2 units
+// Running max moved (and O rescaled) only when it grows by more than 2^64: P is
+// bf16 and O, l fp32, whose ranges hold such factors with room to spare (P <=
+// 2^64, O and l <= 2^64 x rows x max|row|), and a rescale stalls a softmax warp
+// for ~2000 cycles, which a threshold of 2^8 met often in causal prefill.
+constexpr float kRescaleThreshold = 64.0f;         // log2 units
 
 struct TcAttnParams {
   SeqArgs seq;
@@ -194,10 +198,10 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
 // its warp's rows into registers before the stage is free, then widens them to
 // bf16 into the tile; the rope goes by cp.async.
 //
-// MMA warps: warp 12 issues Q K^T_{j+1} (N = 48 rows) as soon as the softmax
-// has read S_j and tile j+1 has landed, so it runs during the softmax of tile
-// j; warp 13 issues P V_j (N = 256 value dims, P read from TMEM) as soon as P_j
-// is written.  (One warp issuing both made a ready P V wait behind the issue
+// MMA warps: warp 12 issues Q K^T_{j+1} (N = 48 rows) as soon as tile j+1 has
+// landed, its logit buffer has been read and P V_{j-1} is queued, so it runs
+// during the softmax of tile j; warp 13 issues P V_j (N = 256 value dims) as
+// soon as P_j is written.  (One warp issuing both made a ready P V wait behind the issue
 // of a Q K^T and vice versa: the issuing thread blocks until the tensor pipe
 // has taken the instructions.)  An M=128
 // K=16 step whose A operand (the query) sits in shared memory reads 6 KB of
@@ -206,13 +210,17 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
 //
 // Softmax (warps 14-17): one thread per head (its TMEM lane), 48 logits a tile,
 // running max moved (and O rescaled in TMEM) only when it grows by more than
-// 2^8.
+// 2^64.
 //
-// bf16 rows -- TMEM: S [0,48), P [64,88), Q [96,256), O [256,512); shared
-// memory: query dims [320, 576) (64 KB) + three 54 KB tiles.  (A dedicated MMA
-// warp issuing Q K^T_{j+1} during softmax_j hides the softmax; the third stage
-// hides the gather of a tile behind the work on the other two.)  FP8 rows: see
-// the T48 plan below.
+// bf16 rows -- TMEM: S double-buffered [0,48) and [48,96), Q [96,256), O
+// [256,512); shared memory: query dims [320, 576) (64 KB) + three 54 KB tiles.
+// Once Q K^T_j is complete, the 256 latent dims of tile j that this CTA's value
+// half does not use are dead, and the softmax writes P_j there (128 x 48 bf16, 128B-swizzled K-major, the A operand of
+// P V_j), so TMEM holds two logit buffers: Q K^T_{j+1} is issued as soon as
+// tile j+1 lands and P V_{j-1} is queued, without waiting for the softmax to
+// read S_j, and the tensor pipe does not idle across that hand-off (~700
+// cycles a tile with one buffer).  The third stage hides the gather of a tile
+// behind the work on the other two.  FP8 rows: see the T48 plan below.
 constexpr int kBR48 = 48;
 constexpr int kTile48Bytes = kBR48 * kDqk * 2;                 // 55296
 constexpr int kT48Threads = 576;   // warps 0-11 producers, 12 Q K^T, 13 P V, 14-17 softmax
@@ -226,8 +234,9 @@ constexpr uint32_t kIdescS48 = make_idesc(kFmtBF16, kFmtBF16, false, false, kH, 
 // FP8 rows: the latent codes are widened to bf16 exactly and the per-row scale
 // is applied to the latent logits and folded into P, so the rope logits need
 // their own 48 TMEM columns (Sr): the query keeps dims [0, 256) in TMEM and
-// [256, 576) in shared memory (80 KB), which leaves room for two stages.
-//   bf16 TMEM: S [0,48), P [64,88), Q [96,256), O [256,512)
+// [256, 576) in shared memory (80 KB), which leaves room for two stages; the
+// logits are single-buffered and P sits in TMEM.
+//   bf16 TMEM: S0 [0,48), S1 [48,96), Q [96,256), O [256,512); P in the stage
 //   FP8  TMEM: S [0,48), Sr [48,96), P [96,120), Q [128,256), O [256,512)
 template <bool kFp8>
 struct T48 {
@@ -251,18 +260,22 @@ struct T48 {
   static constexpr int kOffMask = kOffKV + kStages * kTile48Bytes;     // uint16 [stages][producers]
   static constexpr int kOffScale = kOffMask + 128;                      // float [stages][48] (FP8 rows)
   static constexpr int kOffBar = kOffScale + (kFp8 ? kStages * kBR48 * 4 : 0);
-  // barriers: full[S], empty[S], sfull, sfree, pfull, pvdone, ofull
-  static constexpr int kNumBars = 2 * kStages + 5;
+  // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull
+  static constexpr int kNumBars = 3 * kStages + 7;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kUsed = kOffMisc + 16;                           // bytes used from the aligned base
   // the dynamic shared-memory base is re-aligned to 1024 B inside the kernel;
   // the rest of the allocation is slack for that (the kernel checks it sufficed)
   static constexpr int kSlack = kT48SmemBytes - kUsed;
   static constexpr uint32_t kColS = 0, kColSr = 48;
-  static constexpr uint32_t kColP = kFp8 ? 96 : 64, kColQ = kFp8 ? 128 : 96, kColO = 256;
+  static constexpr uint32_t kColP = 96, kColQ = kFp8 ? 128 : 96, kColO = 256;   // kColP: FP8 rows
+  // bf16 rows: two logit buffers, P in the stage (the other value half's latent
+  // dims, dead once Q K^T of the tile is complete) instead of TMEM
+  static constexpr int kSBufs = kFp8 ? 1 : 2;
+  static constexpr bool kPSmem = !kFp8;
   static_assert(kColQ + kQTmemDims / 2 <= kColO, "TMEM plan");
-  static_assert(kColP + kBR48 / 2 <= kColQ && kColS + kBR48 <= (kFp8 ? kColSr : kColP), "TMEM plan");
-  static_assert(!kFp8 || kColSr + kBR48 <= kColP, "TMEM plan");
+  static_assert(kFp8 ? (kColS + kBR48 <= kColSr && kColSr + kBR48 <= kColP && kColP + kBR48 / 2 <= kColQ)
+                     : (kColS + kSBufs * kBR48 <= kColQ), "TMEM plan");
   static_assert(kStages * kProducers * 2 <= 128 && kSlack >= 128, "shared memory budget");
   static_assert(kGroups * kProducers == 12 && kProducers * kRows == kBR48, "producer warps");
 };
@@ -270,14 +283,14 @@ struct T48 {
 // Q K^T of one 48-row tile (elected lane of the MMA warp).  FP8 rows: the 32
 // latent steps accumulate into S, the 4 rope steps into Sr.
 template <bool kFp8>
-__device__ __forceinline__ void t48_issue_s(uint32_t tmem, uint64_t dq0, uint64_t dk) {
+__device__ __forceinline__ void t48_issue_s(uint32_t tmem, uint32_t scol, uint64_t dq0, uint64_t dk) {
   using C = T48<kFp8>;
 #pragma unroll
   for (int kk = 0; kk < kDqk / 16; ++kk) {
     const uint64_t db = dk + static_cast<uint64_t>(((kk >> 2) * kBR48 * 128 + (kk & 3) * 32) >> 4);
     const bool rope = kFp8 && kk >= kDv / 16;
     const uint32_t acc = (kk == 0 || (kFp8 && kk == kDv / 16)) ? 0u : 1u;
-    const uint32_t d = tmem + (rope ? C::kColSr : C::kColS);
+    const uint32_t d = tmem + (rope ? C::kColSr : scol);
     if (kk < C::kQTmemSteps) {
       umma_f16_tmem_a(d, tmem + C::kColQ + kk * 8, db, kIdescS48, acc);
     } else {
@@ -311,11 +324,11 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
   uint64_t* full = bars;            // [S] tile landed (one arrival per warp of the stage's group)
   uint64_t* empty = bars + S;       // [S] tile consumed by P V
-  uint64_t* sfull = bars + 2 * S;   // logits ready
-  uint64_t* sfree = sfull + 1;      // logits read by the softmax (S buffer reusable)
-  uint64_t* pfull = sfull + 2;
-  uint64_t* pvdone = sfull + 3;
-  uint64_t* ofull = sfull + 4;
+  uint64_t* sfull = bars + 2 * S;   // [2] logits ready (per logit buffer)
+  uint64_t* sfree = sfull + 2;      // [2] logits read by the softmax (buffer reusable)
+  uint64_t* pfull = sfull + 4;      // [S] P of the stage's tile written
+  uint64_t* pvis = pfull + S;       // [2] P V_j issued (alternating by tile)
+  uint64_t* ofull = pvis + 2;       // every MMA done
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + C::kOffMask);   // [stage][warp]
@@ -344,11 +357,13 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     for (int i = 0; i < S; ++i) {
       mbar_init(&full[i], C::kFullCount);
       mbar_init(&empty[i], 1);
+      mbar_init(&pfull[i], 128);
     }
-    mbar_init(sfull, 1);
-    mbar_init(sfree, 128);
-    mbar_init(pfull, 128);
-    mbar_init(pvdone, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], 128);
+      mbar_init(&pvis[i], 1);
+    }
     mbar_init(ofull, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -378,6 +393,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     const int h = (warp & 3) * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint4* qrow = reinterpret_cast<const uint4*>(qg + h * kDqk);
+    // every 128-byte line of this head's TMEM part requested from L2 at once: the
+    // blocks below then wait one L2 round trip each instead of one HBM round trip
+#pragma unroll
+    for (int blk = 0; blk < C::kQTmemDims / 64; ++blk) prefetch_l2(qrow + blk * 8);
 #pragma unroll 1
     for (int blk = 0; blk < C::kQTmemDims / 64; ++blk) {
       uint32_t r[32];
@@ -588,35 +607,52 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       const uint64_t dq0 = make_sdesc(smem_u32(sm + C::kOffQ), 16, 1024, kLayoutSw128);
       const uint64_t dk0 = make_sdesc(smem_u32(sm + C::kOffKV), 16, 1024, kLayoutSw128);
       for (int j = 0; j < ntiles; ++j) {
-        // Q K^T_j: tile j has landed and the softmax has read S_{j-1}
-        if (j >= 1 && !poll(sfree, (j - 1) & 1)) break;
+        // Q K^T_j: tile j has landed and the softmax has read the logits last
+        // held by this buffer (S_{j - kSBufs})
+        const int sb = j % C::kSBufs;
+        if (j >= C::kSBufs && !poll(&sfree[sb], ((j / C::kSBufs) - 1) & 1)) break;
+        // ... and after P V_{j-2}, so that the tensor pipe runs S_{j-1}, P V_{j-2},
+        // S_j, P V_{j-1}, ...: a P V never queues behind two Q K^T, and its stage
+        // is freed as early as it can be (two phases apart on alternating
+        // barriers: P V_j needs S_j, so neither runs ahead of this wait)
+        if (j >= 2 && !poll(&pvis[j & 1], ((j - 2) >> 1) & 1)) break;
         if (!poll(&full[j % S], (j / S) & 1)) break;
         tc_fence_after();
         fence_proxy_async_smem();   // the copies that landed are visible to the tensor core
         if (elect_one()) {
-          t48_issue_s<kFp8>(tmem, dq0, dk0 + static_cast<uint64_t>(((j % S) * kTile48Bytes) >> 4));
-          umma_commit(sfull);
+          t48_issue_s<kFp8>(tmem, C::kColS + sb * kBR48, dq0,
+                            dk0 + static_cast<uint64_t>(((j % S) * kTile48Bytes) >> 4));
+          umma_commit(&sfull[sb]);
         }
         __syncwarp();
       }
     } else {
       const uint64_t dv0 = make_sdesc(smem_u32(sm + C::kOffKV) + c * 4 * kBR48 * 128, kBR48 * 128, 1024, kLayoutSw128);
+      // bf16 rows: P_j in stage j mod S, where the other value half's latent dims were
+      const uint64_t dp0 = make_sdesc(smem_u32(sm + C::kOffKV) + (1 - c) * 4 * kBR48 * 128, 16, 1024, kLayoutSw128);
       for (int j = 0; j < ntiles; ++j) {
-        // P V_j as soon as P_j is written.  Its commits also cover Q K^T_j (complete
+        // P V_j as soon as P_j is written.  Its commit also covers Q K^T_j (complete
         // before the softmax wrote P_j), so empty[st] frees the whole stage and
-        // ofull marks every MMA of the CTA done.
-        if (!poll(pfull, j & 1)) break;
+        // tells the softmax that O holds P V_j; ofull marks every MMA of the CTA done.
+        const int st = j % S;
+        if (!poll(&pfull[st], (j / S) & 1)) break;
         tc_fence_after();
         fence_proxy_async_smem();
-        const uint64_t dv = dv0 + static_cast<uint64_t>(((j % S) * kTile48Bytes) >> 4);
+        const uint64_t dv = dv0 + static_cast<uint64_t>((st * kTile48Bytes) >> 4);
+        const uint64_t dp = dp0 + static_cast<uint64_t>((st * kTile48Bytes) >> 4);
         if (elect_one()) {
 #pragma unroll
-          for (int kk = 0; kk < kBR48 / 16; ++kk)
-            umma_f16_tmem_a(tmem + C::kColO, tmem + C::kColP + kk * 8, dv + static_cast<uint64_t>((kk * 16 * 128) >> 4),
-                            kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(pvdone);
-          umma_commit(&empty[j % S]);
+          for (int kk = 0; kk < kBR48 / 16; ++kk) {
+            const uint64_t db = dv + static_cast<uint64_t>((kk * 16 * 128) >> 4);
+            const uint32_t acc = (j > 0 || kk > 0) ? 1u : 0u;
+            if constexpr (C::kPSmem)
+              umma_f16(tmem + C::kColO, dp + static_cast<uint64_t>((kk * 32) >> 4), db, kIdescPV, acc);
+            else
+              umma_f16_tmem_a(tmem + C::kColO, tmem + C::kColP + kk * 8, db, kIdescPV, acc);
+          }
+          umma_commit(&empty[st]);
           if (j == ntiles - 1) umma_commit(ofull);
+          mbar_arrive(&pvis[j & 1]);
         }
         __syncwarp();
       }
@@ -629,9 +665,13 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     const float sl2 = p.a.softmax_scale * kLog2e;
     float m = -INFINITY, l = 0.f, l32 = 0.f;
     bool ok = true;
+    // P_j goes to stage j mod S, where the latent dims of the other value half were
+    const uint32_t p_row = smem_u32(sm + C::kOffKV) + static_cast<uint32_t>((1 - c) * 4 * kBR48 * 128 + h * 128);
     for (int j = 0; j < ntiles; ++j) {
       const int st = j % S;
-      ok = mbar_wait(sfull, j & 1, &g_status_attn, abort_flag);
+      const int sb = j % C::kSBufs;
+      const uint32_t scol = C::kColS + sb * kBR48;
+      ok = mbar_wait(&sfull[sb], (j / C::kSBufs) & 1, &g_status_attn, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // the producers' row mask is ordered by their release on full[st] (still the
       // current phase: the stage is refilled only after this tile's P V)
@@ -641,8 +681,8 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       float x[kBR48];
       {
         uint32_t s0[32], s1[16];
-        tmem_ld32(tmem + lane_off + C::kColS, s0);
-        tmem_ld16(tmem + lane_off + C::kColS + 32, s1);
+        tmem_ld32(tmem + lane_off + scol, s0);
+        tmem_ld16(tmem + lane_off + scol + 32, s1);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < kBR48; ++i) x[i] = __uint_as_float(i < 32 ? s0[i & 31] : s1[(i - 32) & 15]);
@@ -660,7 +700,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         }
       }
       tc_fence_before();
-      mbar_arrive(sfree);
+      mbar_arrive(&sfree[sb]);
       uint64_t vmask = 0;
 #pragma unroll
       for (int w = 0; w < C::kProducers; ++w)
@@ -671,15 +711,18 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         x[i] = ((vmask >> i) & 1u) ? x[i] * sl2 : -INFINITY;
         mloc = fmaxf(mloc, x[i]);
       }
-      if (j >= 1) {
-        // P V_{j-1} has read P and written O
-        ok = mbar_wait(pvdone, (j - 1) & 1, &g_status_attn, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
+      // P V_{j-1} is done once it has freed its stage: empty[(j-1) mod S] in the
+      // phase of tile j-1 (the phase before it completed when tile j-1 was
+      // loaded, the one after needs P_{j-1+S}, so a parity wait cannot alias)
+      const int stp = (j + S - 1) % S;
+      const uint32_t par_prev = ((j - 1) / S) & 1;
       const float m_new = fmaxf(m, mloc);
       const bool need = m_new > m + kRescaleThreshold;
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
+        // O is rescaled: P V_{j-1} must have written it
+        ok = mbar_wait(&empty[stp], par_prev, &g_status_attn, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
         const float f = need ? exp2f(m - m_new) : 1.f;
 #pragma unroll 1
         for (int cc = 0; cc < kDvHalf / 32; ++cc) {
@@ -721,7 +764,21 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       }
       l += psum;
       l32 += psum32;
-      {
+      if constexpr (C::kPSmem) {
+        // row h of the 128B-swizzled K-major P tile: 16-byte chunk q at q ^ (h & 7)
+        const uint32_t prow = p_row + static_cast<uint32_t>(st * kTile48Bytes);
+#pragma unroll
+        for (int q = 0; q < kBR48 / 8; ++q)
+          st_shared_v4(prow + static_cast<uint32_t>((q ^ (h & 7)) << 4), pk[4 * q], pk[4 * q + 1], pk[4 * q + 2],
+                       pk[4 * q + 3]);
+        fence_proxy_async_smem();   // visible to the tensor core's P V_j
+      } else {
+        if (j >= 1) {
+          // P (one TMEM buffer) was read by P V_{j-1}
+          ok = mbar_wait(&empty[stp], par_prev, &g_status_attn, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+          tc_fence_after();
+        }
         uint32_t pa[16], pb[8];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pa[i] = pk[i];
@@ -729,10 +786,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         for (int i = 0; i < 8; ++i) pb[i] = pk[16 + i];
         tmem_st16(tmem + lane_off + C::kColP, pa);
         tmem_st8(tmem + lane_off + C::kColP + 16, pb);
+        tmem_st_wait();
       }
-      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(pfull);
+      mbar_arrive(&pfull[st]);
     }
     if (ok) {
       ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag);
