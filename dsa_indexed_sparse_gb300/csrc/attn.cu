@@ -733,6 +733,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
           tmem_st32(tmem + lane_off + C::kColO + cc * 32, o);
         }
+        tmem_st_wait();   // O rescaled before P V_j may accumulate into it
       }
       if (need) {
         const float f = exp2f(m - m_new);

@@ -239,6 +239,34 @@ def test_attention_single_slice_many_tiles(dev, name, over):
     P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
 
 
+@pytest.mark.parametrize("workspace", [True, False])
+def test_attention_running_max_jumps(dev, workspace):
+    """Rows late in the selection whose logit for one head lies far (> 2**64 in
+    exp2 units) above every earlier one: the kernel must rescale its TMEM
+    accumulator mid-stream.  Four planted rows, one per TMEM lane quarter, each
+    in the second tile of a row slice; their rope part is 16 x that head's rope
+    query, so the latent (value) part stays N(0, 1)."""
+    wl = W.make("decode_b1", seed=9, ctx=[6000], K=2048)
+    idx = O.topk(O.indexer_scores(wl), wl.q_pos, wl.K)
+    q = (wl.q[0].astype(np.uint32) << 16).view(np.float32)             # [H, 576]
+    kv = wl.kv.copy()
+    for rank, h in [(540, 5), (730, 37), (1500, 69), (1910, 101)]:
+        pos = int(idx[0][rank])
+        row = int(wl.block_table[0, pos // wl.page_size]) * wl.page_size + pos % wl.page_size
+        k = (kv[row].astype(np.uint32) << 16).view(np.float32).copy()
+        k[512:] = 16.0 * q[h, 512:]
+        kv[row] = W._bf16_bits(torch.from_numpy(k))
+    wl.kv = kv
+    run = P.Run(wl, dev)
+    g_out, g_lse, plan = run.attn(idx, workspace=workspace)
+    assert ("split=1," in plan) != workspace, plan
+    o_out, o_lse = O.sparse_mla_attn(wl, idx)
+    P.check_attn(g_out, g_lse, o_out, o_lse, "bf16")
+    # the planted rows dominate their heads: the output is (nearly) their value rows
+    s = o_lse[0, [5, 37, 69, 101]]
+    assert np.all(s > 60.0), s
+
+
 # --------------------------------------------------------------------------- device checks
 
 def test_device_check_flags_bad_page_and_position(dev):
