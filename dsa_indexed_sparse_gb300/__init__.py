@@ -26,7 +26,7 @@ EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_
             "dsa_indexer_scores", "dsa_topk", "dsa_sparse_mla_attn_workspace_size",
             "dsa_sparse_mla_attn", "dsa_decode_workspace_size", "dsa_decode_step",
             "dsa_decode_step_static_ws", "dsa_index_cache_append", "dsa_index_cache_append_mx",
-            "dsa_latent_cache_append",
+            "dsa_latent_cache_append", "dsa_debug_withhold_arrival",
             "dsa_check_status")
 STATIC_WORKSPACE_BYTES = 32 << 20   # DSA_STATIC_WORKSPACE_BYTES
 
@@ -76,6 +76,7 @@ def _load() -> ctypes.CDLL:
         "dsa_index_cache_append": (C, [P, ctypes.c_int32, C, P, P, P, P]),
         "dsa_index_cache_append_mx": (C, [P, ctypes.c_int32, C, P, P, P, P]),
         "dsa_latent_cache_append": (C, [P, P, P, P, P]),
+        "dsa_debug_withhold_arrival": (C, [ctypes.c_int32, ctypes.c_uint64]),
         "dsa_check_status": (C, [P]),
     }
     for name, (res, args) in sig.items():
@@ -272,6 +273,13 @@ def latent_cache_append(seq: Seq, mla: Mla, kv_new: torch.Tensor, stream=None) -
     s, m = seq.desc(), mla.desc()
     _check(_lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), _ptr(kv_new), _ptr(mla.kv_cache),
                                         _stream(stream)))
+
+
+def debug_withhold_arrival(enable: bool, wait_limit_ns: int = 2_000_000) -> None:
+    """Testing aid of the failure-detection path: while enabled, tensor-core
+    attention launches have one producer warp withhold an arrival so a bounded
+    wait runs out (after wait_limit_ns) and check_status() raises DSA_ERR_TIMEOUT."""
+    _check(_lib.dsa_debug_withhold_arrival(1 if enable else 0, int(wait_limit_ns)))
 
 
 def check_status(stream=None) -> None:

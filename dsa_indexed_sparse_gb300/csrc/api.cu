@@ -4,10 +4,12 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <vector>
 
 #include "dsa.h"
 #include "dsa_device.cuh"
@@ -154,6 +156,32 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 namespace dsa {
 
 void set_last_error(const std::string& msg) { g_last_error = msg; }
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device) {
+  struct Entry {
+    const void* kernel;
+    int device;
+    cudaError_t result;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : done)
+    if (e.kernel == kernel && e.device == device) return e.result;
+  const cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  done.push_back(Entry{kernel, device, r});
+  return r;
+}
+
+namespace {
+std::atomic<uint32_t> g_dbg_withhold{0};
+std::atomic<uint64_t> g_dbg_wait_limit_ns{kWaitLimitNs};
+}  // namespace
+
+void debug_wait_state(uint64_t* wait_limit_ns, uint32_t* withhold) {
+  *wait_limit_ns = g_dbg_wait_limit_ns.load(std::memory_order_relaxed);
+  *withhold = g_dbg_withhold.load(std::memory_order_relaxed);
+}
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
 bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,
@@ -315,22 +343,36 @@ static size_t decode_ws_layout(const dsa::SeqArgs& s, const dsa::MlaArgs& a, int
   return scores + idx + dsa::attn_workspace_bytes(s, a, num_sms);
 }
 
-size_t dsa_decode_workspace_size(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
-                                 const dsa_mla_desc_t* mla, int32_t K) {
+}  // extern "C"
+
+namespace dsa {
+dsa_status_t decode_workspace_need(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, int32_t K, size_t* need) {
+  *need = 0;
   try {
-    (void)idx;
     dsa::SeqArgs s;
     dsa::MlaArgs a;
-    if (check_seq(seq, &s) != DSA_OK) return 0;
-    if (check_mla_shape(mla, K, &a) != DSA_OK) return 0;
+    dsa_status_t st = check_seq(seq, &s);
+    if (st != DSA_OK) return st;
+    if ((st = check_mla_shape(mla, K, &a)) != DSA_OK) return st;
     dsa::LaunchEnv env;
-    if (make_env(nullptr, &env) != DSA_OK) return 0;
+    if ((st = make_env(nullptr, &env)) != DSA_OK) return st;
     int64_t ld;
     size_t oi, oa;
-    return decode_ws_layout(s, a, env.num_sms, &ld, &oi, &oa);
+    *need = decode_ws_layout(s, a, env.num_sms, &ld, &oi, &oa);
+    return DSA_OK;
   } catch (...) {
-    return 0;
+    return fail(DSA_ERR_CUDA, "unexpected host exception");
   }
+}
+}  // namespace dsa
+
+extern "C" {
+
+size_t dsa_decode_workspace_size(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
+                                 const dsa_mla_desc_t* mla, int32_t K) {
+  (void)idx;
+  size_t need = 0;
+  return dsa::decode_workspace_need(seq, mla, K, &need) == DSA_OK ? need : 0;
 }
 
 dsa_status_t dsa_decode_step(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx, const dsa_mla_desc_t* mla,
@@ -462,6 +504,14 @@ dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_de
   }
 }
 
+dsa_status_t dsa_debug_withhold_arrival(int32_t enable, uint64_t wait_limit_ns) {
+  if (enable && (wait_limit_ns < 1000ull || wait_limit_ns > dsa::kWaitLimitNs))
+    return fail(DSA_ERR_INVALID_ARG, "wait_limit_ns must be in [1 us, 1 s]");
+  dsa::g_dbg_wait_limit_ns.store(enable ? wait_limit_ns : dsa::kWaitLimitNs, std::memory_order_relaxed);
+  dsa::g_dbg_withhold.store(enable ? 1u : 0u, std::memory_order_relaxed);
+  return DSA_OK;
+}
+
 dsa_status_t dsa_check_status(dsa_stream_t stream) {
   try {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
@@ -475,6 +525,7 @@ dsa_status_t dsa_check_status(dsa_stream_t stream) {
     if (f & dsa::kDevBadIndex) msg += " bad_index";
     if (f & dsa::kDevBadPos) msg += " bad_q_pos";
     if (f & dsa::kDevBadGroup) msg += " bad_q_per_seq";
+    if (f & dsa::kDevConfig) msg += " launch_config";
     g_last_error = msg;
     return (f & dsa::kDevTimeout) ? DSA_ERR_TIMEOUT : DSA_ERR_DEVICE_CHECK;
   } catch (...) {

@@ -169,6 +169,8 @@ struct TcAttnParams {
   int32_t rows_per_split;
   uint16_t* ws_o;        // [n_split, T, H, 512] bf16 partials (n_split > 1), each normalised by its own sum
   float* ws_lse;         // [n_split, T, H]
+  uint64_t wait_limit_ns;   // bound of every pipeline wait
+  uint32_t dbg_withhold;    // testing aid: producer warp 0 withholds its arrival on tile 0
 };
 
 // Byte offset of 16-byte chunk `ch` of tile row `r` in a 128B-swizzled K-major
@@ -261,7 +263,8 @@ struct T48 {
   static constexpr int kOffScale = kOffMask + 128;                      // float [stages][48] (FP8 rows)
   static constexpr int kOffBar = kOffScale + (kFp8 ? kStages * kBR48 * 4 : 0);
   // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull
-  static constexpr int kNumBars = 3 * kStages + 7;
+  // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull, drain
+  static constexpr int kNumBars = 3 * kStages + 8;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kUsed = kOffMisc + 16;                           // bytes used from the aligned base
   // the dynamic shared-memory base is re-aligned to 1024 B inside the kernel;
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   // keeps every access through `sm` in the shared window
   uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   if (sm - sm_raw > C::kSlack) {   // block-uniform: the re-aligned layout would not fit
-    if (threadIdx.x == 0) atomicOr(&g_status_attn, kDevTimeout);
+    if (threadIdx.x == 0) atomicOr(&g_status_attn, kDevConfig);
     return;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::kOffBar);
@@ -329,6 +332,8 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   uint64_t* pfull = sfull + 4;      // [S] P of the stage's tile written
   uint64_t* pvis = pfull + S;       // [2] P V_j issued (alternating by tile)
   uint64_t* ofull = pvis + 2;       // every MMA done
+  uint64_t* drain = ofull + 1;      // both issuing warps' MMAs complete (teardown)
+  const uint64_t wlim = p.wait_limit_ns;
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + C::kOffMask);   // [stage][warp]
@@ -365,6 +370,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       mbar_init(&pvis[i], 1);
     }
     mbar_init(ofull, 1);
+    mbar_init(drain, 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -493,7 +499,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
             if (i < kRows * 9 && prow >= 0) prefetch_l2(kv + prow * p.a.row_bytes + (i % 9) * 128);
           }
         }
-        const bool ok = mbar_wait(&empty[st], ((j / S) - 1) & 1, &g_status_attn, abort_flag);
+        const bool ok = mbar_wait(&empty[st], ((j / S) - 1) & 1, &g_status_attn, abort_flag, wlim);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) mask16[st * C::kProducers + pw] = static_cast<uint16_t>(bits);
@@ -560,6 +566,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           }
         }
       }
+      if (p.dbg_withhold && warp == 0 && j == 0) continue;   // testing aid: this stage never completes
       if constexpr (C::kAsyncArrive) {
         // each lane's copies arrive when they land; lane 0 arrives for the warp's
         // shared stores (row mask, zeroed rows).  The MMA warps fence the async
@@ -593,7 +600,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           const uint64_t now = __shfl_sync(0xffffffffu, globaltimer_ns(), 0);
           if (t0 == 0) {
             t0 = now;
-          } else if (now - t0 > kWaitLimitNs) {
+          } else if (now - t0 > wlim) {
             if (lane == 0) {
               atomicOr(&g_status_attn, kDevTimeout);
               *abort_flag = 1;
@@ -671,11 +678,11 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       const int st = j % S;
       const int sb = j % C::kSBufs;
       const uint32_t scol = C::kColS + sb * kBR48;
-      ok = mbar_wait(&sfull[sb], (j / C::kSBufs) & 1, &g_status_attn, abort_flag);
+      ok = mbar_wait(&sfull[sb], (j / C::kSBufs) & 1, &g_status_attn, abort_flag, wlim);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       // the producers' row mask is ordered by their release on full[st] (still the
       // current phase: the stage is refilled only after this tile's P V)
-      ok = mbar_wait(&full[st], (j / S) & 1, &g_status_attn, abort_flag);
+      ok = mbar_wait(&full[st], (j / S) & 1, &g_status_attn, abort_flag, wlim);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
       float x[kBR48];
@@ -720,7 +727,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       const bool need = m_new > m + kRescaleThreshold;
       if (j >= 1 && __any_sync(0xffffffffu, need)) {
         // O is rescaled: P V_{j-1} must have written it
-        ok = mbar_wait(&empty[stp], par_prev, &g_status_attn, abort_flag);
+        ok = mbar_wait(&empty[stp], par_prev, &g_status_attn, abort_flag, wlim);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
         const float f = need ? exp2f(m - m_new) : 1.f;
@@ -776,7 +783,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       } else {
         if (j >= 1) {
           // P (one TMEM buffer) was read by P V_{j-1}
-          ok = mbar_wait(&empty[stp], par_prev, &g_status_attn, abort_flag);
+          ok = mbar_wait(&empty[stp], par_prev, &g_status_attn, abort_flag, wlim);
           if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
           tc_fence_after();
         }
@@ -793,7 +800,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       mbar_arrive(&pfull[st]);
     }
     if (ok) {
-      ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag);
+      ok = mbar_wait(ofull, 0, &g_status_attn, abort_flag, wlim);
       ok = __all_sync(0xffffffffu, ok);
     }
     if (ok) {
@@ -832,6 +839,13 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     }
   }
 
+  if (warp == kT48Mma || warp == kT48Pv) {
+    // every MMA either issuing warp started has finished before TMEM is released
+    // (after an abort, some may still be running)
+    if (elect_one()) umma_commit(drain);
+    __syncwarp();
+    mbar_drain(drain, 0, &g_status_attn, wlim);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == kT48Mma) {
@@ -966,39 +980,20 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
       split = 1;  // no room for partials: one slice per query
     const int rps = ((a.K + split - 1) / split + tile_rows - 1) / tile_rows * tile_rows;
     split = (a.K + rps - 1) / rps;  // every slice non-empty
-    TcAttnParams p{seq, a, split, rps, nullptr, nullptr};
+    TcAttnParams p{seq, a, split, rps, nullptr, nullptr, kWaitLimitNs, 0u};
+    debug_wait_state(&p.wait_limit_ns, &p.dbg_withhold);
     if (split > 1) {
       const size_t o = static_cast<size_t>(split) * seq.T * kH * kDv * sizeof(uint16_t);
       p.ws_o = static_cast<uint16_t*>(workspace);
       p.ws_lse = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((o + 255) / 256) * 256);
     }
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-      attr_err = cudaFuncSetAttribute(attn_tc48_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      kT48SmemBytes);
-      if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(attn_tc48_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kT48SmemBytes);
-      if (attr_err == cudaSuccess)
-        attr_err = cudaFuncSetAttribute(attn_tc48_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kT48SmemBytes);
-    });
+    void (*kern)(TcAttnParams) = fp8 ? attn_tc48_kernel<true> : (tile ? attn_tc48_kernel<false, true>
+                                                                          : attn_tc48_kernel<false>);
+    const cudaError_t attr_err = ensure_smem_limit(reinterpret_cast<const void*>(kern), kT48SmemBytes, env.device);
     if (attr_err != cudaSuccess) return attr_err;
     const int grid = seq.T * split * 2;
-    if (fp8) {
-      const cudaError_t le =
-          launch_kernel(attn_tc48_kernel<true>, dim3(grid), dim3(kT48Threads), kT48SmemBytes, env.stream, true, 1, p);
-      if (le != cudaSuccess) return le;
-    } else if (tile) {
-      const cudaError_t le = launch_kernel(attn_tc48_kernel<false, true>, dim3(grid), dim3(kT48Threads), kT48SmemBytes,
-                                           env.stream, true, 1, p);
-      if (le != cudaSuccess) return le;
-    } else {
-      const cudaError_t le =
-          launch_kernel(attn_tc48_kernel<false>, dim3(grid), dim3(kT48Threads), kT48SmemBytes, env.stream, true, 1, p);
-      if (le != cudaSuccess) return le;
-    }
+    const cudaError_t le = launch_kernel(kern, dim3(grid), dim3(kT48Threads), kT48SmemBytes, env.stream, true, 1, p);
+    if (le != cudaSuccess) return le;
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     char buf[128];
@@ -1023,9 +1018,11 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
     *why = "attn: K or head dim too large for the generic kernel";
     return cudaSuccess;
   }
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(attn_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(smem));
+  if (smem > 48 * 1024) {
+    const cudaError_t ae = cudaFuncSetAttribute(attn_generic_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(smem));
+    if (ae != cudaSuccess) return ae;
+  }
   dim3 grid(a.H, seq.T);
   const cudaError_t le = launch_kernel(attn_generic_kernel, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
   if (le != cudaSuccess) return le;

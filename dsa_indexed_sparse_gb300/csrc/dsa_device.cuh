@@ -17,6 +17,8 @@ enum : uint32_t {
   kDevBadIndex = 2u,    // page id / selected index out of range
   kDevBadPos = 4u,      // q_pos < 0 or q_pos >= max_ctx
   kDevBadGroup = 8u,    // q_per_seq promise broken (group spans two sequences)
+  kDevConfig = 16u,     // a launch configuration the kernel cannot run (e.g. its
+                        // re-aligned shared-memory layout does not fit); nothing done
 };
 
 // Upper bound of any single pipeline wait (the longest legitimate wait is a few
@@ -64,10 +66,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Gives up after
-// kWaitLimitNs (or as soon as another thread of the CTA has given up), sets
+// limit_ns (or as soon as another thread of the CTA has given up), sets
 // kDevTimeout in *status and returns false; never traps.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          volatile int* abort_flag) {
+                                          volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -75,11 +77,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     if (mbar_try_wait(addr, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         atomicOr(status, kDevTimeout);
         *abort_flag = 1;
         return false;
       }
+    }
+  }
+}
+
+// Waits for a phase without looking at the CTA's abort flag: used on the way
+// out, to let asynchronous copies and tensor-core work that were issued before
+// an abort finish before their shared memory or TMEM is released.  Bounded by
+// limit_ns as well; returns false (and sets kDevTimeout) if it gave up.
+__device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                           uint64_t limit_ns = kWaitLimitNs) {
+  const uint32_t addr = smem_u32(bar);
+  if (mbar_try_wait(addr, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(addr, parity)) return true;
+    if ((it & 63u) == 0u && globaltimer_ns() - t0 > limit_ns) {
+      atomicOr(status, kDevTimeout);
+      return false;
     }
   }
 }

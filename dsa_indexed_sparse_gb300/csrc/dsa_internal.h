@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "dsa.h"
+
 #include <string>
 #include <utility>
 
@@ -116,6 +118,20 @@ cudaError_t launch_latent_append(const SeqArgs& seq, const MlaArgs& a, const voi
 
 // Sets the text dsa_last_error() returns on the calling thread.
 void set_last_error(const std::string& msg);
+
+// Raises `kernel`'s dynamic shared-memory limit to `bytes` on `device` (which
+// must be current), once per (kernel, device); later calls return the first
+// call's result.  Thread-safe.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device);
+
+// The failure-detection testing aid (dsa_debug_withhold_arrival): the wait
+// bound the kernels use and whether the attention producer withholds an arrival.
+void debug_wait_state(uint64_t* wait_limit_ns, uint32_t* withhold);
+
+// Scratch bytes dsa_decode_step needs for these descriptors on the current
+// device, with the status (and dsa_last_error text) dsa_decode_step itself
+// would return for a bad descriptor.
+dsa_status_t decode_workspace_need(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, int32_t K, size_t* need);
 
 // Tensor-map encoder (driver entry point, resolved once).
 bool encode_tmap_2d_u8(void* tmap_out, const void* base, uint64_t inner, uint64_t rows,

@@ -144,8 +144,8 @@ struct TcCfg {
   static constexpr int kOffScale = kOffWq + TcWarps<G>::kEpiWarps * kSlice * 4;
   static constexpr int kOffValid = kOffScale + kTcStages * kTcKeys * 4;  // uint32 [stages]
   static constexpr int kOffBar = kOffValid + kTcStages * 4 + 8;
-  // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2]
-  static constexpr int kNumBars = 2 * kTcStages + 8;
+  // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2], drain
+  static constexpr int kNumBars = 2 * kTcStages + 9;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, sched[2], red[one per warp]
   static constexpr int kSmemBytes = kOffMisc + 256 + 1024;  // + alignment slack
   static constexpr uint32_t kIdesc = make_idesc(kFmtE4M3, kFmtE4M3, false, false, kTcKeys, N);
@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   uint64_t* qempty = qfull + 2;
   uint64_t* accfull = qfull + 4;
   uint64_t* accempty = qfull + 6;
+  uint64_t* drain = qfull + 8;     // every MMA of the issuing warp complete (teardown)
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   int* sched = reinterpret_cast<int*>(misc + 2);   // g0, kt0
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       mbar_init(&accfull[i], 1);
       mbar_init(&accempty[i], kEpiWarps);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -330,6 +332,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     bool b_ok = false;
     uint32_t* valid_s = reinterpret_cast<uint32_t*>(sm + C::kOffValid);
     float* scale_s = reinterpret_cast<float*>(sm + C::kOffScale);
+    int issued = 0;   // tiles whose copies were issued
     for (int it = 0; it < ntiles; ++it, w.advance(p)) {
       if (w.g != cur_g) {
         const int qb = qcount & 1;
@@ -385,7 +388,14 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
                          (static_cast<int64_t>(pid) * kTcPage + (lane & 15) * 4) * 4);
         cp_async_mbar_arrive(&full[st]);
       }
+      ++issued;
     }
+    // On the way out (also after an abort) every copy this warp issued has landed
+    // before the CTA's shared memory is released: the last kTcStages tiles' and
+    // the last two query groups' barriers, each in the phase of its last use.
+    for (int k = max(0, issued - kTcStages); k < issued; ++k)
+      mbar_drain(&full[k % kTcStages], (k / kTcStages) & 1, &g_status_indexer);
+    for (int k = max(0, qcount - 2); k < qcount; ++k) mbar_drain(&qfull[k & 1], (k >> 1) & 1, &g_status_indexer);
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
     TileWalker<G> w;
@@ -431,6 +441,10 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       }
       __syncwarp();
     }
+    // every MMA this warp issued has finished before TMEM is released
+    if (elect_one()) umma_commit(drain);
+    __syncwarp();
+    mbar_drain(drain, 0, &g_status_indexer);
   } else {
     // ------------------------------------------------ epilogue (warps 2 .. 2 + 4G - 1)
     // Warp e reduces query j = e / 4 of every group over the 32 keys of TMEM lane
@@ -632,12 +646,8 @@ cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv&
   const int64_t tiles_ub =
       static_cast<int64_t>(p.n_groups) * ((seq.max_ctx + kTcKeys - 1) / kTcKeys);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles_ub, env.num_sms)));
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(indexer_tc_kernel<G, kMx>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
-  });
+  const cudaError_t attr_err =
+      ensure_smem_limit(reinterpret_cast<const void*>(indexer_tc_kernel<G, kMx>), C::kSmemBytes, env.device);
   if (attr_err != cudaSuccess) return attr_err;
   const cudaError_t le = launch_kernel(indexer_tc_kernel<G, kMx>, dim3(grid), dim3(TcWarps<G>::kThreads), C::kSmemBytes,
                                        env.stream, true, 1,
@@ -679,7 +689,10 @@ cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const Launc
   const int fmt = a.mx ? 2 : (a.e4m3 ? 1 : 0);
   void (*kern)(SeqArgs, IndexerArgs) = fmt == 2 ? indexer_generic_kernel<2>
                                        : (fmt == 1 ? indexer_generic_kernel<1> : indexer_generic_kernel<0>);
-  if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+  if (smem > 48 * 1024) {
+    const cudaError_t ae = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (ae != cudaSuccess) return ae;
+  }
   const cudaError_t le = launch_kernel(kern, grid, dim3(kGenThreads), smem, env.stream, true, 1, seq, a);
   if (le != cudaSuccess) return le;
   *plan += fmt == 2 ? "indexer_generic<mxfp8>" : (fmt == 1 ? "indexer_generic<e4m3>" : "indexer_generic<f32>");

@@ -73,8 +73,9 @@ extern "C" {
 dsa_status_t dsa_decode_step_static_ws(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t* idx,
                                        const dsa_mla_desc_t* mla, int32_t K, void* out, float* lse,
                                        int32_t* idx_out, dsa_stream_t stream) {
-  const size_t need = dsa_decode_workspace_size(seq, idx, mla, K);
-  if (need == 0) return DSA_ERR_INVALID_ARG;  // the size query left the reason in dsa_last_error()
+  size_t need = 0;
+  const dsa_status_t chk = dsa::decode_workspace_need(seq, mla, K, &need);
+  if (chk != DSA_OK) return chk;   // the same status (and dsa_last_error text) dsa_decode_step gives
   if (need > kStaticWorkspaceBytes) {
     char buf[160];
     snprintf(buf, sizeof(buf),

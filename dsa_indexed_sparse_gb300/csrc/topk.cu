@@ -366,12 +366,8 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
   const int slice = ((seq.max_ctx + cl - 1) / cl + 3) & ~3;
   const bool cached = slice <= kCacheKeys;
   const size_t smem = cached ? static_cast<size_t>(slice) * 4 : 0;
-  static std::once_flag once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    kCacheKeys * 4);
-  });
+  const cudaError_t attr_err =
+      ensure_smem_limit(reinterpret_cast<const void*>(topk_kernel), kCacheKeys * 4, env.device);
   if (attr_err != cudaSuccess) return attr_err;
   TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, cached ? slice : 0, seq.T};
   cudaError_t e = launch_kernel(topk_kernel, dim3(seq.T * cl), dim3(kThreads), smem, env.stream, /*pdl=*/false, cl, a);

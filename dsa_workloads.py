@@ -112,6 +112,9 @@ class Spec:
     # small enough that the inputs stay close to N(0, 1) and the bf16 outputs stay
     # in the range where a bf16 result can meet the stated 2e-2 max-abs tolerance
     low_rank_amp: float = 0.5
+    # "e4m3_t128" rows: tile scales as powers of two (the cache writer's rule) or,
+    # when False, any fp32 value (amax / 448 of the tile)
+    t128_pow2: bool = True
 
 
 def spec(name: str, **over) -> Spec:
@@ -286,8 +289,12 @@ def make(name_or_spec, seed: int = 0, **over) -> Workload:
         assert sp.d_latent == 512 and sp.d_rope == 64
         lat = kv_f[:, :sp.d_latent].contiguous()
         _spread_blocks(g, lat, 2, block=128, top=0)   # tiles shrunk by 2**{0,-1,-2}
-        codes, exps = _quant_blocks_mx(lat, block=128)
-        scales = np.ldexp(np.float32(1.0), exps.astype(np.int32) - 127).astype("<f4")   # [rows, 4]
+        if sp.t128_pow2:
+            codes, exps = _quant_blocks_mx(lat, block=128)
+            scales = np.ldexp(np.float32(1.0), exps.astype(np.int32) - 127).astype("<f4")   # [rows, 4]
+        else:   # per-tile amax / 448: arbitrary fp32 scales
+            c4, s4 = _quant_rows_e4m3(lat.view(cache_rows, 4, 128))
+            codes, scales = c4.reshape(cache_rows, 512), s4.astype("<f4")
         kv = np.zeros((cache_rows, FP8_ROW_BYTES), dtype=np.uint8)
         kv[:, :512] = codes
         kv[:, FP8_SCALE_OFFSET:FP8_SCALE_OFFSET + 16] = scales.view(np.uint8).reshape(-1, 16)

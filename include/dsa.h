@@ -53,7 +53,8 @@ typedef enum dsa_status {
   DSA_ERR_WORKSPACE = 3,     /* workspace missing or too small                    */
   DSA_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed              */
   DSA_ERR_TIMEOUT = 5,       /* dsa_check_status: a device-side wait gave up      */
-  DSA_ERR_DEVICE_CHECK = 6   /* dsa_check_status: a device-side bounds check hit  */
+  DSA_ERR_DEVICE_CHECK = 6   /* dsa_check_status: a device-side bounds check hit, */
+                             /* or a kernel could not run its launch layout      */
 } dsa_status_t;
 
 typedef enum dsa_dtype {
@@ -258,6 +259,20 @@ dsa_status_t dsa_index_cache_append_mx(const dsa_seq_desc_t* seq, int32_t D_I, d
  *      exactly), the rope copied to [528,656). */
 dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_desc_t* mla, const void* kv_new,
                                      void* kv_cache, dsa_stream_t stream);
+
+/* Testing aid for the failure-detection path; the pages have no counterpart.
+ * Every pipeline wait in the kernels is bounded: a wait that gives up sets a
+ * sticky device flag, every warp of the CTA leaves its loop, in-flight copies
+ * and tensor-core work are drained, TMEM is freed and the kernel returns (no
+ * trap, the context stays usable).  With enable != 0, launches of the
+ * tensor-core attention kernel made after this call have one producer warp
+ * withhold its arrival for the first tile of every CTA, so the tile never
+ * counts as landed: the issuing warp's wait runs out after wait_limit_ns
+ * (1 us .. 1 s) and dsa_check_status() then reports DSA_ERR_TIMEOUT.  Outputs
+ * of those launches are undefined.  enable = 0 restores normal launches and the
+ * 1 s bound.  Process-wide setting; returns DSA_ERR_INVALID_ARG for a bound
+ * outside the range. */
+dsa_status_t dsa_debug_withhold_arrival(int32_t enable, uint64_t wait_limit_ns);
 
 /* Synchronises `stream`, then returns and clears the device status word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK (dsa_last_error() names the

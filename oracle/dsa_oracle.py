@@ -34,7 +34,7 @@ The FP8 latent cache comes in two granularities: one fp32 scale per token
 "Day0 ... Kimi K3.1 Pro", section 4) -- four fp32 scales per token at bytes
 [512, 528), one per 128 latent dims.
 
-Readings taken where the pages are silent (each also listed in the design doc):
+Readings taken where the pages are silent:
 * a query at position p sees s in [0, p] inclusive (its own key is cached);
 * scores are formed in float64 and then rounded to float32 once -- the Top-K
   and every comparison downstream use those float32 values;

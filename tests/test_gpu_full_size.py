@@ -112,3 +112,17 @@ def test_full_size_decode_step(full):
     P.check_selection(g_idx, o_scores, wl.q_pos, wl.K, ts)
     o_out, o_lse = O.sparse_mla_attn(wl, g_idx, ts)
     P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
+
+
+def test_full_size_topk_every_row_in_the_step_launch(dev):
+    """Decode batch 64: the Top-K of all 64 queries in one launch -- the cluster
+    size the decode step and the benchmark use -- bit-exact on the oracle's
+    scores of every row."""
+    wl = W.make("decode_b64", seed=0)
+    run = P.Run(wl, dev)
+    o_scores = O.indexer_scores(wl)
+    _, _, _, step_plan = run.decode_step()
+    g_idx, plan = run.topk(o_scores)
+    launch = plan.split("[", 1)[1]
+    assert "topk_radix" in plan and launch in step_plan, (plan, step_plan)
+    P.check_topk_exact(g_idx, O.topk(o_scores, wl.q_pos, wl.K), wl.q_pos, wl.K)

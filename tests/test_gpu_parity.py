@@ -45,6 +45,10 @@ CASES = {
     # of one row scaled by 2**{0,-1,-2})
     "t128_b2": ("decode_b4_long", dict(ctx=[3000, 4100], B=2, K=2048, mla_dtype="e4m3_t128")),
     "t128_prefill_400": ("prefill_16k", dict(ctx=[400], q_len=400, K=64, mla_dtype="e4m3_t128")),
+    # tile scales that are not powers of two (amax / 448 per tile): the kernel
+    # rounds code x scale to bf16, held to the FP8-cache tolerance
+    "t128_any_scale_b2": ("decode_b4_long", dict(ctx=[3000, 4100], B=2, K=2048, mla_dtype="e4m3_t128",
+                                                 t128_pow2=False)),
 }
 
 
@@ -285,3 +289,34 @@ def test_device_check_flags_bad_page_and_position(dev):
         run2.topk(O.indexer_scores(W.make("decode_b1", seed=2, ctx=[500], K=64))[:, :400])
     assert e.value.status == 6 and "bad_q_pos" in str(e.value)
     dsa.check_status()                               # cleared
+
+
+# --------------------------------------------------------------------------- bounded waits
+
+@pytest.mark.parametrize("name,over", [("decode_b1", dict(ctx=[3000], K=512)),            # bf16 rows, split
+                                       ("decode_b4_long", dict(ctx=[2500], B=1, K=2048))])  # FP8 rows
+def test_bounded_wait_runs_out_and_the_next_step_is_clean(dev, name, over):
+    """A producer warp withholds its arrival on the first tile (testing aid):
+    the issuing warp's bounded wait runs out after 2 ms, every warp unwinds,
+    TMEM is released and dsa_check_status() reports DSA_ERR_TIMEOUT; the
+    context stays usable and the next normal step matches the oracle."""
+    import dsa_indexed_sparse_gb300 as dsa
+    wl = W.make(name, seed=13, **over)
+    run = P.Run(wl, dev)
+    dsa.debug_withhold_arrival(True, 2_000_000)
+    try:
+        with pytest.raises(dsa.DSAError) as e:
+            run.decode_step()
+    finally:
+        dsa.debug_withhold_arrival(False)
+    assert e.value.status == 5 and "timeout" in str(e.value), str(e.value)
+    dsa.check_status()                               # read and cleared
+    with pytest.raises(dsa.DSAError) as e:
+        dsa.debug_withhold_arrival(True, 10)         # bound outside [1 us, 1 s]
+    assert e.value.status == 1
+    o_scores = O.indexer_scores(wl)
+    g_out, g_lse, g_idx, plan = run.decode_step()
+    assert "attn_tc" in plan, plan
+    P.check_selection(g_idx, o_scores, wl.q_pos, wl.K)
+    o_out, o_lse = O.sparse_mla_attn(wl, g_idx)
+    P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
