@@ -405,12 +405,18 @@ dsa_status_t dsa_decode_step(const dsa_seq_desc_t* seq, const dsa_indexer_desc_t
 
     std::string plan, why;
     bool unsupported = false;
-    cudaError_t e = dsa::launch_indexer(s, ia, env, &plan, &unsupported, &why);
-    if (unsupported) return fail(DSA_ERR_UNSUPPORTED, why);
-    if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
-    plan += " -> ";
-    e = dsa::launch_topk(s, scores, ld, K, sel, env, &plan);
-    if (e != cudaSuccess) return cuda_fail(e, "topk launch");
+    // fused plan (scores stay in shared memory) when the batch and contexts allow
+    cudaError_t e = dsa::launch_decode_fused(s, ia, K, sel, env, &plan, &unsupported, &why);
+    if (e != cudaSuccess) return cuda_fail(e, "fused indexer + top-k launch");
+    if (unsupported) {
+      plan.clear();
+      e = dsa::launch_indexer(s, ia, env, &plan, &unsupported, &why);
+      if (unsupported) return fail(DSA_ERR_UNSUPPORTED, why);
+      if (e != cudaSuccess) return cuda_fail(e, "indexer launch");
+      plan += " -> ";
+      e = dsa::launch_topk(s, scores, ld, K, sel, env, &plan);
+      if (e != cudaSuccess) return cuda_fail(e, "topk launch");
+    }
     plan += " -> ";
     e = dsa::launch_attn(s, a, ws + off_attn, workspace_bytes - off_attn, env, &plan, &unsupported, &why);
     if (unsupported) return fail(DSA_ERR_UNSUPPORTED, why);

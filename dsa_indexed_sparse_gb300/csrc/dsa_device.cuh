@@ -65,16 +65,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait that lets the thread sleep until the phase completes (or hint_ns
+// passes): a waiting warp then takes no issue slots from the warps it shares a
+// sub-partition with.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t addr, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Gives up after
 // limit_ns (or as soon as another thread of the CTA has given up), sets
-// kDevTimeout in *status and returns false; never traps.
+// kDevTimeout in *status and returns false; never traps.  With sleep_ns > 0
+// the waiting thread sleeps between polls (up to sleep_ns, woken when the
+// phase completes).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* status,
-                                          volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs) {
+                                          volatile int* abort_flag, uint64_t limit_ns = kWaitLimitNs,
+                                          uint32_t sleep_ns = 0) {
   const uint32_t addr = smem_u32(bar);
   if (mbar_try_wait(addr, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(addr, parity)) return true;
+    if (sleep_ns ? mbar_try_wait_sleep(addr, parity, sleep_ns) : mbar_try_wait(addr, parity)) return true;
     if ((it & 63u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > limit_ns) {

@@ -66,6 +66,12 @@ struct LaunchEnv {
 cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
                            std::string* plan, bool* unsupported, std::string* why);
 
+// Fused decode plan: indexer scores kept in shared memory and the Top-K selected
+// in the same kernel (clusters of CTAs per query); writes idx [T, K] only.  Sets
+// *unsupported (and launches nothing) when the arguments call for the chained plan.
+cudaError_t launch_decode_fused(const SeqArgs& seq, const IndexerArgs& a, int32_t K, int32_t* idx,
+                                const LaunchEnv& env, std::string* plan, bool* unsupported, std::string* why);
+
 // Top-K.
 cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int32_t K,
                         int32_t* idx, const LaunchEnv& env, std::string* plan);

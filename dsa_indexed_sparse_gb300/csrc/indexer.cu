@@ -28,6 +28,7 @@
 
 #include "dsa_device.cuh"
 #include "dsa_internal.h"
+#include "topk_select.cuh"
 
 DSA_DEFINE_STATUS_WORD(indexer)
 
@@ -109,16 +110,33 @@ constexpr int kTcDim = 128;        // D_I (bytes per key row)
 constexpr int kTcKeys = 128;       // keys per tile = UMMA M
 constexpr int kTcPage = 64;        // tokens per page
 constexpr int kTcStages = 6;       // key-tile ring depth (16 KB each)
+// Waiting warps sleep between polls (woken when the phase completes): spinning
+// epilogue warps took the issue slots of the TMA producer on their sub-partition
+// (one tile issued every ~0.45 us).
+constexpr uint32_t kSleepNs = 1000;
 // warp 0 TMA, warp 1 MMA, then the epilogue: one warp per (query of the group,
-// TMEM lane quarter), so 4*G warps.  The ReLU-weighted head sums (two CUDA-core
-// operations per key, query and head) cost about as much issue time as the
-// MMAs' tensor time at prefill, so they get every warp slot the register
-// budget allows.  (Splitting a single query's heads over two warps per quarter
-// made the decode configurations slower.)
-template <int G>
+// TMEM lane quarter) in each of kRot groups that take the tiles in turn (tile it
+// goes to group it % kRot), so 4*G*kRot warps.  The ReLU-weighted head sums (two
+// CUDA-core operations per key, query and head) cost about as much issue time as
+// the MMAs' tensor time at prefill, so they get every warp slot the register
+// budget allows; with one query per group, four groups rotating over the tiles
+// keep one tile's head sums from pacing the key stream.  (Splitting a single
+// query's heads over two warps per quarter made the decode configurations
+// slower.)
+// Every per-tile role is a chain of dependent issue steps that takes one warp
+// ~0.4 us a tile (the copies: page lookup, barrier arrival, TMA, the scales'
+// cp.async; the MMAs: barrier waits, descriptors, four MMAs, two commits), which
+// capped an SM at ~37 GB/s of keys: kProd producer warps and kMmaWarps issuing
+// warps take the tiles in turn as the epilogue groups do.
+template <int G, bool kMx = false>
 struct TcWarps {
-  static constexpr int kEpiWarps = 4 * G;
-  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kRot = G == 1 ? (kMx ? 2 : 3) : 1;
+  static constexpr int kProd = 2;                  // divides kTcStages
+  static constexpr int kMmaWarps = G == 1 ? 2 : 1;
+  static constexpr int kMma = kProd;               // the first MMA-issuing warp (also allocates TMEM)
+  static constexpr int kEpi0 = kProd + kMmaWarps;  // first epilogue warp
+  static constexpr int kEpiWarps = 4 * G * kRot;
+  static constexpr int kThreads = 32 * (kEpi0 + kEpiWarps);
 };
 
 // kMx: MXFP8 keys and queries (E8M0 scale per 32 elements).  The four 32-wide
@@ -133,7 +151,11 @@ struct TcCfg {
   static constexpr int kAccCols = kBlocks * N;           // TMEM columns per tile
   static constexpr int kStageBytes = kTcKeys * kTcDim;   // 16384
   static constexpr int kQBytes = N * kTcDim;             // one query-group buffer
-  static constexpr uint32_t kTmemCols = (2 * kAccCols <= 128) ? 128u : ((2 * kAccCols <= 256) ? 256u : 512u);
+  // accumulator buffers: two, or one per rotation group
+  static constexpr int kAccBufs = TcWarps<G, kMx>::kRot > 2 ? TcWarps<G, kMx>::kRot : 2;
+  static constexpr int kTmemNeed = kAccBufs * kAccCols;
+  static_assert(kTmemNeed <= 512, "TMEM plan");
+  static constexpr uint32_t kTmemCols = kTmemNeed <= 128 ? 128u : (kTmemNeed <= 256 ? 256u : 512u);
   // per epilogue warp: w / 2 for its 64 heads, then (MXFP8) the query's block
   // factors 2^(e - 127) as float [4][64]
   static constexpr int kSlice = kTcHeads * (1 + (kMx ? kBlocks : 0));
@@ -141,20 +163,33 @@ struct TcCfg {
   static constexpr int kOffQ = kOffStages + kTcStages * kStageBytes;
   static constexpr int kOffWq = kOffQ + 2 * kQBytes;      // float [4G][kSlice]: each epilogue warp's slice
   // key scales: 4 bytes per key (an fp32 scale, or MXFP8's four E8M0 bytes)
-  static constexpr int kOffScale = kOffWq + TcWarps<G>::kEpiWarps * kSlice * 4;
+  static constexpr int kOffScale = kOffWq + TcWarps<G, kMx>::kEpiWarps * kSlice * 4;
   static constexpr int kOffValid = kOffScale + kTcStages * kTcKeys * 4;  // uint32 [stages]
   static constexpr int kOffBar = kOffValid + kTcStages * 4 + 8;
-  // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[2], accempty[2], drain
-  static constexpr int kNumBars = 2 * kTcStages + 9;
+  // barriers: full[S], empty[S], qfull[2], qempty[2], accfull[A], accempty[A], drain
+  static constexpr int kNumBars = 2 * kTcStages + 4 + 2 * kAccBufs + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort, sched[2], red[one per warp]
   static constexpr int kSmemBytes = kOffMisc + 256 + 1024;  // + alignment slack
+  // fused decode plan: the selection's scratch, then this CTA's keys (read 16
+  // bytes at a time), both 128-byte aligned
+  static constexpr int kOffSel = (kOffMisc + 256 + 127) / 128 * 128;
+  static constexpr int kOffKeys = (kOffSel + static_cast<int>(sizeof(SelectSmem)) + 127) / 128 * 128;
+  static_assert(kOffKeys % 16 == 0 && kOffSel % 16 == 0, "aligned fused-plan regions");
   static constexpr uint32_t kIdesc = make_idesc(kFmtE4M3, kFmtE4M3, false, false, kTcKeys, N);
 };
+
+// Keys of one query a CTA of the fused plan holds in shared memory at most.
+constexpr int kFusedMaxKeys = 16384;
+// Largest cluster (CTAs per query) the fused plan is chosen for.
+constexpr int kFusedMaxCluster = 2;
 
 struct TcParams {
   SeqArgs seq;
   IndexerArgs a;
   int32_t n_groups;
+  // fused decode plan: the selection's K and the index rows [T, K]
+  int32_t K;
+  int32_t* idx;
 };
 
 // Number of 128-key tiles of query group g (its longest causal history), with
@@ -211,13 +246,27 @@ __device__ __forceinline__ int block_sum(int v, int* red) {
   return tot;
 }
 
-template <int G, bool kMx>
-__global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
-    indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap,
+// kFused (one query per group): the fused decode plan.  A cluster of CTAs per
+// query, each CTA streaming a contiguous run of its key tiles; the epilogue
+// writes each score as an order key into this CTA's shared memory (never to
+// global memory) and counts it into the first histogram; once the cluster's
+// keys are complete the CTAs select the Top-K together and only the index row
+// leaves the SM.
+template <int G, bool kMx, bool kFused>
+__global__ void __launch_bounds__(TcWarps<G, kMx>::kThreads, 1)
+    indexer_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap kmap2,
                       const __grid_constant__ CUtensorMap qmap, TcParams p) {
+  static_assert(!kFused || G == 1, "the fused plan runs one query per group");
   using C = TcCfg<G, kMx>;
-  constexpr int kTcThreads = TcWarps<G>::kThreads;
-  constexpr int kEpiWarps = TcWarps<G>::kEpiWarps;
+  constexpr int kTcThreads = TcWarps<G, kMx>::kThreads;
+  constexpr int kRot = TcWarps<G, kMx>::kRot;
+  constexpr int kProd = TcWarps<G, kMx>::kProd;
+  constexpr int kMmaWarp = TcWarps<G, kMx>::kMma;
+  constexpr int kMmaWarps = TcWarps<G, kMx>::kMmaWarps;
+  constexpr int kEpi0 = TcWarps<G, kMx>::kEpi0;
+  static_assert(kTcStages % kProd == 0, "each producer owns every kProd-th stage");
+  constexpr int kGroupWarps = 4 * G;           // epilogue warps that share one tile
+  constexpr int NB = C::kAccBufs;
   static_assert(4 + kTcThreads / 32 <= 64, "misc area holds one int per warp");
   // No grid_dep_wait() yet: the work split, barriers and TMEM (inputs only)
   // overlap the tail of the kernel before when that one lets this grid start early.
@@ -231,8 +280,8 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   uint64_t* qfull = bars + 2 * kTcStages;
   uint64_t* qempty = qfull + 2;
   uint64_t* accfull = qfull + 4;
-  uint64_t* accempty = qfull + 6;
-  uint64_t* drain = qfull + 8;     // every MMA of the issuing warp complete (teardown)
+  uint64_t* accempty = accfull + NB;
+  uint64_t* drain = accempty + NB;   // every MMA of the issuing warp complete (teardown)
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   int* sched = reinterpret_cast<int*>(misc + 2);   // g0, kt0
@@ -241,6 +290,42 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
+  SelectSmem* sel = reinterpret_cast<SelectSmem*>(sm + C::kOffSel);
+  uint32_t* keys_s = reinterpret_cast<uint32_t*>(sm + C::kOffKeys);
+  int f_lo = 0, f_len = 0, f_CL = 1;   // fused: this CTA's slice of the query's history
+  int32_t* f_out = nullptr;
+  int64_t begin = 0, end = 0;
+  if constexpr (kFused) {
+    // ---- one query per cluster; an equal share of its tiles per CTA -----------
+    f_CL = static_cast<int>(cl_size());
+    const int rank = static_cast<int>(cl_rank());
+    const int t = p.seq.T - 1 - static_cast<int>(blockIdx.x) / f_CL;
+    int qp = __ldg(p.seq.q_pos + t);
+    if (qp < 0 || qp >= p.seq.max_ctx) {
+      if (threadIdx.x == 0 && rank == 0) atomicOr(&g_status_indexer, kDevBadPos);
+      qp = -1;
+    }
+    const int n = qp + 1;
+    f_out = p.idx + static_cast<int64_t>(t) * p.K;
+    if (n <= p.K) {   // cluster-uniform: every position is kept, no score needed
+      grid_dep_wait();   // the index row may still be read by the kernel before
+      for (int i = rank * kTcThreads + threadIdx.x; i < p.K; i += f_CL * kTcThreads) f_out[i] = i < n ? i : -1;
+      grid_dep_launch();
+      return;
+    }
+    const int tiles = (n + kTcKeys - 1) / kTcKeys;
+    const int kt0 = static_cast<int>(static_cast<int64_t>(rank) * tiles / f_CL);
+    const int kt1 = static_cast<int>(static_cast<int64_t>(rank + 1) * tiles / f_CL);
+    if (threadIdx.x == 0) {
+      sched[0] = t;
+      sched[1] = kt0;
+    }
+    begin = 0;
+    end = kt1 - kt0;
+    f_lo = kt0 * kTcKeys;
+    f_len = max(0, min(n, kt1 * kTcKeys) - f_lo);
+    select_prepare<kTcThreads>(sel, f_CL);   // zeroes the histograms, arrives at the cluster barrier
+  } else {
   // ---- work split: equal share of the global tile list -----------------
   int total = 0;
   for (int g0 = 0; g0 < p.n_groups; g0 += kTcThreads) {
@@ -249,8 +334,8 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     const int c = (g < p.n_groups) ? group_tiles<G>(p, g, &nh) : 0;
     total += block_sum<kTcThreads>(c, red);
   }
-  const int64_t begin = static_cast<int64_t>(blockIdx.x) * total / gridDim.x;
-  const int64_t end = static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x;
+  begin = static_cast<int64_t>(blockIdx.x) * total / gridDim.x;
+  end = static_cast<int64_t>(blockIdx.x + 1) * total / gridDim.x;
   if (begin >= end) return;  // block-uniform
   {
     int run = 0;
@@ -281,6 +366,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       run += chunk;
     }
   }
+  }
 
   // ---- barriers and TMEM -------------------------------------------------
   if (threadIdx.x == 0) {
@@ -289,24 +375,28 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     const uint32_t full_count = 1u + (p.a.k_scale != nullptr ? 32u : 0u);
     for (int i = 0; i < kTcStages; ++i) {
       mbar_init(&full[i], full_count);
-      // freed by the MMA (keys read) and by each epilogue warp (key scales read)
-      mbar_init(&empty[i], 1 + kEpiWarps);
+      // freed by the MMA (keys read) and by each epilogue warp of the tile's
+      // group (key scales read)
+      mbar_init(&empty[i], 1 + kGroupWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&qfull[i], 1);
-      mbar_init(&qempty[i], 1);
-      mbar_init(&accfull[i], 1);
-      mbar_init(&accempty[i], kEpiWarps);
+      mbar_init(&qempty[i], kMmaWarps);   // each issuing warp releases a group's Q
     }
-    mbar_init(drain, 1);
+    for (int i = 0; i < NB; ++i) {
+      mbar_init(&accfull[i], 1);
+      mbar_init(&accempty[i], kGroupWarps);
+    }
+    mbar_init(drain, kMmaWarps);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&kmap);
+    tma_prefetch_desc(&kmap2);
     tma_prefetch_desc(&qmap);
   }
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tmem_alloc(misc, C::kTmemCols);
     tmem_relinquish();
   }
@@ -318,56 +408,69 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
   const int ntiles = static_cast<int>(end - begin);   // <= total, an int
   grid_dep_wait();
 
-  if (warp == 0) {
-    // ------------------------------------------------ TMA producer (warp 0)
-    // The warp keeps the page ids of a window of 32 logical pages in registers
-    // (one per lane, loaded in parallel); lane 0 issues, per 128-key tile, the TMA
-    // tile loads of its two pages and the bulk copies of their per-key scales.
+  if (warp < kProd) {
+    // ------------------------------------------------ TMA producers (warps 0 .. kProd - 1)
+    // Producer pw issues the copies of the tiles it with it % kProd == pw (and so
+    // of the stages st with st % kProd == pw).  It keeps the page ids of its next
+    // 16 tiles in registers (lane l: tile l / 2, page l % 2, loaded in parallel);
+    // lane 0 issues the TMA tile loads, every lane one 16-byte copy of key
+    // scales.  A query group's own TMA load goes with the producer of the
+    // group's first tile in this CTA.
+    const int pw = warp;
     TileWalker<G> w;
     w.init(p, g_start, kt_start);
     int cur_g = -1, qcount = 0;
-    int win = -1;           // first logical page held in the window
-    int32_t my_page = -1;   // page id of logical page win + lane
+    int win_kt = -1;        // kt of the window's first tile; the window holds kt, kt + kProd, ...
+    int32_t my_page = -1;   // page id of window tile lane / 2, page lane % 2
     const int32_t* bt = p.seq.block_table;
     bool b_ok = false;
+    int npg = 0;
     uint32_t* valid_s = reinterpret_cast<uint32_t*>(sm + C::kOffValid);
     float* scale_s = reinterpret_cast<float*>(sm + C::kOffScale);
-    int issued = 0;   // tiles whose copies were issued
+    int issued = 0, last_it = -1;   // tiles whose copies this warp issued, the last of them
+    uint32_t q_mine = 0;   // bit b: the last Q load into buffer b was issued by this warp
     for (int it = 0; it < ntiles; ++it, w.advance(p)) {
       if (w.g != cur_g) {
         const int qb = qcount & 1;
-        if (qcount >= 2) {
-          const bool ok = mbar_wait(&qempty[qb], ((qcount >> 1) - 1) & 1, &g_status_indexer, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) break;
+        const bool mine = it % kProd == pw;
+        if (mine) {
+          if (qcount >= 2) {
+            const bool ok = mbar_wait(&qempty[qb], ((qcount >> 1) - 1) & 1, &g_status_indexer, abort_flag,
+                                      kWaitLimitNs, kSleepNs);
+            if (!__all_sync(0xffffffffu, ok)) break;
+          }
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
+            tma_load_2d(sm + C::kOffQ + qb * C::kQBytes, &qmap, &qfull[qb], 0, w.g * G * kTcHeads);
+          }
         }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&qfull[qb], C::kQBytes);
-          tma_load_2d(sm + C::kOffQ + qb * C::kQBytes, &qmap, &qfull[qb], 0, w.g * G * kTcHeads);
-        }
+        q_mine = mine ? (q_mine | (1u << qb)) : (q_mine & ~(1u << qb));
         const int b = __ldg(p.seq.q_seq + w.g * G);
         b_ok = (b >= 0 && b < p.seq.B);
         bt = p.seq.block_table + static_cast<int64_t>(b_ok ? b : 0) * p.seq.bt_stride;
-        win = -1;
+        npg = (w.nhist + kTcPage - 1) / kTcPage;
+        win_kt = -1;
         cur_g = w.g;
         ++qcount;
       }
-      const int npg = (w.nhist + kTcPage - 1) / kTcPage;
-      const int lp0 = 2 * w.kt;
-      if (win < 0 || lp0 + 1 >= win + 32) {
-        win = lp0;
-        const int lp = win + lane;
+      if (it % kProd != pw) continue;
+      if (win_kt < 0 || (w.kt - win_kt) / kProd >= 16) {
+        win_kt = w.kt;
+        const int lp = 2 * (win_kt + (lane >> 1) * kProd) + (lane & 1);
         my_page = (b_ok && lp < npg) ? __ldg(bt + lp) : -1;
         if (lp < npg && (my_page < 0 || my_page >= p.seq.n_pages || !b_ok)) {
           atomicOr(&g_status_indexer, kDevBadIndex);
           my_page = -1;
         }
       }
-      const int32_t pid0 = __shfl_sync(0xffffffffu, my_page, lp0 - win);
-      int32_t pid1 = __shfl_sync(0xffffffffu, my_page, min(lp0 + 1 - win, 31));
-      if (lp0 + 1 >= npg) pid1 = -1;
+      const int wi = 2 * ((w.kt - win_kt) / kProd);
+      const int32_t pid0 = __shfl_sync(0xffffffffu, my_page, wi);
+      int32_t pid1 = __shfl_sync(0xffffffffu, my_page, wi + 1);
+      if (2 * w.kt + 1 >= npg) pid1 = -1;
       const int st = it % kTcStages;
       if (it >= kTcStages) {
-        const bool ok = mbar_wait(&empty[st], ((it / kTcStages) - 1) & 1, &g_status_indexer, abort_flag);
+        const bool ok = mbar_wait(&empty[st], ((it / kTcStages) - 1) & 1, &g_status_indexer, abort_flag,
+                                  kWaitLimitNs, kSleepNs);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) {
@@ -375,8 +478,13 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         valid_s[st] = (pid0 >= 0 ? 1u : 0u) | (pid1 >= 0 ? 2u : 0u);
         mbar_arrive_expect_tx(&full[st], (pid0 >= 0 ? per_page : 0u) + (pid1 >= 0 ? per_page : 0u));
         uint8_t* dst = sm + C::kOffStages + st * C::kStageBytes;
-        if (pid0 >= 0) tma_load_2d(dst, &kmap, &full[st], 0, pid0 * kTcPage);
-        if (pid1 >= 0) tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid1 * kTcPage);
+        // two adjacent pages go in one 128-row box (kmap2), the others one page each
+        if (pid0 >= 0 && pid1 == pid0 + 1) {
+          tma_load_2d(dst, &kmap2, &full[st], 0, pid0 * kTcPage);
+        } else {
+          if (pid0 >= 0) tma_load_2d(dst, &kmap, &full[st], 0, pid0 * kTcPage);
+          if (pid1 >= 0) tma_load_2d(dst + C::kStageBytes / 2, &kmap, &full[st], 0, pid1 * kTcPage);
+        }
       }
       if (p.a.k_scale != nullptr) {
         // lanes 0-15: the 64 scales of the first page, lanes 16-31: the second (16 B each)
@@ -389,15 +497,25 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         cp_async_mbar_arrive(&full[st]);
       }
       ++issued;
+      last_it = it;
     }
     // On the way out (also after an abort) every copy this warp issued has landed
-    // before the CTA's shared memory is released: the last kTcStages tiles' and
-    // the last two query groups' barriers, each in the phase of its last use.
-    for (int k = max(0, issued - kTcStages); k < issued; ++k)
+    // before the CTA's shared memory is released: its last tiles, one per stage
+    // it owns, and the Q loads of the last two groups if it issued them, each in
+    // the phase of its last use.
+    for (int m = 0; m < min(issued, kTcStages / kProd); ++m) {
+      const int k = last_it - m * kProd;
       mbar_drain(&full[k % kTcStages], (k / kTcStages) & 1, &g_status_indexer);
-    for (int k = max(0, qcount - 2); k < qcount; ++k) mbar_drain(&qfull[k & 1], (k >> 1) & 1, &g_status_indexer);
-  } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer (whole warp, elected lane issues)
+    }
+    for (int k = max(0, qcount - 2); k < qcount; ++k)
+      if ((q_mine >> (k & 1)) & 1u) mbar_drain(&qfull[k & 1], (k >> 1) & 1, &g_status_indexer);
+  } else if (warp < kMmaWarp + kMmaWarps) {
+    // ------------------------------------------------ MMA issuers (whole warps, an elected lane issues)
+    // Issuing warp mw takes the tiles it with it % kMmaWarps == mw.  Every issuing
+    // warp waits for each group's Q and releases it (its commit arrives once its
+    // own MMAs on it are done), so no warp can release a buffer's next group
+    // before that group's Q has landed.
+    const int mw = warp - kMmaWarp;
     TileWalker<G> w;
     w.init(p, g_start, kt_start);
     int cur_g = -1, qcount = 0, qb = 0;
@@ -408,17 +526,18 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
           __syncwarp();
         }
         qb = qcount & 1;
-        const bool ok = mbar_wait(&qfull[qb], (qcount >> 1) & 1, &g_status_indexer, abort_flag);
+        const bool ok = mbar_wait(&qfull[qb], (qcount >> 1) & 1, &g_status_indexer, abort_flag, kWaitLimitNs, kSleepNs);
         if (!__all_sync(0xffffffffu, ok)) break;
         cur_g = w.g;
         ++qcount;
       }
+      if (kMmaWarps > 1 && it % kMmaWarps != mw) continue;
       const int st = it % kTcStages;
-      bool ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
+      bool ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag, kWaitLimitNs, kSleepNs);
       if (!__all_sync(0xffffffffu, ok)) break;
-      const int ab = it & 1;
-      if (it >= 2) {
-        ok = mbar_wait(&accempty[ab], ((it >> 1) - 1) & 1, &g_status_indexer, abort_flag);
+      const int ab = it % NB;
+      if (it >= NB) {
+        ok = mbar_wait(&accempty[ab], ((it / NB) - 1) & 1, &g_status_indexer, abort_flag, kWaitLimitNs, kSleepNs);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       tc_fence_after();
@@ -446,15 +565,16 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
     __syncwarp();
     mbar_drain(drain, 0, &g_status_indexer);
   } else {
-    // ------------------------------------------------ epilogue (warps 2 .. 2 + 4G - 1)
+    // ------------------------------------------------ epilogue (warps kEpi0 ..)
     // Warp e reduces query j = e / 4 of every group over the 32 keys of TMEM lane
     // quarter warp % 4.  Its head weights (w * q_scale) live in its own 64-float
     // slice of shared memory; the next group's weights and positions are fetched
     // into registers while the current group runs, so a group switch costs no
     // global-memory round trip.
-    const int e = warp - 2;
-    const int quarter = warp & 3;
-    const int j = e >> 2;                     // query of the group
+    const int e = warp - kEpi0;
+    const int quarter = warp & 3;   // the TMEM lanes a warp may read: 32 * (warp % 4) ..
+    const int rg = e / kGroupWarps;           // rotation group: tiles it with it % kRot == rg
+    const int j = (e % kGroupWarps) >> 2;     // query of the group
     const int row = quarter * 32 + lane;          // key within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     float* wq = wq_s + e * C::kSlice;
@@ -494,6 +614,7 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
       }
     };
     for (int it = 0; it < ntiles; ++it, w.advance(p)) {
+      if (kRot > 1 && it % kRot != rg) continue;
       if (w.g != cur_g) {
         if (pf_g != w.g) prefetch(w.g);
         const int tq = w.g * G + j;
@@ -521,14 +642,14 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         cur_g = w.g;
         if (w.g + 1 < p.n_groups) prefetch(w.g + 1);
       }
-      const int ab = it & 1;
-      bool ok = mbar_wait(&accfull[ab], (it >> 1) & 1, &g_status_indexer, abort_flag);
+      const int ab = it % NB;
+      bool ok = mbar_wait(&accfull[ab], (it / NB) & 1, &g_status_indexer, abort_flag, kWaitLimitNs, kSleepNs);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
       // the stage (keys, scales, page validity) is still this tile's: the
       // producer refills it only after this warp's arrival on empty[st]
       const int st = it % kTcStages;
-      ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag);
+      ok = mbar_wait(&full[st], (it / kTcStages) & 1, &g_status_indexer, abort_flag, kWaitLimitNs, kSleepNs);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int s = w.kt * kTcKeys + row;
       uint32_t vmask;
@@ -617,16 +738,32 @@ __global__ void __launch_bounds__(TcWarps<G>::kThreads, 1)
         }
       }
       const float sum = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-      if (key_ok && s <= qp) srow[s] = sum * sk;
+      if constexpr (kFused) {
+        // a key on a bad page (flagged above) gets the lowest key of all
+        if (s <= qp) {
+          const uint32_t k = key_ok ? order_key(sum * sk) : 0u;
+          keys_s[s - f_lo] = k;
+          select_count0(sel, k);
+        }
+      } else {
+        if (key_ok && s <= qp) srow[s] = sum * sk;
+      }
     }
   }
 
   grid_dep_launch();  // this CTA's work is done: the next kernel may launch
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
+  }
+  if constexpr (kFused) {
+    // this CTA's keys are complete (the barrier above); select over the cluster
+    select_run<kTcThreads>(
+        sel, [&](int i) -> uint32_t { return keys_s[i]; },
+        [&](int i) -> uint4 { return reinterpret_cast<const uint4*>(keys_s)[i >> 2]; }, f_len, f_lo, p.K, f_out,
+        true);
   }
 }
 
@@ -634,24 +771,26 @@ template <int G, bool kMx = false>
 cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
                       std::string* plan, bool* unsupported, std::string* why) {
   using C = TcCfg<G, kMx>;
-  alignas(64) CUtensorMap kmap, qmap;
+  alignas(64) CUtensorMap kmap, kmap2, qmap;
   if (!encode_tmap_2d_u8(&kmap, a.k, kTcDim, static_cast<uint64_t>(seq.cache_rows), kTcDim,
                          kTcDim, kTcPage, why) ||
+      !encode_tmap_2d_u8(&kmap2, a.k, kTcDim, static_cast<uint64_t>(seq.cache_rows), kTcDim,
+                         kTcDim, 2 * kTcPage, why) ||
       !encode_tmap_2d_u8(&qmap, a.q, kTcDim, static_cast<uint64_t>(seq.T) * kTcHeads, kTcDim,
                          kTcDim, C::N, why)) {
     *unsupported = true;
     return cudaSuccess;
   }
-  TcParams p{seq, a, (seq.T + G - 1) / G};
+  TcParams p{seq, a, (seq.T + G - 1) / G, 0, nullptr};
   const int64_t tiles_ub =
       static_cast<int64_t>(p.n_groups) * ((seq.max_ctx + kTcKeys - 1) / kTcKeys);
   const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(tiles_ub, env.num_sms)));
   const cudaError_t attr_err =
-      ensure_smem_limit(reinterpret_cast<const void*>(indexer_tc_kernel<G, kMx>), C::kSmemBytes, env.device);
+      ensure_smem_limit(reinterpret_cast<const void*>(indexer_tc_kernel<G, kMx, false>), C::kSmemBytes, env.device);
   if (attr_err != cudaSuccess) return attr_err;
-  const cudaError_t le = launch_kernel(indexer_tc_kernel<G, kMx>, dim3(grid), dim3(TcWarps<G>::kThreads), C::kSmemBytes,
+  const cudaError_t le = launch_kernel(indexer_tc_kernel<G, kMx, false>, dim3(grid), dim3(TcWarps<G, kMx>::kThreads), C::kSmemBytes,
                                        env.stream, true, 1,
-                                    kmap, qmap, p);
+                                    kmap, kmap2, qmap, p);
   if (le != cudaSuccess) return le;
   char buf[160];
   snprintf(buf, sizeof(buf), "indexer_tc<G=%d%s>[grid=%d,tiles<=%lld]", G, kMx ? ",mxfp8" : "", grid,
@@ -660,7 +799,93 @@ cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv&
   return cudaGetLastError();
 }
 
+// Fused decode plan (indexer + Top-K, scores in shared memory): clusters of CL
+// CTAs, one cluster per query.  CL: the whole GPU in one wave at small batch
+// (up to 16 CTAs per query, non-portable cluster size), and enough CTAs that a
+// slice's keys fit kFusedMaxKeys.  Returns CL, or 0 when the plan does not apply.
+template <bool kMx>
+int fused_cluster(const SeqArgs& seq, const LaunchEnv& env) {
+  const int need = (seq.max_ctx + kFusedMaxKeys - 1) / kFusedMaxKeys;
+  int cl = 1;
+  while (cl < 16 && static_cast<int64_t>(seq.T) * cl * 2 <= env.num_sms) cl *= 2;
+  cl = std::max(cl, need);
+  if (cl > 16) return 0;
+  // every cluster of the launch resident at once is not required, but a cluster
+  // of this size must fit on the GPU
+  using C = TcCfg<1, kMx>;
+  const int keys = (((seq.max_ctx + kTcKeys - 1) / kTcKeys + cl - 1) / cl) * kTcKeys;
+  const size_t smem = static_cast<size_t>(C::kOffKeys) + static_cast<size_t>(keys) * 4 + 1024;
+  void (*kern)(CUtensorMap, CUtensorMap, CUtensorMap, TcParams) = indexer_tc_kernel<1, kMx, true>;
+  if (ensure_smem_limit(reinterpret_cast<const void*>(kern),
+                        C::kOffKeys + kFusedMaxKeys * 4 + 1024, env.device) != cudaSuccess)
+    return 0;
+  static_cast<void>(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  while (cl > 1) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(seq.T * cl);
+    cfg.blockDim = dim3(TcWarps<1, kMx>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(cl);
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) break;
+    cudaGetLastError();
+    cl /= 2;
+    if (cl < need) return 0;
+  }
+  return cl;
+}
+
+template <bool kMx>
+cudaError_t launch_fused(const SeqArgs& seq, const IndexerArgs& a, int32_t K, int32_t* idx, int cl,
+                         const LaunchEnv& env, std::string* plan, std::string* why, bool* unsupported) {
+  using C = TcCfg<1, kMx>;
+  alignas(64) CUtensorMap kmap, kmap2, qmap;
+  if (!encode_tmap_2d_u8(&kmap, a.k, kTcDim, static_cast<uint64_t>(seq.cache_rows), kTcDim, kTcDim, kTcPage, why) ||
+      !encode_tmap_2d_u8(&kmap2, a.k, kTcDim, static_cast<uint64_t>(seq.cache_rows), kTcDim, kTcDim, 2 * kTcPage,
+                         why) ||
+      !encode_tmap_2d_u8(&qmap, a.q, kTcDim, static_cast<uint64_t>(seq.T) * kTcHeads, kTcDim, kTcDim, C::N, why)) {
+    *unsupported = true;
+    return cudaSuccess;
+  }
+  TcParams p{seq, a, seq.T, K, idx};
+  const int keys = (((seq.max_ctx + kTcKeys - 1) / kTcKeys + cl - 1) / cl) * kTcKeys;
+  const size_t smem = static_cast<size_t>(C::kOffKeys) + static_cast<size_t>(keys) * 4 + 1024;
+  const cudaError_t le = launch_kernel(indexer_tc_kernel<1, kMx, true>, dim3(seq.T * cl), dim3(TcWarps<1, kMx>::kThreads),
+                                       smem, env.stream, true, cl, kmap, kmap2, qmap, p);
+  if (le != cudaSuccess) return le;
+  char buf[160];
+  snprintf(buf, sizeof(buf), "indexer_topk_fused<%s>[cluster=%d,grid=%d]", kMx ? "mxfp8" : "e4m3", cl, seq.T * cl);
+  *plan += buf;
+  return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_decode_fused(const SeqArgs& seq, const IndexerArgs& a, int32_t K, int32_t* idx,
+                                const LaunchEnv& env, std::string* plan, bool* unsupported, std::string* why) {
+  *unsupported = true;
+  if (seq.T == 0 || K < 1) return cudaSuccess;
+  const bool tc_ok = a.e4m3 && a.H_I == kTcHeads && a.D_I == kTcDim && seq.page_size == kTcPage &&
+                     (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.q) % 16 == 0);
+  // several queries of one sequence share their key reads in the chained plan
+  if (!tc_ok || seq.q_per_seq > 1 || seq.T > env.num_sms) return cudaSuccess;
+  const int cl = a.mx ? fused_cluster<true>(seq, env) : fused_cluster<false>(seq, env);
+  // Measured on GB300: with one or two CTAs per query (a batch of >= num_sms / 4
+  // queries) the fused kernel beats the chained indexer + Top-K (decode batch 64:
+  // 81.0 vs 83.7 us a step); with more CTAs per query the selection's exchanges
+  // between them cost more than the chained plan's score round trip (decode
+  // batch 1: 25.9 vs 25.7 us; batch 4 at 131072 positions: 61.1 vs 55.8 us).
+  if (cl < 1 || cl > kFusedMaxCluster) return cudaSuccess;
+  *unsupported = false;
+  return a.mx ? launch_fused<true>(seq, a, K, idx, cl, env, plan, why, unsupported)
+              : launch_fused<false>(seq, a, K, idx, cl, env, plan, why, unsupported);
+}
 
 cudaError_t launch_indexer(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv& env,
                            std::string* plan, bool* unsupported, std::string* why) {

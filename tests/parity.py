@@ -69,6 +69,16 @@ class Run:
         dsa.check_status()
         return out.float().cpu().numpy(), lse.cpu().numpy(), plan
 
+    def chained_indices(self):
+        """The chained plan's selection made from the separate calls: the GPU's
+        own scores (dsa_indexer_scores), then dsa_topk on them."""
+        s = torch.full((self.wl.T, self.ld), float("-inf"), dtype=torch.float32, device=self.dev)
+        dsa.indexer_scores(self.seq, self.idxr, s)
+        idx = torch.full((self.wl.T, self.wl.K), -7, dtype=torch.int32, device=self.dev)
+        dsa.topk(self.seq, s, self.wl.K, idx)
+        dsa.check_status()
+        return idx.cpu().numpy()
+
     def decode_step(self):
         wl = self.wl
         out = torch.full((wl.T, wl.H, wl.d_v), float("nan"), dtype=self.out_dtype, device=self.dev)
@@ -123,6 +133,14 @@ def check_selection(g_idx, o_scores, q_pos, K, ts=None):
         assert chosen.max() <= q_pos[t]
         kth = np.sort(row)[::-1][min(K, n) - 1]
         assert np.all(row[chosen] >= kth - 1e-3 * np.abs(row).max()), f"row {t}: selection below the K-th score"
+
+
+def step_plan_ok(plan):
+    """The decode step ran the tensor-core kernels: the fused indexer + Top-K
+    kernel, or the chained indexer and Top-K kernels; then the attention."""
+    fused = "indexer_topk_fused" in plan
+    chained = "indexer_tc" in plan and "topk_radix" in plan
+    return (fused or chained) and "attn_tc" in plan
 
 
 def check_attn(g_out, g_lse, o_out, o_lse, dtype):

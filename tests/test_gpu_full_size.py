@@ -108,21 +108,23 @@ def test_full_size_topk_bit_exact_on_oracle_scores(full):
 def test_full_size_decode_step(full):
     wl, run, ts, o_scores = full
     g_out, g_lse, g_idx, plan = _decode_step_rows(run, ts)
-    assert "indexer_tc" in plan and "topk_radix" in plan and "attn_tc" in plan, plan
+    assert P.step_plan_ok(plan), plan
     P.check_selection(g_idx, o_scores, wl.q_pos, wl.K, ts)
     o_out, o_lse = O.sparse_mla_attn(wl, g_idx, ts)
     P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
 
 
 def test_full_size_topk_every_row_in_the_step_launch(dev):
-    """Decode batch 64: the Top-K of all 64 queries in one launch -- the cluster
-    size the decode step and the benchmark use -- bit-exact on the oracle's
-    scores of every row."""
+    """Decode batch 64, all 64 queries: dsa_topk in one launch over the whole
+    batch (the cluster size the benchmark's Top-K stage uses) is bit-exact on the
+    oracle's scores of every row, and the decode step's own selection (the fused
+    plan) equals dsa_topk run on the GPU's scores, bit for bit."""
     wl = W.make("decode_b64", seed=0)
     run = P.Run(wl, dev)
     o_scores = O.indexer_scores(wl)
-    _, _, _, step_plan = run.decode_step()
     g_idx, plan = run.topk(o_scores)
-    launch = plan.split("[", 1)[1]
-    assert "topk_radix" in plan and launch in step_plan, (plan, step_plan)
+    assert "topk_radix[cluster=2," in plan, plan
     P.check_topk_exact(g_idx, O.topk(o_scores, wl.q_pos, wl.K), wl.q_pos, wl.K)
+    _, _, s_idx, step_plan = run.decode_step()
+    np.testing.assert_array_equal(s_idx, run.chained_indices())
+    P.check_selection(s_idx, o_scores, wl.q_pos, wl.K)

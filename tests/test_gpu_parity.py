@@ -87,8 +87,11 @@ def test_attention_on_oracle_selection(case):
 def test_decode_step_end_to_end(case):
     wl, run, o_scores = case
     g_out, g_lse, g_idx, plan = run.decode_step()
-    assert "indexer_tc" in plan and "topk_radix" in plan and "attn_tc" in plan, plan
+    assert P.step_plan_ok(plan), plan
     P.check_selection(g_idx, o_scores, wl.q_pos, wl.K)
+    if "indexer_topk_fused" in plan:
+        # the fused plan selects exactly what the chained plan selects
+        np.testing.assert_array_equal(g_idx, run.chained_indices())
     o_out, o_lse = O.sparse_mla_attn(wl, g_idx)
     P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
 
@@ -320,3 +323,41 @@ def test_bounded_wait_runs_out_and_the_next_step_is_clean(dev, name, over):
     P.check_selection(g_idx, o_scores, wl.q_pos, wl.K)
     o_out, o_lse = O.sparse_mla_attn(wl, g_idx)
     P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
+
+
+@pytest.mark.parametrize("name,over,cluster", [
+    ("decode_b64", dict(ctx_range=(1000, 3000), B=40, K=256), 2),        # two CTAs per query
+    ("decode_b64", dict(ctx_range=(100, 5000), B=80, K=512), 1),         # one CTA per query, rows with n <= K
+    ("decode_b1", dict(ctx=[20000] * 40, K=2048), 2),                    # 10000 keys per CTA
+    ("decode_b4_long", dict(ctx=[9000] * 40, B=40, K=2048), 2),          # FP8 latent rows
+    ("decode_b64", dict(ctx_range=(300, 3000), B=50, K=256, idx_dtype="mx_e4m3"), 2),   # MXFP8 keys
+])
+def test_fused_decode_plan(dev, name, over, cluster):
+    """The fused plan (indexer scores kept in shared memory, Top-K selected in the
+    same kernel by the CTAs of a cluster per query): its selection equals the
+    chained plan's bit for bit, meets the end-to-end rule against the oracle, and
+    the attention on it matches the oracle."""
+    wl = W.make(name, seed=21, **over)
+    run = P.Run(wl, dev)
+    g_out, g_lse, g_idx, plan = run.decode_step()
+    m = re.search(r"indexer_topk_fused<[a-z0-9]+>\[cluster=(\d+)", plan)
+    assert m and int(m.group(1)) == cluster, plan
+    np.testing.assert_array_equal(g_idx, run.chained_indices())
+    ts = list(range(0, wl.T, max(1, wl.T // 8)))           # oracle rows: a spread sample
+    o_scores = O.indexer_scores(wl, ts)
+    P.check_selection(g_idx[ts], o_scores, wl.q_pos, wl.K, ts)
+    o_out, o_lse = O.sparse_mla_attn(wl, g_idx[ts], ts)
+    P.check_attn(g_out[ts], g_lse[ts], o_out, o_lse, wl.mla_dtype)
+
+
+def test_fused_plan_ties_across_cluster_slices(dev):
+    """Index keys made identical for every position: every score ties, so the
+    selection must be positions 0..K-1 in every plan (ties to the lower
+    position across the CTAs of the cluster)."""
+    wl = W.make("decode_b1", seed=22, ctx=[9000] * 40, K=1000)
+    wl.k_i = np.tile(wl.k_i[:1], (wl.k_i.shape[0], 1))
+    wl.k_i_scale = np.full_like(wl.k_i_scale, wl.k_i_scale[0])
+    run = P.Run(wl, dev)
+    _, _, g_idx, plan = run.decode_step()
+    assert "indexer_topk_fused<e4m3>[cluster=2" in plan, plan
+    np.testing.assert_array_equal(g_idx, np.tile(np.arange(wl.K, dtype=np.int32), (wl.T, 1)))
