@@ -367,3 +367,77 @@ def device_tensors(wl: Workload, device, copies: int = 1) -> dict:
     if copies == 1:
         return one()
     return [one() for _ in range(copies)]
+
+
+# ----------------------------------------------------------------------------- the indexer prolog
+
+@dataclasses.dataclass
+class PrologWorkload:
+    """New tokens for the indexer prolog: hidden states x [T, d_model] and query
+    latents x_q [T, d_q] (bf16 bit patterns), the projection weights (bf16 bit
+    patterns, output x input), the key normalisation's gamma / beta (fp32), and a
+    paged index-key cache the new keys are written into."""
+    name: str
+    B: int
+    T: int
+    q_seq: np.ndarray          # int32 [T]
+    q_pos: np.ndarray          # int32 [T] position of each new token
+    block_table: np.ndarray    # int32 [B, pages]
+    page_size: int
+    cache_rows: int
+    max_ctx: int
+    d_model: int
+    d_q: int
+    H_I: int
+    D_I: int
+    x: np.ndarray              # uint16 [T, d_model]
+    x_q: np.ndarray            # uint16 [T, d_q]
+    w_q: np.ndarray            # uint16 [H_I * D_I, d_q]
+    w_k: np.ndarray            # uint16 [D_I, d_model]
+    w_w: np.ndarray            # uint16 [H_I, d_model]
+    gamma: np.ndarray          # float32 [D_I]
+    beta: np.ndarray           # float32 [D_I]
+    k_cache: np.ndarray        # uint8 [cache_rows, D_I] (earlier keys)
+    k_scale: np.ndarray        # float32 [cache_rows]
+
+
+PROLOG_SPECS = {
+    # sizes of the projections are not on the pages: a 7168-wide hidden state and
+    # a 1536-wide query latent, 64 indexer heads of 128 (the decode configurations)
+    "prolog_decode_b64": dict(B=64, q_len=1, ctx=4096, d_model=7168, d_q=1536, H_I=64, D_I=128),
+    "prolog_prefill_4k": dict(B=1, q_len=4096, ctx=4096, d_model=7168, d_q=1536, H_I=64, D_I=128),
+    "prolog_tiny": dict(B=2, q_len=3, ctx=70, d_model=64, d_q=32, H_I=2, D_I=8),
+}
+
+
+def make_prolog(name: str, seed: int = 0, **over) -> PrologWorkload:
+    """Seeded draws: x, x_q ~ N(0, 1); W_q ~ N(0, 1/d_q) (so q ~ N(0, 1));
+    W_k ~ N(0, 1/d_model); W_w ~ N(0, 1/(H_I d_model)) (so w ~ N(0, 1/H_I), the
+    head weights of the decode configurations); gamma ~ 1 + N(0, 0.1^2),
+    beta ~ N(0, 0.1^2); earlier cache keys random E4M3 codes with scale 0.01.
+    Sequence b's new tokens sit at positions ctx - q_len .. ctx - 1; pages are a
+    seeded permutation of the pool."""
+    sp = dict(PROLOG_SPECS[name])
+    sp.update(over)
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    B, q_len, ctx, P = sp["B"], sp["q_len"], sp["ctx"], PAGE_SIZE
+    dm, dq, H, D = sp["d_model"], sp["d_q"], sp["H_I"], sp["D_I"]
+    npg = (ctx + P - 1) // P
+    perm = torch.randperm(B * npg, generator=g).numpy().astype(np.int32)
+    block_table = perm.reshape(B, npg)
+    T = B * q_len
+    q_seq = np.repeat(np.arange(B, dtype=np.int32), q_len)
+    q_pos = np.tile(np.arange(ctx - q_len, ctx, dtype=np.int32), B)
+    x = _bf16_bits(torch.randn((T, dm), generator=g))
+    x_q = _bf16_bits(torch.randn((T, dq), generator=g))
+    w_q = _bf16_bits(torch.randn((H * D, dq), generator=g) / math.sqrt(dq))
+    w_k = _bf16_bits(torch.randn((D, dm), generator=g) / math.sqrt(dm))
+    w_w = _bf16_bits(torch.randn((H, dm), generator=g) / math.sqrt(H * dm))
+    gamma = (1.0 + 0.1 * torch.randn((D,), generator=g)).numpy().astype(np.float32)
+    beta = (0.1 * torch.randn((D,), generator=g)).numpy().astype(np.float32)
+    rows = B * npg * P
+    k_cache = torch.randint(0, 126, (rows, D), generator=g, dtype=torch.int32).numpy().astype(np.uint8)
+    k_scale = np.full(rows, 0.01, dtype=np.float32)
+    return PrologWorkload(name=name, B=B, T=T, q_seq=q_seq, q_pos=q_pos, block_table=block_table, page_size=P,
+                          cache_rows=rows, max_ctx=ctx, d_model=dm, d_q=dq, H_I=H, D_I=D, x=x, x_q=x_q,
+                          w_q=w_q, w_k=w_k, w_w=w_w, gamma=gamma, beta=beta, k_cache=k_cache, k_scale=k_scale)

@@ -380,3 +380,58 @@ def latent_cache_append(block_table, page_size, q_seq, q_pos, kv_new_bits, cache
         rope = bits[t, d_latent:d_latent + d_rope].astype("<u2").tobytes()
         cache[row, d_latent + 16:d_latent + 16 + len(rope)] = np.frombuffer(rope, dtype=np.uint8)
     return cache
+
+
+# ---------------------------------------------------------------------------
+# the indexer prolog: step 1's query, head weights and new key made from the new
+# tokens' hidden states (page "Large Language Model Inference Acceleration in
+# Practice", section 3.2 "Indexer Prolog": query projection, key normalisation
+# with the key-cache update, query quantisation, head-weight projection; the
+# pages give the four steps, not their formulas -- the readings below are the
+# plainest that fit: linear projections, a layer normalisation of the key, and
+# the cache formats' own quantisation rule)
+# ---------------------------------------------------------------------------
+
+LAYERNORM_EPS = 1e-6
+
+
+def project(x_bits, w_bits) -> np.ndarray:
+    """y[t] = W x[t] for every token: x bfloat16 bit patterns [T, d], W bfloat16
+    bit patterns [n, d] (output x input), sums in float64.  Returns float64 [T, n]."""
+    return decode_bf16(x_bits) @ decode_bf16(w_bits).T
+
+
+def layer_norm(v, gamma, beta, eps: float = LAYERNORM_EPS) -> np.ndarray:
+    """Over the last axis: (v - mean) / sqrt(var + eps) * gamma + beta, with the
+    mean and the population variance (mean square deviation) of v; float64."""
+    v = np.asarray(v, dtype=np.float64)
+    mean = v.mean(axis=-1, keepdims=True)
+    var = ((v - mean) ** 2).mean(axis=-1, keepdims=True)
+    return (v - mean) / np.sqrt(var + eps) * np.asarray(gamma, np.float64) + np.asarray(beta, np.float64)
+
+
+def indexer_prolog(pl) -> dict:
+    """The prolog of one batch of new tokens `pl` (dsa_workloads.PrologWorkload):
+
+    * q[t] = W_q x_q[t] as H_I heads of D_I values; each (t, h) vector quantised
+      by the cache formats' rule (quantize_e4m3_row: fp32 scale amax / 448, E4M3
+      codes of the fp32 quotient) -- the indexer query of step 1;
+    * w[t] = W_w x[t] -- the head weights of step 1;
+    * k[t] = layer_norm(W_k x[t], gamma, beta) -- the new index key, quantised
+      and written to the cache row of position q_pos[t] (index_cache_append).
+
+    Values are formed in float64 and rounded to float32 where the rule quantises
+    them.  Returns q (float64 [T, H_I, D_I]), q_codes, q_scale, w (float64
+    [T, H_I]), k (float64 [T, D_I]) and the updated k_cache / k_scale."""
+    T = pl.T
+    q = project(pl.x_q, pl.w_q).reshape(T, pl.H_I, pl.D_I)
+    q_codes = np.empty((T, pl.H_I, pl.D_I), dtype=np.uint8)
+    q_scale = np.empty((T, pl.H_I), dtype=np.float32)
+    for t in range(T):
+        for h in range(pl.H_I):
+            q_codes[t, h], q_scale[t, h] = quantize_e4m3_row(q[t, h].astype(np.float32))
+    w = project(pl.x, pl.w_w)
+    k = layer_norm(project(pl.x, pl.w_k), pl.gamma, pl.beta)
+    k_cache, k_scale = index_cache_append(pl.block_table, pl.page_size, pl.q_seq, pl.q_pos,
+                                          k.astype(np.float32), pl.k_cache, pl.k_scale)
+    return dict(q=q, q_codes=q_codes, q_scale=q_scale, w=w, k=k, k_cache=k_cache, k_scale=k_scale)

@@ -543,3 +543,97 @@ def test_cache_append_oracle_mx_keys_and_tile128_rows():
     others = np.ones(128, bool)
     others[row] = False
     assert np.array_equal(out[others], cache0[others])
+
+
+# --------------------------------------------------------------------------- the indexer prolog
+
+def _bits(a):
+    return W._bf16_bits(torch.as_tensor(np.asarray(a, dtype=np.float32)))
+
+
+def test_project_one_hot_weight_and_brute_force():
+    """W = e_i e_j^T picks input j into output i; on random tiny inputs the
+    projection equals a pure-Python triple loop over the bf16 values."""
+    rng = np.random.default_rng(0)
+    x = _bits(rng.standard_normal((3, 5)))
+    w = np.zeros((4, 5), np.float32)
+    w[2, 3] = 1.0
+    y = O.project(x, _bits(w))
+    xv = O.decode_bf16(x)
+    assert np.array_equal(y[:, 2], xv[:, 3]) and np.count_nonzero(y[:, [0, 1, 3]]) == 0
+    wr = _bits(rng.standard_normal((4, 5)))
+    wv = O.decode_bf16(wr)
+    y = O.project(x, wr)
+    for t in range(3):
+        for i in range(4):
+            acc = 0.0
+            for j in range(5):
+                acc += float(xv[t, j]) * float(wv[i, j])
+            assert abs(y[t, i] - acc) <= 1e-12 * (1 + abs(acc))
+
+
+def test_layer_norm_hand_example_and_invariants():
+    v = np.array([1.0, 2.0, 3.0, 4.0])
+    # mean 2.5, population variance 1.25
+    ref = (v - 2.5) / math.sqrt(1.25)
+    assert np.allclose(O.layer_norm(v, np.ones(4), np.zeros(4), eps=0.0), ref, rtol=0, atol=1e-15)
+    assert np.allclose(O.layer_norm(v, 2 * np.ones(4), np.ones(4), eps=0.0), 2 * ref + 1, rtol=0, atol=1e-15)
+    rng = np.random.default_rng(1)
+    u = rng.standard_normal((5, 128)) * 3 + 7
+    n = O.layer_norm(u, np.ones(128), np.zeros(128))
+    assert np.allclose(n.mean(axis=1), 0, atol=1e-12)
+    assert np.allclose((n ** 2).mean(axis=1), 1 / (1 + O.LAYERNORM_EPS / u.var(axis=1)), rtol=1e-12)
+    # a constant vector normalises to beta (its deviation is zero)
+    assert np.allclose(O.layer_norm(np.full(8, 3.0), np.ones(8), np.arange(8.0)), np.arange(8.0))
+
+
+def test_indexer_prolog_brute_force_tiny():
+    """Every output of the prolog from pure-Python loops over the bf16 inputs:
+    the projections, the layer normalisation of the key, the per-(token, head)
+    quantisation of the query (the quantisation rule is pinned on its own above),
+    and the cache row of each new key."""
+    pl = W.make_prolog("prolog_tiny", seed=3)
+    r = O.indexer_prolog(pl)
+    xv, xq = O.decode_bf16(pl.x), O.decode_bf16(pl.x_q)
+    wq, wk, ww = O.decode_bf16(pl.w_q), O.decode_bf16(pl.w_k), O.decode_bf16(pl.w_w)
+    for t in range(pl.T):
+        for h in range(pl.H_I):
+            qv = [sum(float(wq[h * pl.D_I + d, j]) * float(xq[t, j]) for j in range(pl.d_q)) for d in range(pl.D_I)]
+            assert np.allclose(r["q"][t, h], qv, rtol=1e-12, atol=1e-12)
+            amax = max(abs(np.float32(v)) for v in qv)
+            assert r["q_scale"][t, h] == np.float32(np.float32(amax) / np.float32(448.0))
+            codes, _ = O.quantize_e4m3_row(np.asarray(qv, np.float32))
+            assert np.array_equal(r["q_codes"][t, h], codes)
+        for h in range(pl.H_I):
+            wv = sum(float(ww[h, j]) * float(xv[t, j]) for j in range(pl.d_model))
+            assert abs(r["w"][t, h] - wv) <= 1e-12 * (1 + abs(wv))
+        kv = [sum(float(wk[d, j]) * float(xv[t, j]) for j in range(pl.d_model)) for d in range(pl.D_I)]
+        mean = sum(kv) / pl.D_I
+        var = sum((v - mean) ** 2 for v in kv) / pl.D_I
+        kn = [(v - mean) / math.sqrt(var + 1e-6) * float(pl.gamma[d]) + float(pl.beta[d]) for d, v in enumerate(kv)]
+        assert np.allclose(r["k"][t], kn, rtol=1e-12, atol=1e-12)
+        b, p = int(pl.q_seq[t]), int(pl.q_pos[t])
+        row = int(pl.block_table[b, p // pl.page_size]) * pl.page_size + p % pl.page_size
+        codes, scale = O.quantize_e4m3_row(np.asarray(kn, np.float32))
+        assert np.array_equal(r["k_cache"][row], codes) and r["k_scale"][row] == scale
+    # rows of no new token are untouched
+    touched = {int(pl.block_table[int(b), int(p) // pl.page_size]) * pl.page_size + int(p) % pl.page_size
+               for b, p in zip(pl.q_seq, pl.q_pos)}
+    others = np.array(sorted(set(range(pl.cache_rows)) - touched))
+    assert np.array_equal(r["k_cache"][others], pl.k_cache[others])
+    assert np.array_equal(r["k_scale"][others], pl.k_scale[others])
+
+
+def test_indexer_prolog_quantisation_error_bound():
+    """Dequantised query and key stay within half an E4M3 step (relative 2**-4
+    of the value, or half the smallest subnormal step) of the exact values --
+    the error bound of round-to-nearest into E4M3."""
+    pl = W.make_prolog("prolog_tiny", seed=4, H_I=4, D_I=16, d_model=96)
+    r = O.indexer_prolog(pl)
+    deq = O.decode_e4m3(r["q_codes"]) * r["q_scale"].astype(np.float64)[..., None]
+    ulp_half = np.maximum(np.abs(r["q"]) * 2.0 ** -4, r["q_scale"].astype(np.float64)[..., None] * 2.0 ** -10)
+    assert np.all(np.abs(deq - r["q"]) <= ulp_half * (1 + 1e-6))
+    rows = [int(pl.block_table[int(b), int(p) // 64]) * 64 + int(p) % 64 for b, p in zip(pl.q_seq, pl.q_pos)]
+    kd = O.decode_e4m3(r["k_cache"][rows]) * r["k_scale"][rows].astype(np.float64)[:, None]
+    kh = np.maximum(np.abs(r["k"]) * 2.0 ** -4, r["k_scale"][rows].astype(np.float64)[:, None] * 2.0 ** -10)
+    assert np.all(np.abs(kd - r["k"]) <= kh * (1 + 1e-6))
