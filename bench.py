@@ -199,7 +199,7 @@ class ClockSampler:
 
 def kernel_count(plan: str) -> int:
     return sum(plan.count(k) for k in ("indexer_tc", "indexer_generic", "topk_radix", "topk_fused", "attn_tc",
-                                       "attn_generic", "attn_combine"))
+                                       "attn_generic", "attn_combine", "prolog_proj", "prolog_epilogue"))
 
 
 def traffic_from_profiles(kernel_file: str, workload: str):
@@ -502,6 +502,68 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
     return res
 
 
+# ----------------------------------------------------------------------------- the indexer prolog
+
+def measure_prolog(torch, dsa, W, name, steps, warmup, peaks, dev, clk):
+    """dsa_indexer_prolog on one batch of new tokens: exactly `steps` timed calls
+    over rotated input copies (graph replays), with the roofline of the
+    projection: weights + inputs + outputs against HBM for a decode batch, the
+    projections' flops against the BF16 peak for a prefill batch."""
+    pl = W.make_prolog(name, seed=0)
+    HD = pl.H_I * pl.D_I
+    w_bytes = 2 * (HD * pl.d_q + (pl.D_I + pl.H_I) * pl.d_model)
+    in_bytes = 2 * pl.T * (pl.d_model + pl.d_q)
+    out_bytes = pl.T * (HD + 4 * pl.H_I + 4 * pl.H_I + pl.D_I + 4)
+    flops = 2 * pl.T * (HD * pl.d_q + (pl.D_I + pl.H_I) * pl.d_model)
+    step_bytes = w_bytes + in_bytes + out_bytes
+    R = max(1, min(16, math.ceil(2 * L2_BYTES / step_bytes) + 1))
+    stream = torch.cuda.Stream()
+    runs = []
+    for _ in range(R):
+        d = W.prolog_device_tensors(pl, dev)
+        seq, pro = dsa.Seq(**d["seq"]), dsa.Prolog(**d["prolog"])
+        runs.append(dict(seq=seq, pro=pro, k_cache=d["k_cache"], k_scale=d["k_scale"],
+                         q=torch.empty((pl.T, pl.H_I, pl.D_I), dtype=torch.uint8, device=dev),
+                         qs=torch.empty((pl.T, pl.H_I), dtype=torch.float32, device=dev),
+                         w=torch.empty((pl.T, pl.H_I), dtype=torch.float32, device=dev)))
+    ws = torch.empty(dsa.indexer_prolog_workspace_size(runs[0]["seq"], runs[0]["pro"]), dtype=torch.uint8, device=dev)
+
+    def call(r):
+        dsa.indexer_prolog(r["seq"], r["pro"], r["q"], r["qs"], r["w"], r["k_cache"], r["k_scale"], ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        call(runs[0])
+    plan = dsa.last_plan()
+    dsa.check_status(stream)
+    g_full = capture(torch, call, runs, stream)
+    g_rem = capture(torch, call, runs[:steps % R], stream) if steps % R else None
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(warmup / R))):
+            g_full.replay()
+    torch.cuda.synchronize()
+    t, win = time_replays(torch, [g_full] * (steps // R) + ([g_rem] if g_rem is not None else []), stream)
+    clk.window(*win)
+    dsa.check_status(stream)
+    us = 1e6 * t / steps
+    if pl.T >= 1024:
+        ach = flops / (us * 1e-6) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16_tflops"], "peak_src": "measured bf16 burst"}
+    else:
+        ach = step_bytes / (us * 1e-6) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / peaks["hbm_gbs"], "peak_src": peaks["src"] + " hbm copy"}
+    roof["traffic"] = traffic_from_profiles("prolog.cu", name)
+    res = {"workload": f"{name}: {pl.T} new tokens, hidden {pl.d_model}, query latent {pl.d_q}, "
+                       f"indexer {pl.H_I}x{pl.D_I}; bf16 inputs and weights",
+           "us_per_call": us, "tok_s": pl.T / (us * 1e-6), "steps": steps, "plan": plan,
+           "algorithmic_bytes": step_bytes, "flops": flops, "roofline": roof,
+           "l2": f"{R} rotated input copies"}
+    del runs, ws, g_full, g_rem
+    torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -518,6 +580,7 @@ def main():
                     help="length of the sustained run per workload")
     ap.add_argument("--oracle-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prolog", action="store_true", help="skip the indexer-prolog measurement")
     ap.add_argument("--stage", choices=["indexer", "topk", "attn", "step"], default=None,
                     help="profiling mode: run this stage --reps times on one input copy and exit "
                          "(no timing, no JSON line); for ncu captures")
@@ -591,6 +654,9 @@ def main():
         for nm in names:
             results[nm] = measure_workload(torch, np, dsa, W, nm, args.steps, warmup, args.min_seconds, peaks, dev,
                                            clk, 0.0)
+        prolog = {} if args.no_prolog or args.workload else {
+            nm: measure_prolog(torch, dsa, W, nm, args.steps, warmup, peaks, dev, clk)
+            for nm in ("prolog_decode_b64", "prolog_prefill_4k")}
     clocks = clk.summary()
     # the CPU oracle after the GPU work (host cores only; not inside any timed window)
     if oracle_s > 0:
@@ -618,6 +684,7 @@ def main():
         "clocks": clocks,
         "peaks": {k: peaks[k] for k in ("hbm_gbs", "bf16_tflops", "fp8_tflops", "fp8_src", "src")},
         "workloads": results,
+        "prolog": prolog,
     }
     if "cpu_baseline" in head:
         line["cpu_baseline"] = head["cpu_baseline"]

@@ -27,6 +27,7 @@ EXPORTED = ("dsa_abi_version", "dsa_status_string", "dsa_last_error", "dsa_last_
             "dsa_sparse_mla_attn", "dsa_decode_workspace_size", "dsa_decode_step",
             "dsa_decode_step_static_ws", "dsa_index_cache_append", "dsa_index_cache_append_mx",
             "dsa_latent_cache_append", "dsa_debug_withhold_arrival",
+            "dsa_indexer_prolog_workspace_size", "dsa_indexer_prolog",
             "dsa_check_status")
 STATIC_WORKSPACE_BYTES = 32 << 20   # DSA_STATIC_WORKSPACE_BYTES
 
@@ -48,6 +49,13 @@ class MlaDesc(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("d_latent", ctypes.c_int32), ("d_rope", ctypes.c_int32),
                 ("dtype", ctypes.c_int), ("q", ctypes.c_void_p), ("kv_cache", ctypes.c_void_p),
                 ("row_bytes", ctypes.c_int64), ("softmax_scale", ctypes.c_float)]
+
+
+class PrologDesc(ctypes.Structure):
+    _fields_ = [("d_model", ctypes.c_int32), ("d_q", ctypes.c_int32), ("H_I", ctypes.c_int32),
+                ("D_I", ctypes.c_int32), ("x", ctypes.c_void_p), ("x_q", ctypes.c_void_p), ("w_q", ctypes.c_void_p),
+                ("w_k", ctypes.c_void_p), ("w_w", ctypes.c_void_p), ("gamma", ctypes.c_void_p),
+                ("beta", ctypes.c_void_p)]
 
 
 class DSAError(RuntimeError):
@@ -77,6 +85,8 @@ def _load() -> ctypes.CDLL:
         "dsa_index_cache_append_mx": (C, [P, ctypes.c_int32, C, P, P, P, P]),
         "dsa_latent_cache_append": (C, [P, P, P, P, P]),
         "dsa_debug_withhold_arrival": (C, [ctypes.c_int32, ctypes.c_uint64]),
+        "dsa_indexer_prolog_workspace_size": (ctypes.c_size_t, [P, P]),
+        "dsa_indexer_prolog": (C, [P, P, P, P, P, P, P, P, ctypes.c_size_t, P]),
         "dsa_check_status": (C, [P]),
     }
     for name, (res, args) in sig.items():
@@ -198,6 +208,39 @@ class Mla(_CachedDesc):
         row_bytes = self.kv_cache.stride(0) * self.kv_cache.element_size()
         return MlaDesc(self.q.shape[1], self.d_latent, self.d_rope, dt, _ptr(self.q), _ptr(self.kv_cache),
                        row_bytes, self.softmax_scale)
+
+
+@dataclasses.dataclass
+class Prolog(_CachedDesc):
+    """Indexer prolog inputs; see dsa_prolog_desc_t (bf16 tensors, weights as
+    [output, input])."""
+    x: torch.Tensor                    # [T, d_model] bf16
+    x_q: torch.Tensor                  # [T, d_q] bf16
+    w_q: torch.Tensor                  # [H_I * D_I, d_q] bf16
+    w_k: torch.Tensor                  # [D_I, d_model] bf16
+    w_w: torch.Tensor                  # [H_I, d_model] bf16
+    gamma: torch.Tensor                # [D_I] fp32
+    beta: torch.Tensor                 # [D_I] fp32
+
+    def _build_desc(self) -> PrologDesc:
+        return PrologDesc(self.x.shape[1], self.x_q.shape[1], self.w_w.shape[0], self.w_k.shape[0], _ptr(self.x),
+                          _ptr(self.x_q), _ptr(self.w_q), _ptr(self.w_k), _ptr(self.w_w), _ptr(self.gamma),
+                          _ptr(self.beta))
+
+
+def indexer_prolog_workspace_size(seq: Seq, pro: Prolog) -> int:
+    s, d = seq.desc(), pro.desc()
+    return _lib.dsa_indexer_prolog_workspace_size(ctypes.byref(s), ctypes.byref(d))
+
+
+def indexer_prolog(seq: Seq, pro: Prolog, q_codes: torch.Tensor, q_scale: torch.Tensor, w: torch.Tensor,
+                   k_cache: torch.Tensor, k_scale: torch.Tensor, workspace: torch.Tensor, stream=None) -> None:
+    """The indexer's query (E4M3 codes + per-head scales), head weights and the new
+    tokens' normalised keys (quantised into k_cache / k_scale at their positions)."""
+    s, d = seq.desc(), pro.desc()
+    _check(_lib.dsa_indexer_prolog(ctypes.byref(s), ctypes.byref(d), _ptr(q_codes), _ptr(q_scale), _ptr(w),
+                                   _ptr(k_cache), _ptr(k_scale), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def indexer_scores(seq: Seq, idx: Indexer, scores: torch.Tensor, stream=None) -> torch.Tensor:

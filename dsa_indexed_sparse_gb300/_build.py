@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa.so")
-SOURCES = ("api.cu", "indexer.cu", "topk.cu", "attn.cu", "static_ws.cu", "cache_append.cu")
+SOURCES = ("api.cu", "indexer.cu", "topk.cu", "attn.cu", "static_ws.cu", "cache_append.cu", "prolog.cu")
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
 
 

@@ -510,6 +510,67 @@ dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_de
   }
 }
 
+namespace {
+dsa_status_t check_prolog(const dsa_seq_desc_t* seq, const dsa_prolog_desc_t* pd, dsa::SeqArgs* s) {
+  dsa_status_t st = check_seq(seq, s);
+  if (st != DSA_OK) return st;
+  if (!pd) return fail(DSA_ERR_INVALID_ARG, "prolog descriptor is NULL");
+  if (pd->D_I != 128) return fail(DSA_ERR_UNSUPPORTED, "the prolog kernels need D_I == 128");
+  if (pd->H_I < 1 || pd->H_I > 128) return fail(DSA_ERR_UNSUPPORTED, "the prolog kernels need 1 <= H_I <= 128");
+  if (pd->d_model < 64 || pd->d_model % 64 != 0 || pd->d_q < 64 || pd->d_q % 64 != 0)
+    return fail(DSA_ERR_UNSUPPORTED, "d_model and d_q must be positive multiples of 64");
+  return DSA_OK;
+}
+}  // namespace
+
+size_t dsa_indexer_prolog_workspace_size(const dsa_seq_desc_t* seq, const dsa_prolog_desc_t* pd) {
+  try {
+    dsa::SeqArgs s;
+    if (check_prolog(seq, pd, &s) != DSA_OK) return 0;
+    dsa::LaunchEnv env;
+    if (make_env(nullptr, &env) != DSA_OK) return 0;
+    return dsa::prolog_workspace_bytes(s.T, pd->H_I, pd->d_model, pd->d_q, env.num_sms);
+  } catch (...) {
+    return 0;
+  }
+}
+
+dsa_status_t dsa_indexer_prolog(const dsa_seq_desc_t* seq, const dsa_prolog_desc_t* pd, uint8_t* q_codes,
+                                float* q_scale, float* w, uint8_t* k_cache, float* k_scale, void* workspace,
+                                size_t workspace_bytes, dsa_stream_t stream) {
+  try {
+    dsa::SeqArgs s;
+    dsa_status_t st = check_prolog(seq, pd, &s);
+    if (st != DSA_OK) return st;
+    if (s.T > 0 && (!pd->x || !pd->x_q || !pd->w_q || !pd->w_k || !pd->w_w || !pd->gamma || !pd->beta ||
+                    !q_codes || !q_scale || !w || !k_cache || !k_scale))
+      return fail(DSA_ERR_INVALID_ARG, "prolog inputs and outputs must be non-NULL");
+    if (!aligned16(pd->x) || !aligned16(pd->x_q) || !aligned16(pd->w_q) || !aligned16(pd->w_k) ||
+        !aligned16(pd->w_w) || !aligned16(q_codes) || !aligned16(q_scale) || !aligned16(w) || !aligned16(k_cache) ||
+        !aligned16(k_scale))
+      return fail(DSA_ERR_INVALID_ARG, "prolog pointers must be 16-byte aligned");
+    dsa::LaunchEnv env;
+    if ((st = make_env(stream, &env)) != DSA_OK) return st;
+    const size_t need = dsa::prolog_workspace_bytes(s.T, pd->H_I, pd->d_model, pd->d_q, env.num_sms);
+    if (s.T > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need)) {
+      char buf[128];
+      snprintf(buf, sizeof(buf), "prolog workspace: need %zu bytes, 16-byte aligned", need);
+      return fail(DSA_ERR_WORKSPACE, buf);
+    }
+    const dsa::PrologArgs a{pd->d_model, pd->d_q, pd->H_I, pd->x, pd->x_q, pd->w_q, pd->w_k, pd->w_w, pd->gamma,
+                            pd->beta, q_codes, q_scale, w, k_cache, k_scale};
+    std::string plan, why;
+    bool unsupported = false;
+    const cudaError_t e = dsa::launch_prolog(s, a, workspace, env, &plan, &unsupported, &why);
+    if (unsupported) return fail(DSA_ERR_UNSUPPORTED, why);
+    if (e != cudaSuccess) return cuda_fail(e, "prolog launch");
+    g_last_plan = plan;
+    return DSA_OK;
+  } catch (...) {
+    return fail(DSA_ERR_CUDA, "unexpected host exception");
+  }
+}
+
 dsa_status_t dsa_debug_withhold_arrival(int32_t enable, uint64_t wait_limit_ns) {
   if (enable && (wait_limit_ns < 1000ull || wait_limit_ns > dsa::kWaitLimitNs))
     return fail(DSA_ERR_INVALID_ARG, "wait_limit_ns must be in [1 us, 1 s]");
@@ -523,7 +584,8 @@ dsa_status_t dsa_check_status(dsa_stream_t stream) {
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     const uint32_t f = dsa_status_read_clear_indexer() | dsa_status_read_clear_topk() |
-                       dsa_status_read_clear_attn() | dsa_status_read_clear_cache();
+                       dsa_status_read_clear_attn() | dsa_status_read_clear_cache() |
+                       dsa_status_read_clear_prolog();
     if (f == 0) return DSA_OK;
     if (f == 0xFFFFFFFFu) return fail(DSA_ERR_CUDA, "could not read the device status word");
     std::string msg = "device flags:";

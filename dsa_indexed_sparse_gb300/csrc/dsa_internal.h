@@ -114,6 +114,26 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// The indexer prolog (projections, key normalisation, quantisation, key append).
+struct PrologArgs {
+  int32_t d_model, d_q, H_I;
+  const void* x;        // bf16 [T, d_model]
+  const void* x_q;      // bf16 [T, d_q]
+  const void* w_q;      // bf16 [H_I * 128, d_q]
+  const void* w_k;      // bf16 [128, d_model]
+  const void* w_w;      // bf16 [H_I, d_model]
+  const float* gamma;   // [128]
+  const float* beta;    // [128]
+  uint8_t* q_codes;     // [T, H_I, 128]
+  float* q_scale;       // [T, H_I]
+  float* w;             // [T, H_I]
+  uint8_t* k_cache;     // [cache_rows, 128]
+  float* k_scale;       // [cache_rows]
+};
+size_t prolog_workspace_bytes(int T, int H_I, int d_model, int d_q, int num_sms);
+cudaError_t launch_prolog(const SeqArgs& seq, const PrologArgs& a, void* workspace, const LaunchEnv& env,
+                          std::string* plan, bool* unsupported, std::string* why);
+
 // Cache writers (the new tokens' index keys / latent rows into the paged caches).
 cudaError_t launch_index_append(const SeqArgs& seq, int32_t D, bool bf16_in, const void* k_new, uint8_t* k_cache,
                                 float* k_scale, const LaunchEnv& env, std::string* plan);
@@ -154,3 +174,4 @@ uint32_t dsa_status_read_clear_indexer();
 uint32_t dsa_status_read_clear_topk();
 uint32_t dsa_status_read_clear_attn();
 uint32_t dsa_status_read_clear_cache();
+uint32_t dsa_status_read_clear_prolog();

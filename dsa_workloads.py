@@ -441,3 +441,17 @@ def make_prolog(name: str, seed: int = 0, **over) -> PrologWorkload:
     return PrologWorkload(name=name, B=B, T=T, q_seq=q_seq, q_pos=q_pos, block_table=block_table, page_size=P,
                           cache_rows=rows, max_ctx=ctx, d_model=dm, d_q=dq, H_I=H, D_I=D, x=x, x_q=x_q,
                           w_q=w_q, w_k=w_k, w_w=w_w, gamma=gamma, beta=beta, k_cache=k_cache, k_scale=k_scale)
+
+
+def prolog_device_tensors(pl: PrologWorkload, device) -> dict:
+    """A prolog workload's arrays on ``device``, grouped as the binding's Seq and
+    Prolog records plus the key cache they update."""
+    def t(a, dtype=None):
+        x = torch.from_numpy(np.ascontiguousarray(a))
+        return (x.view(dtype) if dtype is not None else x).to(device)
+    bf = lambda a: t(a.view(np.int16), torch.bfloat16)
+    seq = dict(q_seq=t(pl.q_seq), q_pos=t(pl.q_pos), block_table=t(pl.block_table), max_ctx=pl.max_ctx,
+               cache_rows=pl.cache_rows, page_size=pl.page_size, q_per_seq=0)
+    pro = dict(x=bf(pl.x), x_q=bf(pl.x_q), w_q=bf(pl.w_q), w_k=bf(pl.w_k), w_w=bf(pl.w_w), gamma=t(pl.gamma),
+               beta=t(pl.beta))
+    return dict(seq=seq, prolog=pro, k_cache=t(pl.k_cache), k_scale=t(pl.k_scale))

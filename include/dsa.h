@@ -274,6 +274,48 @@ dsa_status_t dsa_latent_cache_append(const dsa_seq_desc_t* seq, const dsa_mla_de
  * outside the range. */
 dsa_status_t dsa_debug_withhold_arrival(int32_t enable, uint64_t wait_limit_ns);
 
+/* The indexer prolog -- step 1's inputs made from the new tokens.
+ * "Large Language Model Inference Acceleration in Practice", section 3.2
+ * "Indexer Prolog": before the indexer runs, a query projection, a key
+ * normalisation with the key-cache update, a query quantisation and a
+ * head-weight projection (run there on three streams; here the projection tiles
+ * of all three weights are one grid).  The pages give the steps, not formulas;
+ * this library computes, per new token t (bf16 inputs and weights, fp32 sums):
+ *   q[t] = W_q x_q[t]  as H_I heads of D_I = 128 values, each head quantised to
+ *          E4M3 with scale amax / 448 (1 for an all-zero head), round to nearest
+ *          even, saturated: q_codes [T, H_I, 128] (uint8) and q_scale [T, H_I]
+ *          (fp32) -- dsa_indexer_desc_t's q and q_scale for DSA_E4M3;
+ *   w[t] = W_w x[t]  -> w [T, H_I] fp32, the head weights;
+ *   k[t] = (v - mean(v)) / sqrt(var(v) + 1e-6) * gamma + beta,  v = W_k x[t]
+ *          (population variance over the 128 values), quantised like a query
+ *          head and written to the index-key cache row of position q_pos[t] of
+ *          sequence q_seq[t] (k_cache [cache_rows, 128], k_scale [cache_rows]),
+ *          as dsa_index_cache_append does.  Bad positions / pages are skipped and
+ *          flagged (dsa_check_status).
+ * Layouts: x bf16 [T, d_model], x_q bf16 [T, d_q], W_q bf16 [H_I * 128, d_q],
+ * W_k bf16 [128, d_model], W_w bf16 [H_I, d_model] (row = output feature,
+ * input dims contiguous), gamma / beta fp32 [128].  D_I must be 128, 1 <= H_I
+ * <= 128, d_model and d_q multiples of 64 (else DSA_ERR_UNSUPPORTED).  The call
+ * uses a caller-provided workspace of dsa_indexer_prolog_workspace_size() bytes
+ * (the fp32 projections). */
+typedef struct dsa_prolog_desc {
+  int32_t d_model;           /* hidden size (multiple of 64)                       */
+  int32_t d_q;               /* query latent size (multiple of 64)                 */
+  int32_t H_I;               /* indexer heads (1 .. 128)                           */
+  int32_t D_I;               /* indexer head dim (128)                             */
+  const void* x;             /* device bf16 [T, d_model]                           */
+  const void* x_q;           /* device bf16 [T, d_q]                               */
+  const void* w_q;           /* device bf16 [H_I * D_I, d_q]                       */
+  const void* w_k;           /* device bf16 [D_I, d_model]                         */
+  const void* w_w;           /* device bf16 [H_I, d_model]                         */
+  const float* gamma;        /* device fp32 [D_I]                                  */
+  const float* beta;         /* device fp32 [D_I]                                  */
+} dsa_prolog_desc_t;
+size_t dsa_indexer_prolog_workspace_size(const dsa_seq_desc_t* seq, const dsa_prolog_desc_t* pd);
+dsa_status_t dsa_indexer_prolog(const dsa_seq_desc_t* seq, const dsa_prolog_desc_t* pd, uint8_t* q_codes,
+                                float* q_scale, float* w, uint8_t* k_cache, float* k_scale, void* workspace,
+                                size_t workspace_bytes, dsa_stream_t stream);
+
 /* Synchronises `stream`, then returns and clears the device status word:
  * DSA_OK, DSA_ERR_TIMEOUT or DSA_ERR_DEVICE_CHECK (dsa_last_error() names the
  * flags), or DSA_ERR_CUDA if the stream itself reports an error. */
