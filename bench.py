@@ -574,14 +574,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workloads", default=",".join(DEFAULT_WORKLOADS),
                     help="comma-separated workloads; the first is the headline line")
-    ap.add_argument("--workload", default=None, choices=sorted(DESCRIPTIONS),
+    ap.add_argument("--workload", default=None,
                     help="one workload only (also the workload of --stage and --impl reference)")
     ap.add_argument("--min-seconds", type=float, default=0.25,
                     help="length of the sustained run per workload")
     ap.add_argument("--oracle-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prolog", action="store_true", help="skip the indexer-prolog measurement")
-    ap.add_argument("--stage", choices=["indexer", "topk", "attn", "step"], default=None,
+    ap.add_argument("--stage", choices=["indexer", "topk", "attn", "step", "prolog"], default=None,
                     help="profiling mode: run this stage --reps times on one input copy and exit "
                          "(no timing, no JSON line); for ncu captures")
     ap.add_argument("--reps", type=int, default=3)
@@ -597,7 +597,7 @@ def main():
     import dsa_workloads as W
     names = [args.workload] if args.workload else [s for s in args.workloads.split(",") if s]
     for nm in names:
-        if nm not in DESCRIPTIONS:
+        if nm not in DESCRIPTIONS and not (args.stage == "prolog" and nm in W.PROLOG_SPECS):
             ap.error(f"unknown workload {nm}")
 
     if args.impl == "reference":
@@ -634,6 +634,22 @@ def main():
     peaks = load_peaks()
     dev = torch.device("cuda:0")
     torch.cuda.set_device(dev)
+    if args.stage == "prolog":
+        # profiling mode for the indexer prolog: --reps calls on one input copy
+        nm = args.workload if args.workload in W.PROLOG_SPECS else "prolog_decode_b64"
+        pl = W.make_prolog(nm, seed=0)
+        d = W.prolog_device_tensors(pl, dev)
+        seq, pro = dsa.Seq(**d["seq"]), dsa.Prolog(**d["prolog"])
+        q = torch.empty((pl.T, pl.H_I, pl.D_I), dtype=torch.uint8, device=dev)
+        qs = torch.empty((pl.T, pl.H_I), dtype=torch.float32, device=dev)
+        w = torch.empty((pl.T, pl.H_I), dtype=torch.float32, device=dev)
+        ws = torch.empty(dsa.indexer_prolog_workspace_size(seq, pro), dtype=torch.uint8, device=dev)
+        for _ in range(args.reps):
+            dsa.indexer_prolog(seq, pro, q, qs, w, d["k_cache"], d["k_scale"], ws)
+        torch.cuda.synchronize()
+        dsa.check_status()
+        print(f"profiled prolog x{args.reps} on {nm}: {dsa.last_plan()}")
+        return 0
     if args.stage:
         nm = names[0]
         if args.prefill_len is not None:
