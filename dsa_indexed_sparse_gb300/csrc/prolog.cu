@@ -16,7 +16,7 @@
 //
 // Two kernels:
 //  * prolog_proj_kernel -- tcgen05 bf16 GEMM, swap-AB: a CTA multiplies 128 rows
-//    of one weight (output features; M) by up to 128 tokens (N), over a range of
+//    of one weight (output features; M) by up to 256 tokens (N), over a range of
 //    64-wide K atoms (split-K when the batch is small: each K range writes its
 //    own fp32 slice of the workspace, no atomics and no zeroing); weights and
 //    tokens arrive by 2-D TMA (128-byte swizzle), the accumulator lives in TMEM.
@@ -37,16 +37,18 @@ namespace {
 
 constexpr int kPM = 128;           // output features per CTA (UMMA M)
 constexpr int kPAtom = 64;         // bf16 elements per K atom (one 128-byte swizzle row)
-constexpr int kPMaxN = 128;        // tokens per CTA at most (UMMA N)
+constexpr int kPMaxN = 256;        // tokens per CTA at most (UMMA N)
 constexpr int kPStages = 4;
 constexpr int kPThreads = 192;     // warp 0 TMA, warp 1 MMA, warps 2-5 epilogue
 constexpr int kPABytes = kPM * kPAtom * 2;             // 16 KB
-constexpr int kPBBytes = kPMaxN * kPAtom * 2;          // 16 KB
-constexpr int kPStageBytes = kPABytes + kPBBytes;
-constexpr int kPOffBar = kPStages * kPStageBytes;
 constexpr int kPNumBars = 2 * kPStages + 2;            // full, empty, accfull, drain
-constexpr int kPOffMisc = kPOffBar + kPNumBars * 8;
-constexpr int kPSmemBytes = kPOffMisc + 64 + 1024;     // + re-alignment slack
+// Shared memory of a CTA for n_tok tokens: kPStages x (weight tile + token tile),
+// barriers, misc words, re-alignment slack.  Sized by the token tile so that two
+// CTAs share an SM at small batches (two independent issue chains per SM).
+__host__ __device__ constexpr int prolog_stage_bytes(int n_tok) { return kPABytes + n_tok * kPAtom * 2; }
+__host__ __device__ constexpr int prolog_smem_bytes(int n_tok) {
+  return kPStages * prolog_stage_bytes(n_tok) + kPNumBars * 8 + 64 + 1024;
+}
 
 struct ProjJob {
   int32_t n_feat;      // output features of this weight
@@ -61,23 +63,25 @@ struct ProjJob {
 
 struct ProjParams {
   int32_t T;
-  int32_t n_tok;       // tokens per CTA (multiple of 16, <= 128)
+  int32_t n_tok;       // tokens per CTA (multiple of 16, <= 256)
+  uint32_t tmem_cols;  // power of two >= n_tok, >= 32
   int32_t t_tiles;
   ProjJob job[3];      // 0: query (W_q, x_q), 1: key (W_k, x), 2: head weights (W_w, x)
   uint64_t wait_limit_ns;
 };
 
-__global__ void __launch_bounds__(kPThreads, 1)
+__global__ void __launch_bounds__(kPThreads, 2)
     prolog_proj_kernel(const __grid_constant__ CUtensorMap wq_map, const __grid_constant__ CUtensorMap wk_map,
                        const __grid_constant__ CUtensorMap ww_map, const __grid_constant__ CUtensorMap xq_map,
                        const __grid_constant__ CUtensorMap x_map, ProjParams p) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPOffBar);
+  const int stage_bytes = prolog_stage_bytes(p.n_tok);
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kPStages * stage_bytes);
   uint64_t* empty = full + kPStages;
   uint64_t* accfull = empty + kPStages;
   uint64_t* drain = accfull + 1;
-  uint32_t* misc = reinterpret_cast<uint32_t*>(sm + kPOffMisc);
+  uint32_t* misc = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint64_t wlim = p.wait_limit_ns;
@@ -114,7 +118,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
     tma_prefetch_desc(bmap);
   }
   if (warp == 1) {
-    tmem_alloc(misc, kPMaxN);
+    tmem_alloc(misc, p.tmem_cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -134,7 +138,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) {
-        uint8_t* a = sm + st * kPStageBytes;
+        uint8_t* a = sm + st * stage_bytes;
         mbar_arrive_expect_tx(&full[st], bytes);
         tma_load_2d(a, amap, &full[st], (a0 + i) * kPAtom, f0);
         tma_load_2d(a + kPABytes, bmap, &full[st], (a0 + i) * kPAtom, t0);
@@ -154,8 +158,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
       const bool ok = mbar_wait(&full[st], (i / kPStages) & 1, &g_status_prolog, abort_flag, wlim);
       if (!__all_sync(0xffffffffu, ok)) break;
       tc_fence_after();
-      const uint64_t da = make_sdesc(smem_u32(sm + st * kPStageBytes), 16, 1024, kLayoutSw128);
-      const uint64_t db = make_sdesc(smem_u32(sm + st * kPStageBytes + kPABytes), 16, 1024, kLayoutSw128);
+      const uint64_t da = make_sdesc(smem_u32(sm + st * stage_bytes), 16, 1024, kLayoutSw128);
+      const uint64_t db = make_sdesc(smem_u32(sm + st * stage_bytes + kPABytes), 16, 1024, kLayoutSw128);
       if (elect_one()) {
 #pragma unroll
         for (int k = 0; k < kPAtom / 16; ++k)   // 16 bf16 = 32 bytes per step
@@ -200,7 +204,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, kPMaxN);
+    tmem_dealloc(tmem, p.tmem_cols);
   }
 }
 
@@ -313,10 +317,10 @@ __global__ void __launch_bounds__(32 * kEpiHeads) prolog_epilogue_kernel(EpiPara
   if (lane == 0) p.k_scale[row] = scale;
 }
 
-int split_for(int tiles, int atoms, int num_sms) {
-  // enough CTAs for one wave, at least 4 K atoms (256 values) each
+int split_for(int tiles, int atoms, int slots) {
+  // enough CTAs to fill the resident slots, at least 4 K atoms (256 values) each
   int s = 1;
-  while (s * 2 <= atoms / 4 && static_cast<int64_t>(tiles) * s * 2 <= num_sms) s *= 2;
+  while (s * 2 <= atoms / 4 && static_cast<int64_t>(tiles) * s * 2 <= slots) s *= 2;
   return s;
 }
 
@@ -329,11 +333,15 @@ struct PrologPlan {
 };
 PrologPlan prolog_plan(int T, int H_I, int d_model, int d_q, int num_sms) {
   PrologPlan pp;
+  // tokens per CTA: a 64-wide K atom's MMAs (128 x n_tok x 64) per ~0.4 us of
+  // issue steps; the widest tile for large batches
   pp.n_tok = T >= kPMaxN ? kPMaxN : ((T + 15) / 16) * 16;
   pp.t_tiles = (T + pp.n_tok - 1) / pp.n_tok;
   const int q_tiles = H_I;   // 128 features = one head per tile
-  pp.split_q = split_for(q_tiles * pp.t_tiles, d_q / kPAtom, num_sms);
-  pp.split_kw = split_for(2 * pp.t_tiles, d_model / kPAtom, num_sms);
+  // two CTAs per SM when their stages fit twice in shared memory (small batches)
+  const int slots = (2 * prolog_smem_bytes(pp.n_tok) <= 227 * 1024 ? 2 : 1) * num_sms;
+  pp.split_q = split_for(q_tiles * pp.t_tiles, d_q / kPAtom, slots);
+  pp.split_kw = split_for(2 * pp.t_tiles, d_model / kPAtom, slots);
   pp.q_bytes = (static_cast<size_t>(pp.split_q) * T * H_I * 128 * 4 + 255) / 256 * 256;
   pp.kw_bytes = (static_cast<size_t>(pp.split_kw) * T * 256 * 4 + 255) / 256 * 256;
   return pp;
@@ -371,6 +379,7 @@ cudaError_t launch_prolog(const SeqArgs& seq, const PrologArgs& a, void* workspa
   ProjParams p{};
   p.T = T;
   p.n_tok = n_tok;
+  p.tmem_cols = n_tok <= 32 ? 32u : (n_tok <= 64 ? 64u : (n_tok <= 128 ? 128u : 256u));
   p.t_tiles = t_tiles;
   const int q_atoms = a.d_q / kPAtom, x_atoms = a.d_model / kPAtom;
   const int q_tiles = HD / kPM;
@@ -383,11 +392,11 @@ cudaError_t launch_prolog(const SeqArgs& seq, const PrologArgs& a, void* workspa
   const int grid = p.job[0].first_cta + q_tiles * t_tiles * p.job[0].split;
   uint32_t dbg_withhold = 0;
   debug_wait_state(&p.wait_limit_ns, &dbg_withhold);
-  const cudaError_t attr = ensure_smem_limit(reinterpret_cast<const void*>(prolog_proj_kernel), kPSmemBytes,
-                                             env.device);
+  const cudaError_t attr = ensure_smem_limit(reinterpret_cast<const void*>(prolog_proj_kernel),
+                                             prolog_smem_bytes(kPMaxN), env.device);
   if (attr != cudaSuccess) return attr;
-  cudaError_t e = launch_kernel(prolog_proj_kernel, dim3(grid), dim3(kPThreads), kPSmemBytes, env.stream, false, 1,
-                                wq_map, wk_map, ww_map, xq_map, x_map, p);
+  cudaError_t e = launch_kernel(prolog_proj_kernel, dim3(grid), dim3(kPThreads), prolog_smem_bytes(n_tok), env.stream,
+                                false, 1, wq_map, wk_map, ww_map, xq_map, x_map, p);
   if (e != cudaSuccess) return e;
   EpiParams ep{seq, a.H_I, yq, pp.split_q, ykw, pp.split_kw, a.gamma, a.beta, a.q_codes, a.q_scale, a.w,
                a.k_cache, a.k_scale};
