@@ -190,11 +190,14 @@ def test_topk_ties_and_boundaries(dev, K):
 
 def test_topk_long_history_cluster_and_uncached(dev):
     """Long histories are split over a cluster of CTAs; beyond the clusters'
-    shared-memory key cache the scores are re-read from L2."""
+    shared-memory key cache the scores are re-read from L2.  The all-equal row
+    puts every key of every CTA's slice on the threshold (ties across the whole
+    cluster, taken in position order)."""
     rng = np.random.default_rng(5)
     L = 70000
-    scores = np.stack([rng.standard_normal(L), rng.integers(0, 50, L).astype(np.float64)]).astype(np.float32)
-    plan = _topk_run(dev, scores, [L - 1, 60001], 2048)
+    scores = np.stack([rng.standard_normal(L), rng.integers(0, 50, L).astype(np.float64),
+                       np.zeros(L)]).astype(np.float32)
+    plan = _topk_run(dev, scores, [L - 1, 60001, L - 1], 2048)
     m = re.search(r"cluster=(\d+),smem", plan)
     assert m and int(m.group(1)) > 1, plan
     L = 400000
