@@ -6,7 +6,6 @@
 
 #include <atomic>
 #include <cstdio>
-#include <cstring>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -171,6 +170,38 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device) {
   const cudaError_t r = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   done.push_back(Entry{kernel, device, r});
   return r;
+}
+
+bool cluster_fits(const void* kernel, int device, int cl, int threads, size_t smem) {
+  struct Entry {
+    const void* kernel;
+    int device, cl, threads;
+    size_t smem;
+    bool fits;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> done;
+  std::lock_guard<std::mutex> lock(mu);
+  for (const Entry& e : done)
+    if (e.kernel == kernel && e.device == device && e.cl == cl && e.threads == threads && e.smem == smem)
+      return e.fits;
+  if (cl > 8) static_cast<void>(cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(cl));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeClusterDimension;
+  attr.val.clusterDim.x = static_cast<unsigned>(cl);
+  attr.val.clusterDim.y = 1;
+  attr.val.clusterDim.z = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  const bool fits = cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) == cudaSuccess && n >= 1;
+  cudaGetLastError();
+  done.push_back(Entry{kernel, device, cl, threads, smem, fits});
+  return fits;
 }
 
 namespace {

@@ -149,6 +149,10 @@ void set_last_error(const std::string& msg);
 // must be current), once per (kernel, device); later calls return the first
 // call's result.  Thread-safe.
 cudaError_t ensure_smem_limit(const void* kernel, int bytes, int device);
+// Whether one cluster of `cl` CTAs of `kernel` (`threads` threads, `smem` bytes of
+// dynamic shared memory each) can be resident on `device`; the occupancy query is
+// made once per distinct argument set (and allows non-portable sizes above 8).
+bool cluster_fits(const void* kernel, int device, int cl, int threads, size_t smem);
 
 // The failure-detection testing aid (dsa_debug_withhold_arrival): the wait
 // bound the kernels use and whether the attention producer withholds an arrival.

@@ -804,12 +804,12 @@ cudaError_t launch_tc(const SeqArgs& seq, const IndexerArgs& a, const LaunchEnv&
 // (up to 16 CTAs per query, non-portable cluster size), and enough CTAs that a
 // slice's keys fit kFusedMaxKeys.  Returns CL, or 0 when the plan does not apply.
 template <bool kMx>
-int fused_cluster(const SeqArgs& seq, const LaunchEnv& env) {
+int fused_cluster(const SeqArgs& seq, const LaunchEnv& env, int max_cl) {
   const int need = (seq.max_ctx + kFusedMaxKeys - 1) / kFusedMaxKeys;
   int cl = 1;
   while (cl < 16 && static_cast<int64_t>(seq.T) * cl * 2 <= env.num_sms) cl *= 2;
   cl = std::max(cl, need);
-  if (cl > 16) return 0;
+  if (cl > 16 || cl > max_cl) return 0;
   // every cluster of the launch resident at once is not required, but a cluster
   // of this size must fit on the GPU
   using C = TcCfg<1, kMx>;
@@ -819,22 +819,7 @@ int fused_cluster(const SeqArgs& seq, const LaunchEnv& env) {
   if (ensure_smem_limit(reinterpret_cast<const void*>(kern),
                         C::kOffKeys + kFusedMaxKeys * 4 + 1024, env.device) != cudaSuccess)
     return 0;
-  static_cast<void>(cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1));
-  while (cl > 1) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(seq.T * cl);
-    cfg.blockDim = dim3(TcWarps<1, kMx>::kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = static_cast<unsigned>(cl);
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess && n >= 1) break;
-    cudaGetLastError();
+  while (cl > 1 && !cluster_fits(reinterpret_cast<const void*>(kern), env.device, cl, TcWarps<1, kMx>::kThreads, smem)) {
     cl /= 2;
     if (cl < need) return 0;
   }
@@ -875,7 +860,7 @@ cudaError_t launch_decode_fused(const SeqArgs& seq, const IndexerArgs& a, int32_
                      (reinterpret_cast<uintptr_t>(a.k) % 16 == 0) && (reinterpret_cast<uintptr_t>(a.q) % 16 == 0);
   // several queries of one sequence share their key reads in the chained plan
   if (!tc_ok || seq.q_per_seq > 1 || seq.T > env.num_sms) return cudaSuccess;
-  const int cl = a.mx ? fused_cluster<true>(seq, env) : fused_cluster<false>(seq, env);
+  const int cl = a.mx ? fused_cluster<true>(seq, env, kFusedMaxCluster) : fused_cluster<false>(seq, env, kFusedMaxCluster);
   // Measured on GB300: with one or two CTAs per query (a batch of >= num_sms / 4
   // queries) the fused kernel beats the chained indexer + Top-K (decode batch 64:
   // 81.0 vs 83.7 us a step); with more CTAs per query the selection's exchanges
