@@ -712,12 +712,23 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 #pragma unroll
       for (int w = 0; w < C::kProducers; ++w)
         vmask |= static_cast<uint64_t>(mask16[st * C::kProducers + w]) << (w * C::kRows);
-      float mloc = -INFINITY;
+      // logits scaled in pairs (packed fp32 multiplies); the row maximum over four
+      // independent partial maxima (short dependency chains)
+      // (FP8 rows: scalar, as their register budget is tighter)
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < kBR48; ++i) {
-        x[i] = ((vmask >> i) & 1u) ? x[i] * sl2 : -INFINITY;
-        mloc = fmaxf(mloc, x[i]);
+      for (int i = 0; i < kBR48; i += 2) {
+        if constexpr (kFp8) {
+          x[i] *= sl2;
+          x[i + 1] *= sl2;
+        } else {
+          mul2(x[i], x[i + 1], x[i], x[i + 1], sl2, sl2);
+        }
+        x[i] = ((vmask >> i) & 1u) ? x[i] : -INFINITY;
+        x[i + 1] = ((vmask >> (i + 1)) & 1u) ? x[i + 1] : -INFINITY;
+        mq[(i >> 1) & 3] = fmaxf(mq[(i >> 1) & 3], fmaxf(x[i], x[i + 1]));
       }
+      const float mloc = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
       // P V_{j-1} is done once it has freed its stage: empty[(j-1) mod S] in the
       // phase of tile j-1 (the phase before it completed when tile j-1 was
       // loaded, the one after needs P_{j-1+S}, so a parity wait cannot alias)
@@ -751,11 +762,27 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       const float msub = (m == -INFINITY) ? 0.f : m;
       float psum = 0.f, psum32 = 0.f;
       uint32_t pk[kBR48 / 2];
+      if constexpr (!kFp8) {
+        // bf16 rows: packed subtract and sums over pairs, two pairs of running sums
+        // each of the rounded weights (what P V multiplies) and of the exact ones
+        float sr[4] = {0.f, 0.f, 0.f, 0.f}, se[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < kBR48 / 2; ++i) {
-        const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
-        psum32 += p0 + p1;
-        if constexpr (kFp8) {
+        for (int i = 0; i < kBR48 / 2; ++i) {
+          float d0, d1;
+          add2(d0, d1, x[2 * i], x[2 * i + 1], -msub, -msub);
+          const float p0 = fast_exp2(d0), p1 = fast_exp2(d1);
+          const int a = 2 * (i & 1);
+          add2(se[a], se[a + 1], se[a], se[a + 1], p0, p1);
+          pk[i] = pack_bf16x2(p0, p1);
+          add2(sr[a], sr[a + 1], sr[a], sr[a + 1], __uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u));
+        }
+        psum = (sr[0] + sr[1]) + (sr[2] + sr[3]);
+        psum32 = (se[0] + se[1]) + (se[2] + se[3]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kBR48 / 2; ++i) {
+          const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
+          psum32 += p0 + p1;
           // P V runs on the unscaled codes: the row scale is folded into P, and
           // the denominator takes the rounded weights divided back by the scale
           const float s0 = row_scale[st * kBR48 + 2 * i], s1 = row_scale[st * kBR48 + 2 * i + 1];
@@ -763,11 +790,6 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           pk[i] = *reinterpret_cast<uint32_t*>(&v);
           const float2 back = __bfloat1622float2(v);
           psum += (s0 > 0.f ? back.x / s0 : 0.f) + (s1 > 0.f ? back.y / s1 : 0.f);
-        } else {
-          __nv_bfloat162 v = __floats2bfloat162_rn(p0, p1);
-          pk[i] = *reinterpret_cast<uint32_t*>(&v);
-          const float2 back = __bfloat1622float2(v);
-          psum += back.x + back.y;
         }
       }
       l += psum;

@@ -406,6 +406,15 @@ __device__ __forceinline__ void mul2(float& r0, float& r1, float x0, float x1, f
       : "=f"(r0), "=f"(r1)
       : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
 }
+// (r0, r1) = (x0 + y0, x1 + y1): two IEEE fp32 adds in one packed instruction
+// (PTX add.rn.f32x2).
+__device__ __forceinline__ void add2(float& r0, float& r1, float x0, float x1, float y0, float y1) {
+  asm("{\n\t.reg .b64 rx, ry, rr;\n\t"
+      "mov.b64 rx, {%2, %3};\n\tmov.b64 ry, {%4, %5};\n\t"
+      "add.rn.f32x2 rr, rx, ry;\n\tmov.b64 {%0, %1}, rr;\n\t}"
+      : "=f"(r0), "=f"(r1)
+      : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
