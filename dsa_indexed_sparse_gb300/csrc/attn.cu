@@ -712,23 +712,25 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 #pragma unroll
       for (int w = 0; w < C::kProducers; ++w)
         vmask |= static_cast<uint64_t>(mask16[st * C::kProducers + w]) << (w * C::kRows);
-      // logits scaled in pairs (packed fp32 multiplies); the row maximum over four
-      // independent partial maxima (short dependency chains)
-      // (FP8 rows: scalar, as their register budget is tighter)
+      // Rows that select nothing are set to -inf (the selects skipped when every
+      // row of the tile is valid: CTA-uniform); the row maximum is taken over four
+      // independent partial maxima of three-input maxes.  bf16 rows keep the
+      // logits unscaled here: fl(x * s) is monotone in x, so the maximum of the
+      // scaled logits is the scaled maximum, and the exponent below is one packed
+      // fma x * s - m.  FP8 rows scale them first (scalar: a tighter register budget).
+      if constexpr (kFp8) {
+#pragma unroll
+        for (int i = 0; i < kBR48; ++i) x[i] *= sl2;
+      }
+      if (vmask != (1ull << kBR48) - 1u) {
+#pragma unroll
+        for (int i = 0; i < kBR48; ++i) x[i] = ((vmask >> i) & 1u) ? x[i] : -INFINITY;
+      }
       float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int i = 0; i < kBR48; i += 2) {
-        if constexpr (kFp8) {
-          x[i] *= sl2;
-          x[i + 1] *= sl2;
-        } else {
-          mul2(x[i], x[i + 1], x[i], x[i + 1], sl2, sl2);
-        }
-        x[i] = ((vmask >> i) & 1u) ? x[i] : -INFINITY;
-        x[i + 1] = ((vmask >> (i + 1)) & 1u) ? x[i + 1] : -INFINITY;
-        mq[(i >> 1) & 3] = fmaxf(mq[(i >> 1) & 3], fmaxf(x[i], x[i + 1]));
-      }
-      const float mloc = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      for (int i = 0; i < kBR48; i += 2) mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], x[i], x[i + 1]);
+      const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      const float mloc = kFp8 ? mx : mx * sl2;
       // P V_{j-1} is done once it has freed its stage: empty[(j-1) mod S] in the
       // phase of tile j-1 (the phase before it completed when tile j-1 was
       // loaded, the one after needs P_{j-1+S}, so a parity wait cannot alias)
@@ -763,13 +765,14 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       float psum = 0.f, psum32 = 0.f;
       uint32_t pk[kBR48 / 2];
       if constexpr (!kFp8) {
-        // bf16 rows: packed subtract and sums over pairs, two pairs of running sums
-        // each of the rounded weights (what P V multiplies) and of the exact ones
+        // bf16 rows: exponents x * s - m as packed fmas, sums over pairs, two pairs
+        // of running sums each of the rounded weights (what P V multiplies) and of
+        // the exact ones
         float sr[4] = {0.f, 0.f, 0.f, 0.f}, se[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < kBR48 / 2; ++i) {
-          float d0, d1;
-          add2(d0, d1, x[2 * i], x[2 * i + 1], -msub, -msub);
+          float d0 = -msub, d1 = -msub;
+          fma2(d0, d1, x[2 * i], x[2 * i + 1], sl2, sl2);
           const float p0 = fast_exp2(d0), p1 = fast_exp2(d1);
           const int a = 2 * (i & 1);
           add2(se[a], se[a + 1], se[a], se[a + 1], p0, p1);

@@ -406,6 +406,12 @@ __device__ __forceinline__ void mul2(float& r0, float& r1, float x0, float x1, f
       : "=f"(r0), "=f"(r1)
       : "f"(x0), "f"(x1), "f"(y0), "f"(y1));
 }
+// max(a, b, c) in one instruction (PTX three-input max.f32).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 // (r0, r1) = (x0 + y0, x1 + y1): two IEEE fp32 adds in one packed instruction
 // (PTX add.rn.f32x2).
 __device__ __forceinline__ void add2(float& r0, float& r1, float x0, float x1, float y0, float y1) {
