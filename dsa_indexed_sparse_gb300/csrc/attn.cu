@@ -260,8 +260,9 @@ struct T48 {
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kQSmemAtoms * kH * 128;
   static constexpr int kOffMask = kOffKV + kStages * kTile48Bytes;     // uint16 [stages][producers]
-  static constexpr int kOffScale = kOffMask + 128;                      // float [stages][48] (FP8 rows)
-  static constexpr int kOffBar = kOffScale + (kFp8 ? kStages * kBR48 * 4 : 0);
+  // FP8 rows: float [stages][48] row scales, then float [stages][48] their reciprocals
+  static constexpr int kOffScale = kOffMask + 128;
+  static constexpr int kOffBar = kOffScale + (kFp8 ? 2 * kStages * kBR48 * 4 : 0);
   // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull
   // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull, drain
   static constexpr int kNumBars = 3 * kStages + 8;
@@ -338,6 +339,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(misc + 1);
   volatile uint16_t* mask16 = reinterpret_cast<volatile uint16_t*>(sm + C::kOffMask);   // [stage][warp]
   volatile float* row_scale = reinterpret_cast<volatile float*>(sm + C::kOffScale);    // [stage][48], FP8 rows
+  volatile float* row_rcp = row_scale + S * kBR48;                                     // 1 / scale (0 for none)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x & 1;
@@ -503,7 +505,10 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (lane == 0) mask16[st * C::kProducers + pw] = static_cast<uint16_t>(bits);
-      if (kFp8 && lane < kRows) row_scale[st * kBR48 + pw * kRows + lane] = my_scale;
+      if (kFp8 && lane < kRows) {
+        row_scale[st * kBR48 + pw * kRows + lane] = my_scale;
+        row_rcp[st * kBR48 + pw * kRows + lane] = my_scale > 0.f ? 1.f / my_scale : 0.f;
+      }
       if constexpr (!kFp8 && !kTile) {
 #pragma unroll
         for (int rr = 0; rr < kRows; ++rr) {
@@ -709,9 +714,27 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       tc_fence_before();
       mbar_arrive(&sfree[sb]);
       uint64_t vmask = 0;
+      if constexpr (C::kProducers == 12 && C::kRows == 4) {
+        // bf16 rows: the twelve 4-bit masks as three 8-byte loads (each u16 holds
+        // its warp's bits in its low nibble); a full tile needs no compaction
+        const volatile uint64_t* m64 = reinterpret_cast<const volatile uint64_t*>(mask16 + st * C::kProducers);
+        const uint64_t w0 = m64[0], w1 = m64[1], w2 = m64[2];
+        constexpr uint64_t kAll = 0x000F000F000F000Full;
+        if (((w0 ^ kAll) | (w1 ^ kAll) | (w2 ^ kAll)) == 0) {
+          vmask = (1ull << kBR48) - 1u;
+        } else {
+          auto nib = [](uint64_t w) -> uint64_t {
+            w &= kAll;
+            w = (w | (w >> 12)) & 0x000000FF000000FFull;
+            return (w | (w >> 24)) & 0xFFFFull;
+          };
+          vmask = nib(w0) | (nib(w1) << 16) | (nib(w2) << 32);
+        }
+      } else {
 #pragma unroll
-      for (int w = 0; w < C::kProducers; ++w)
-        vmask |= static_cast<uint64_t>(mask16[st * C::kProducers + w]) << (w * C::kRows);
+        for (int w = 0; w < C::kProducers; ++w)
+          vmask |= static_cast<uint64_t>(mask16[st * C::kProducers + w]) << (w * C::kRows);
+      }
       // Rows that select nothing are set to -inf (the selects skipped when every
       // row of the tile is valid: CTA-uniform); the row maximum is taken over four
       // independent partial maxima of three-input maxes.  bf16 rows keep the
@@ -787,12 +810,13 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
           psum32 += p0 + p1;
           // P V runs on the unscaled codes: the row scale is folded into P, and
-          // the denominator takes the rounded weights divided back by the scale
+          // the denominator takes the rounded weights times the reciprocal scale
+          // (the producers' 1 / scale, 0 for a row without one)
           const float s0 = row_scale[st * kBR48 + 2 * i], s1 = row_scale[st * kBR48 + 2 * i + 1];
           __nv_bfloat162 v = __floats2bfloat162_rn(p0 * s0, p1 * s1);
           pk[i] = *reinterpret_cast<uint32_t*>(&v);
           const float2 back = __bfloat1622float2(v);
-          psum += (s0 > 0.f ? back.x / s0 : 0.f) + (s1 > 0.f ? back.y / s1 : 0.f);
+          psum = fmaf(back.x, row_rcp[st * kBR48 + 2 * i], fmaf(back.y, row_rcp[st * kBR48 + 2 * i + 1], psum));
         }
       }
       l += psum;
