@@ -675,6 +675,9 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     const int h = quarter * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const float sl2 = p.a.softmax_scale * kLog2e;
+    // FP8 rows: the stage's row scales and their reciprocals (shared addresses)
+    const uint32_t scale_addr = smem_u32(sm + C::kOffScale);
+    const uint32_t rcp_addr = scale_addr + S * kBR48 * 4;
     float m = -INFINITY, l = 0.f, l32 = 0.f;
     bool ok = true;
     // P_j goes to stage j mod S, where the latent dims of the other value half were
@@ -700,15 +703,26 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         for (int i = 0; i < kBR48; ++i) x[i] = __uint_as_float(i < 32 ? s0[i & 31] : s1[(i - 32) & 15]);
       }
       if constexpr (kFp8) {
-        // logit = row scale * latent part + rope part
+        // logit = row scale * latent part + rope part (packed fmas; the row scales
+        // as 16-byte shared loads)
 #pragma unroll
         for (int c16 = 0; c16 < kBR48 / 16; ++c16) {
           uint32_t r16[16];
           tmem_ld16(tmem + lane_off + C::kColSr + c16 * 16, r16);
           tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            x[c16 * 16 + i] = fmaf(row_scale[st * kBR48 + c16 * 16 + i], x[c16 * 16 + i], __uint_as_float(r16[i]));
+          for (int q = 0; q < 4; ++q) {
+            const uint4 sc = ld_shared_v4(scale_addr + static_cast<uint32_t>((st * kBR48 + c16 * 16 + 4 * q) * 4));
+            const int i = c16 * 16 + 4 * q;
+            float y0 = __uint_as_float(r16[4 * q]), y1 = __uint_as_float(r16[4 * q + 1]);
+            float y2 = __uint_as_float(r16[4 * q + 2]), y3 = __uint_as_float(r16[4 * q + 3]);
+            fma2(y0, y1, __uint_as_float(sc.x), __uint_as_float(sc.y), x[i], x[i + 1]);
+            fma2(y2, y3, __uint_as_float(sc.z), __uint_as_float(sc.w), x[i + 2], x[i + 3]);
+            x[i] = y0;
+            x[i + 1] = y1;
+            x[i + 2] = y2;
+            x[i + 3] = y3;
+          }
         }
       }
       tc_fence_before();
@@ -737,14 +751,9 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
       }
       // Rows that select nothing are set to -inf (the selects skipped when every
       // row of the tile is valid: CTA-uniform); the row maximum is taken over four
-      // independent partial maxima of three-input maxes.  bf16 rows keep the
-      // logits unscaled here: fl(x * s) is monotone in x, so the maximum of the
-      // scaled logits is the scaled maximum, and the exponent below is one packed
-      // fma x * s - m.  FP8 rows scale them first (scalar: a tighter register budget).
-      if constexpr (kFp8) {
-#pragma unroll
-        for (int i = 0; i < kBR48; ++i) x[i] *= sl2;
-      }
+      // independent partial maxima of three-input maxes.  The logits stay unscaled
+      // here: fl(x * s) is monotone in x, so the maximum of the scaled logits is
+      // the scaled maximum, and the exponent below is one packed fma x * s - m.
       if (vmask != (1ull << kBR48) - 1u) {
 #pragma unroll
         for (int i = 0; i < kBR48; ++i) x[i] = ((vmask >> i) & 1u) ? x[i] : -INFINITY;
@@ -753,7 +762,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 #pragma unroll
       for (int i = 0; i < kBR48; i += 2) mq[(i >> 1) & 3] = fmax3(mq[(i >> 1) & 3], x[i], x[i + 1]);
       const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
-      const float mloc = kFp8 ? mx : mx * sl2;
+      const float mloc = mx * sl2;
       // P V_{j-1} is done once it has freed its stage: empty[(j-1) mod S] in the
       // phase of tile j-1 (the phase before it completed when tile j-1 was
       // loaded, the one after needs P_{j-1+S}, so a parity wait cannot alias)
@@ -805,19 +814,31 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         psum = (sr[0] + sr[1]) + (sr[2] + sr[3]);
         psum32 = (se[0] + se[1]) + (se[2] + se[3]);
       } else {
+        // FP8 rows: P V runs on the unscaled codes, so the row scale is folded into
+        // P, and the denominator takes the rounded weights times the reciprocal
+        // scale (the producers' 1 / scale, 0 for a row without one); packed ops,
+        // scales and reciprocals as 16-byte shared loads, four logits at a time
+        float sr[2] = {0.f, 0.f}, se[2] = {0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < kBR48 / 2; ++i) {
-          const float p0 = fast_exp2(x[2 * i] - msub), p1 = fast_exp2(x[2 * i + 1] - msub);
-          psum32 += p0 + p1;
-          // P V runs on the unscaled codes: the row scale is folded into P, and
-          // the denominator takes the rounded weights times the reciprocal scale
-          // (the producers' 1 / scale, 0 for a row without one)
-          const float s0 = row_scale[st * kBR48 + 2 * i], s1 = row_scale[st * kBR48 + 2 * i + 1];
-          __nv_bfloat162 v = __floats2bfloat162_rn(p0 * s0, p1 * s1);
-          pk[i] = *reinterpret_cast<uint32_t*>(&v);
-          const float2 back = __bfloat1622float2(v);
-          psum = fmaf(back.x, row_rcp[st * kBR48 + 2 * i], fmaf(back.y, row_rcp[st * kBR48 + 2 * i + 1], psum));
+        for (int c4 = 0; c4 < kBR48 / 4; ++c4) {
+          const uint32_t off = static_cast<uint32_t>((st * kBR48 + 4 * c4) * 4);
+          const uint4 sc = ld_shared_v4(scale_addr + off), rc = ld_shared_v4(rcp_addr + off);
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const int i = 2 * c4 + q;   // logit pair
+            float d0 = -msub, d1 = -msub;
+            fma2(d0, d1, x[2 * i], x[2 * i + 1], sl2, sl2);
+            const float p0 = fast_exp2(d0), p1 = fast_exp2(d1);
+            add2(se[0], se[1], se[0], se[1], p0, p1);
+            float w0, w1;
+            mul2(w0, w1, p0, p1, __uint_as_float(q ? sc.z : sc.x), __uint_as_float(q ? sc.w : sc.y));
+            pk[i] = pack_bf16x2(w0, w1);
+            fma2(sr[0], sr[1], __uint_as_float(pk[i] << 16), __uint_as_float(pk[i] & 0xFFFF0000u),
+                 __uint_as_float(q ? rc.z : rc.x), __uint_as_float(q ? rc.w : rc.y));
+          }
         }
+        psum = sr[0] + sr[1];
+        psum32 = se[0] + se[1];
       }
       l += psum;
       l32 += psum32;
