@@ -201,7 +201,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
 // bf16 into the tile; the rope goes by cp.async.
 //
 // MMA warps: warp 12 issues Q K^T_{j+1} (N = 48 rows) as soon as tile j+1 has
-// landed, its logit buffer has been read and P V_{j-1} is queued, so it runs
+// landed and its logit buffer has been read, so it runs
 // during the softmax of tile j; warp 13 issues P V_j (N = 256 value dims) as
 // soon as P_j is written.  (One warp issuing both made a ready P V wait behind the issue
 // of a Q K^T and vice versa: the issuing thread blocks until the tensor pipe
@@ -219,7 +219,7 @@ __device__ __forceinline__ uint32_t sw128_offset(int r, int ch, int rows) {
 // Once Q K^T_j is complete, the 256 latent dims of tile j that this CTA's value
 // half does not use are dead, and the softmax writes P_j there (128 x 48 bf16, 128B-swizzled K-major, the A operand of
 // P V_j), so TMEM holds two logit buffers: Q K^T_{j+1} is issued as soon as
-// tile j+1 lands and P V_{j-1} is queued, without waiting for the softmax to
+// tile j+1 lands, without waiting for the softmax to
 // read S_j, and the tensor pipe does not idle across that hand-off (~700
 // cycles a tile with one buffer).  The third stage hides the gather of a tile
 // behind the work on the other two.  FP8 rows: see the T48 plan below.
@@ -263,9 +263,8 @@ struct T48 {
   // FP8 rows: float [stages][48] row scales, then float [stages][48] their reciprocals
   static constexpr int kOffScale = kOffMask + 128;
   static constexpr int kOffBar = kOffScale + (kFp8 ? 2 * kStages * kBR48 * 4 : 0);
-  // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull
-  // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], pvis[2], ofull, drain
-  static constexpr int kNumBars = 3 * kStages + 8;
+  // barriers: full[S], empty[S], sfull[2], sfree[2], pfull[S], ofull, drain
+  static constexpr int kNumBars = 3 * kStages + 6;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kUsed = kOffMisc + 16;                           // bytes used from the aligned base
   // the dynamic shared-memory base is re-aligned to 1024 B inside the kernel;
@@ -331,8 +330,7 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
   uint64_t* sfull = bars + 2 * S;   // [2] logits ready (per logit buffer)
   uint64_t* sfree = sfull + 2;      // [2] logits read by the softmax (buffer reusable)
   uint64_t* pfull = sfull + 4;      // [S] P of the stage's tile written
-  uint64_t* pvis = pfull + S;       // [2] P V_j issued (alternating by tile)
-  uint64_t* ofull = pvis + 2;       // every MMA done
+  uint64_t* ofull = pfull + S;      // every MMA done
   uint64_t* drain = ofull + 1;      // both issuing warps' MMAs complete (teardown)
   const uint64_t wlim = p.wait_limit_ns;
   uint32_t* misc = reinterpret_cast<uint32_t*>(sm + C::kOffMisc);
@@ -369,7 +367,6 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sfull[i], 1);
       mbar_init(&sfree[i], 128);
-      mbar_init(&pvis[i], 1);
     }
     mbar_init(ofull, 1);
     mbar_init(drain, 2);
@@ -623,11 +620,9 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
         // held by this buffer (S_{j - kSBufs})
         const int sb = j % C::kSBufs;
         if (j >= C::kSBufs && !poll(&sfree[sb], ((j / C::kSBufs) - 1) & 1)) break;
-        // ... and after P V_{j-2}, so that the tensor pipe runs S_{j-1}, P V_{j-2},
-        // S_j, P V_{j-1}, ...: a P V never queues behind two Q K^T, and its stage
-        // is freed as early as it can be (two phases apart on alternating
-        // barriers: P V_j needs S_j, so neither runs ahead of this wait)
-        if (j >= 2 && !poll(&pvis[j & 1], ((j - 2) >> 1) & 1)) break;
+        // (Q K^T_j used to wait for P V_{j-2} to be queued as well; with the
+        // softmax as short as it is now, letting it go as soon as its buffer and
+        // tile are ready measured 0.7 % faster at decode batch 64.)
         if (!poll(&full[j % S], (j / S) & 1)) break;
         tc_fence_after();
         fence_proxy_async_smem();   // the copies that landed are visible to the tensor core
@@ -664,7 +659,6 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
           }
           umma_commit(&empty[st]);
           if (j == ntiles - 1) umma_commit(ofull);
-          mbar_arrive(&pvis[j & 1]);
         }
         __syncwarp();
       }
