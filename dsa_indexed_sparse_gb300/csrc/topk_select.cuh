@@ -66,7 +66,7 @@ __device__ __forceinline__ void cl_wait() { asm volatile("barrier.cluster.wait.a
 constexpr int kSelBins = 2048;
 constexpr int kSelMaxCluster = 16;
 
-struct SelectSmem {
+struct alignas(16) SelectSmem {
   uint32_t bins[2][kSelBins];        // the cluster's histogram, by pass parity (peers push into it)
   uint32_t local[kSelBins];          // this CTA's histogram of the current pass
   uint32_t wred[2][32];              // per-warp partials of the block scans
@@ -184,7 +184,16 @@ __device__ void select_run(SelectSmem* sm, KeyAt key_at, Key4At key4_at, int len
     const int shift = sel_shift(pass);
     const uint32_t mask = sel_mask(pass);
     if (pass > 0) {
-      for (int i = tid; i < len; i += kThreads) {
+      // keys four at a time (the slice starts on a 16-byte boundary), then the tail
+      const int len4 = len & ~3;
+      for (int i = 4 * tid; i < len4; i += 4 * kThreads) {
+        const uint4 k4 = key4_at(i);
+        const uint32_t kk[4] = {k4.x, k4.y, k4.z, k4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if ((kk[e] & pmask) == prefix) atomicAdd(&sm->local[(kk[e] >> shift) & mask], 1u);
+      }
+      for (int i = len4 + tid; i < len; i += kThreads) {
         const uint32_t k = key_at(i);
         if ((k & pmask) == prefix) atomicAdd(&sm->local[(k >> shift) & mask], 1u);
       }
@@ -248,10 +257,27 @@ __device__ void select_run(SelectSmem* sm, KeyAt key_at, Key4At key4_at, int len
   const int wl = ((len + kWarps - 1) / kWarps + 127) & ~127;
   const int wlo = min(len, warp * wl), whi = min(len, wlo + wl);
   uint32_t n_gt = 0, n_eq = 0;
-  for (int i = wlo + lane; i < whi; i += 32) {
-    const uint32_t km = key_at(i) & pmask;
-    n_gt += km > prefix ? 1u : 0u;
-    n_eq += km == prefix ? 1u : 0u;
+  for (int b = wlo; b < whi; b += 128) {   // 128 keys a step, four per lane
+    const int i4 = b + 4 * lane;
+    uint32_t k[4];
+    if (i4 + 3 < whi) {
+      const uint4 v = key4_at(i4);
+      k[0] = v.x;
+      k[1] = v.y;
+      k[2] = v.z;
+      k[3] = v.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) k[e] = i4 + e < whi ? key_at(i4 + e) : 0u;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (i4 + e < whi) {
+        const uint32_t km = k[e] & pmask;
+        n_gt += km > prefix ? 1u : 0u;
+        n_eq += km == prefix ? 1u : 0u;
+      }
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
