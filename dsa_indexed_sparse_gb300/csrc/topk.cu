@@ -25,6 +25,7 @@ namespace {
 
 constexpr int kThreads = 512;
 constexpr int kMaxCluster = 8;          // portable cluster size
+constexpr int kMaxClusterOne = 16;      // non-portable, for a single query
 constexpr int kMinSliceKeys = 1024;     // smallest history slice worth a CTA
 constexpr int kCacheKeys = 48 * 1024;   // shared-memory key cache per CTA (192 KB)
 
@@ -120,13 +121,21 @@ cudaError_t launch_topk(const SeqArgs& seq, const float* scores, int64_t ld, int
   const int want = std::max(1, env.num_sms / seq.T);   // one wave: T x cluster <= SMs
   const int feed = std::max(1, seq.max_ctx / kMinSliceKeys);
   const int fit = (seq.max_ctx + kCacheKeys - 1) / kCacheKeys;
-  const int cl = std::max(1, std::min(kMaxCluster, std::max(std::min(want, feed), fit)));
-  const int slice = ((seq.max_ctx + cl - 1) / cl + 3) & ~3;
-  const bool cached = slice <= kCacheKeys;
-  const size_t smem = cached ? static_cast<size_t>(slice) * 4 : 0;
   const cudaError_t attr_err =
       ensure_smem_limit(reinterpret_cast<const void*>(topk_kernel), kCacheKeys * 4, env.device);
   if (attr_err != cudaSuccess) return attr_err;
+  // A single query may take a non-portable cluster of 16 CTAs when the GPU can
+  // place one (decode batch 1: 0.15 us per step faster than 8 in an A/B; with
+  // four queries 16 was slower, the clusters crowding the attention launched
+  // behind them)
+  int max_cl = kMaxCluster;
+  if (seq.T == 1 && std::min(want, feed) > kMaxCluster &&
+      cluster_fits(reinterpret_cast<const void*>(topk_kernel), env.device, kMaxClusterOne, kThreads, kCacheKeys * 4))
+    max_cl = kMaxClusterOne;
+  const int cl = std::max(1, std::min(max_cl, std::max(std::min(want, feed), fit)));
+  const int slice = ((seq.max_ctx + cl - 1) / cl + 3) & ~3;
+  const bool cached = slice <= kCacheKeys;
+  const size_t smem = cached ? static_cast<size_t>(slice) * 4 : 0;
   TopkArgs a{scores, ld, seq.q_pos, seq.max_ctx, K, idx, cached ? slice : 0, seq.T};
   // Programmatic dependent launch: the clusters are placed as the indexer's CTAs
   // finish (each triggers its dependents when its tiles are done) and wait for
