@@ -920,44 +920,50 @@ __global__ void __launch_bounds__(kT48Threads, 1) attn_tc48_kernel(TcAttnParams 
 
 // Merges row slices: out[t,h,:] = sum_s w_s O_s / sum_s w_s, w_s = exp(lse_s - max_s lse_s);
 // lse = max + log sum_s w_s.  The partials O_s are bf16 rows, each normalised by
-// its own slice's sum.  One CTA of two warps per (query, pair of heads); a warp per
-// head, each lane owning 16 value dims (two 16-byte vectors per slice).  Slices go
-// in batches of 16 whose row loads and LSE loads are all in flight together (one
-// L2 round trip per batch), merged with a running maximum across batches.
-constexpr int kCombineHeads = 2;
-constexpr int kCombineBatch = 16;
-__global__ void __launch_bounds__(32 * kCombineHeads)
+// its own slice's sum.  A CTA takes HPC heads of one query with SW warps per head:
+// warp w of a head takes the slices w, w + SW, w + 2 SW, ..., eight at a time with
+// all of their row and LSE loads in flight together; lane l owns the value dims
+// [8l, 8l + 8) and [256 + 8l, 256 + 8l + 8), so each load instruction reads 512
+// contiguous bytes.  A head's warps meet in shared memory with their running
+// (max, sum, weighted row), and its threads write the output four dims at a time.
+constexpr int kCombineBatch = 8;   // slices per warp per round trip
+template <int SW, int HPC>
+__global__ void __launch_bounds__(32 * SW * HPC)
     attn_combine_kernel(const uint16_t* ws_o, const float* ws_lse, int n_split, int T,
                         __nv_bfloat16* out, float* lse_out) {
   grid_dep_launch();   // the next kernel waits for this grid before it uses out
   grid_dep_wait();
   constexpr int H = kH;
+  __shared__ float s_acc[SW * HPC][16][32];   // [warp][value slot][lane]
+  __shared__ float s_m[SW * HPC], s_l[SW * HPC];
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kCombineHeads + warp;
+  const int hl = warp / SW, sv = warp % SW;   // head within the CTA, slice phase
+  const int h = blockIdx.y * HPC + hl;
   const int64_t th = static_cast<int64_t>(t) * H + h;
   const int64_t slice_stride = static_cast<int64_t>(T) * H * (kDv / 8);   // in 16-byte vectors
-  const uint4* src = reinterpret_cast<const uint4*>(ws_o) + th * (kDv / 8) + 2 * lane;
+  const uint4* src = reinterpret_cast<const uint4*>(ws_o) + th * (kDv / 8) + lane;
   float acc[16];
 #pragma unroll
   for (int k = 0; k < 16; ++k) acc[k] = 0.f;
   float m = -INFINITY, l = 0.f;
-  for (int s0 = 0; s0 < n_split; s0 += kCombineBatch) {
-    const int nb = min(kCombineBatch, n_split - s0);
+  for (int s0 = sv; s0 < n_split; s0 += SW * kCombineBatch) {
+    const int nb = min(kCombineBatch, (n_split - s0 + SW - 1) / SW);   // slices s0 + u*SW, u < nb
     uint4 v[kCombineBatch][2];
 #pragma unroll
     for (int u = 0; u < kCombineBatch; ++u) {
       if (u < nb) {
-        v[u][0] = __ldcs(src + (s0 + u) * slice_stride);
-        v[u][1] = __ldcs(src + (s0 + u) * slice_stride + 1);
+        v[u][0] = __ldcs(src + (s0 + u * SW) * slice_stride);
+        v[u][1] = __ldcs(src + (s0 + u * SW) * slice_stride + kDv / 16);
       }
     }
-    const float ls = lane < nb ? ws_lse[(static_cast<int64_t>(s0 + lane) * T + t) * H + h] : -INFINITY;
+    const float ls =
+        lane < nb ? ws_lse[(static_cast<int64_t>(s0 + lane * SW) * T + t) * H + h] : -INFINITY;
     float mb = ls;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
     const float m_new = fmaxf(m, mb);
-    // previous batches rescaled to the new maximum (all zero while m is -inf)
+    // earlier batches rescaled to the new maximum (all zero while m is -inf)
     const float f = (m == -INFINITY) ? 0.f : __expf(m - m_new);
     const float wl = (ls == -INFINITY) ? 0.f : __expf(ls - m_new);
     float wsum = wl;
@@ -981,14 +987,61 @@ __global__ void __launch_bounds__(32 * kCombineHeads)
       }
     }
   }
-  if (lane == 0 && lse_out) lse_out[th] = l > 0.f ? m + logf(l) : -INFINITY;
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  uint32_t pk[8];
 #pragma unroll
-  for (int k = 0; k < 8; ++k) pk[k] = pack_bf16x2(acc[2 * k] * inv, acc[2 * k + 1] * inv);
-  uint4* dst = reinterpret_cast<uint4*>(out + th * kDv) + 2 * lane;
-  dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-  dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+  for (int k = 0; k < 16; ++k) s_acc[warp][k][lane] = acc[k];
+  if (lane == 0) {
+    s_m[warp] = m;
+    s_l[warp] = l;
+  }
+  __syncthreads();
+  const int w0 = hl * SW;   // the head's first warp
+  float mm = s_m[w0];
+#pragma unroll
+  for (int w = 1; w < SW; ++w) mm = fmaxf(mm, s_m[w0 + w]);
+  float fw[SW], ll = 0.f;
+#pragma unroll
+  for (int w = 0; w < SW; ++w) {
+    fw[w] = (s_m[w0 + w] == -INFINITY) ? 0.f : __expf(s_m[w0 + w] - mm);
+    ll = fmaf(fw[w], s_l[w0 + w], ll);
+  }
+  const int i0 = threadIdx.x - w0 * 32;   // thread within the head's warps
+  if (i0 == 0 && lse_out) lse_out[th] = ll > 0.f ? mm + logf(ll) : -INFINITY;
+  const float inv = ll > 0.f ? 1.f / ll : 0.f;
+  uint2* dst = reinterpret_cast<uint2*>(out + th * kDv);
+  // quad q holds dims [4q, 4q + 4): lane (q mod 64) / 2 of the warps, slots
+  // 8 * (q / 64) + 4 * (q mod 2) .. + 3
+#pragma unroll
+  for (int q = i0; q < kDv / 4; q += 32 * SW) {
+    const int src_lane = (q & 63) >> 1, k0 = 8 * (q >> 6) + 4 * (q & 1);
+    float r[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float x = 0.f;
+#pragma unroll
+      for (int w = 0; w < SW; ++w) x = fmaf(fw[w], s_acc[w0 + w][k0 + c][src_lane], x);
+      r[c] = x * inv;
+    }
+    dst[q] = make_uint2(pack_bf16x2(r[0], r[1]), pack_bf16x2(r[2], r[3]));
+  }
+}
+
+// Launches the slice merge for T queries.  While the (query, head) pairs are no
+// more than the SMs, four warps per head and one head per CTA, so that the loads
+// spread over as many SMs as there are pairs; otherwise two heads per CTA with
+// enough warps per head (1, 2 or 4) that each takes one batch of kCombineBatch
+// slices.
+cudaError_t launch_combine(const uint16_t* ws_o, const float* ws_lse, int n_split, int T,
+                           __nv_bfloat16* out, float* lse_out, const LaunchEnv& env) {
+  const int64_t pairs = static_cast<int64_t>(T) * kH;
+  const int need = (n_split + kCombineBatch - 1) / kCombineBatch;
+#define DSA_COMBINE(SW_, HPC_)                                                                           \
+  launch_kernel(attn_combine_kernel<SW_, HPC_>, dim3(T, kH / (HPC_)), dim3(32 * (SW_) * (HPC_)), 0,      \
+                env.stream, true, 1, ws_o, ws_lse, n_split, T, out, lse_out)
+  if (pairs <= env.num_sms) return DSA_COMBINE(4, 1);
+  if (need > 2) return DSA_COMBINE(4, 2);
+  if (need > 1) return DSA_COMBINE(2, 2);
+  return DSA_COMBINE(1, 2);
+#undef DSA_COMBINE
 }
 
 bool tc_supported(const SeqArgs& seq, const MlaArgs& a) {
@@ -1065,10 +1118,8 @@ cudaError_t launch_attn(const SeqArgs& seq, const MlaArgs& a, void* workspace, s
              split, grid);
     *plan += buf;
     if (split > 1) {
-      e = launch_kernel(attn_combine_kernel, dim3(seq.T, kH / kCombineHeads), dim3(32 * kCombineHeads), 0, env.stream,
-                        true, 1,
-                     static_cast<const uint16_t*>(p.ws_o), static_cast<const float*>(p.ws_lse), split, seq.T,
-                     static_cast<__nv_bfloat16*>(a.out), a.lse);
+      e = launch_combine(static_cast<const uint16_t*>(p.ws_o), static_cast<const float*>(p.ws_lse), split, seq.T,
+                         static_cast<__nv_bfloat16*>(a.out), a.lse, env);
       if (e != cudaSuccess) return e;
       *plan += "+attn_combine";
       e = cudaGetLastError();

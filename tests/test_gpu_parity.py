@@ -22,6 +22,8 @@ CASES = {
     "b1_ctx65_K64": ("decode_b1", dict(ctx=[65], K=64)),
     "b1_ctx300_K2048": ("decode_b1", dict(ctx=[300], K=2048)),
     "b1_ctx5000": ("decode_b1", dict(ctx=[5000], K=2048)),
+    # 43 row slices of 96 rows: the slice merge takes more than one batch per warp
+    "b1_ctx7000_K4096": ("decode_b1", dict(ctx=[7000], K=4096)),
     "b7_shuffled": ("decode_b64", dict(ctx_range=(100, 3000), B=7, K=256)),
     "b5_shuffled_K2048": ("decode_b64", dict(ctx_range=(2048, 8192), B=5, K=2048)),
     "fp8_b2": ("decode_b4_long", dict(ctx=[3000, 4100], B=2, K=2048)),
@@ -80,6 +82,8 @@ def test_attention_on_oracle_selection(case):
     o_idx = O.topk(o_scores, wl.q_pos, wl.K)
     g_out, g_lse, plan = run.attn(o_idx)
     assert "attn_tc" in plan, plan
+    if wl.K == 4096 and wl.T == 1:
+        assert "split=43" in plan and "attn_combine" in plan, plan
     o_out, o_lse = O.sparse_mla_attn(wl, o_idx)
     P.check_attn(g_out, g_lse, o_out, o_lse, wl.mla_dtype)
 
