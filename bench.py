@@ -426,10 +426,12 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
     # inputs (indexer query + scales + head weights, MLA query, positions; for a
     # prefill also the caches its tokens fill) host -> device in one packed
     # buffer, out + lse back in another, exactly `steps` steps.  Pipelined as a
-    # serving loop runs it: two device buffer sets; step i + 1's inputs go in on a
+    # serving loop runs it: NS device buffer sets; later steps' inputs go in on a
     # copy stream while step i computes, step i's results come back on another.
     # Every step's copies are inside the timed region; a slot's buffers are reused
-    # only after the copies and the step that used them two steps earlier are done.
+    # only after the copies and the step that used them NS steps earlier are done
+    # (three sets give each slot's copies a whole step of slack: at prefill size
+    # the two directions' copies take about as long as the step's compute).
     r0 = runs[0]
     parts = [r0["idxr"].q, r0["idxr"].q_scale, r0["idxr"].w, r0["mla"].q, r0["seq"].q_pos, r0["seq"].q_seq]
     if prefill:
@@ -440,8 +442,9 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
     for t, o, n in zip(parts, offs[:-1], sizes):
         h_pack[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
     out_bytes = r0["out"].numel() * 2
+    NS = 3
     slots = []
-    for _ in range(2):
+    for _ in range(NS):
         d_pack = torch.empty(int(offs[-1]), dtype=torch.uint8, device=dev)
         views = [d_pack[o:o + n].view(t.dtype).view(t.shape) for t, o, n in zip(parts, offs[:-1], sizes)]
         kc, ks, kv = (views[6], views[7], views[8]) if prefill else (r0["idxr"].k_cache, r0["idxr"].k_scale,
@@ -464,15 +467,15 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
     s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
 
     def e2e_step(i):
-        sl = slots[i % 2]
-        if i >= 2:
-            s_in.wait_event(sl["computed"])      # the step two back has read this slot's inputs
+        sl = slots[i % NS]
+        if i >= NS:
+            s_in.wait_event(sl["computed"])      # the step NS back has read this slot's inputs
         with torch.cuda.stream(s_in):
             sl["pack"].copy_(h_pack, non_blocking=True)
             sl["loaded"].record(s_in)
         stream.wait_event(sl["loaded"])
-        if i >= 2:
-            stream.wait_event(sl["returned"])    # its results from two steps back are on the host
+        if i >= NS:
+            stream.wait_event(sl["returned"])    # its results from NS steps back are on the host
         with torch.cuda.stream(stream):
             dsa.decode_step(sl["seq"], sl["idx"], sl["mla"], wl.K, sl["out"], ws, lse=sl["lse"], stream=stream)
             sl["computed"].record(stream)
@@ -488,7 +491,10 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
     # n pipelined steps captured in one CUDA graph (the copy streams forked from
     # and joined back into the capturing stream), as the device-side steps are:
     # replays then cost no host time per step.  Replays run in stream order, so a
-    # replay's first two steps find their slots free.
+    # replay's first NS steps find their slots free.  Each replay fills and drains
+    # the pipeline (its first step's inputs and its last step's results cross alone),
+    # so up to 400 steps go into one graph: one fill and drain per timed run, as in
+    # a serving loop that runs on.
     def capture_e2e(n):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
@@ -498,11 +504,11 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
             s_out.wait_event(fork)
             for i in range(n):
                 e2e_step(i)
-            for k in range(min(n, 2)):
-                stream.wait_event(slots[(n - 1 - k) % 2]["returned"])
+            for k in range(min(n, NS)):
+                stream.wait_event(slots[(n - 1 - k) % NS]["returned"])
         return g
 
-    E = min(steps, 40)
+    E = min(steps, 400)
     g_e2e = capture_e2e(E)
     g_e2e_rem = capture_e2e(steps % E) if steps % E else None
     with torch.cuda.stream(stream):
@@ -513,7 +519,7 @@ def measure_workload(torch, np, dsa, W, name, steps, warmup, min_seconds, peaks,
     del g_e2e, g_e2e_rem
     e2e = {"value": wl.T * steps / t_e2e, "unit": "tok/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": 1e3 * t_e2e / steps,
-           "pipeline": f"two buffer sets: inputs in on a copy stream while the step before computes, results "
+           "pipeline": f"{NS} buffer sets: inputs in on a copy stream while earlier steps compute, results "
                        f"out on another; {E} steps per CUDA graph replay; every step's copies inside the timed "
                        f"region"}
     dsa.check_status(stream)
