@@ -13,7 +13,7 @@ the method states it:
    (page "Day0 Inference Adaptation ... Kimi K3.1 Pro", section 3: relevance
    scores between queries and historical positions, head-weight weighting, then
    Top-K; page "Large Language Model Inference Acceleration in Practice",
-   section 1.2 "DSA", LI sub-module).  Per the spec definition:
+   section 1.2 "DSA", LI sub-module).  Written out, the head-weighted score is
        I[t, s] = sum_h w[t, h] * ReLU(q_I[t, h] . k_I[s])
    with q_I, k_I the dequantised FP8 values (code * scale): one fp32 scale per
    key and per (query, head), or -- the pages' MXFP8 variant ("Day0 ... Kimi
