@@ -84,6 +84,51 @@ def test_host_validation_rejects_bad_arguments(dsa):
     assert lib.dsa_index_cache_append_mx(ctypes.byref(s), 48, dsa.DSA_F32, 16, 16, 16, None) == 2
 
 
+def test_host_validation_of_writers_prolog_and_debug_switch(dsa):
+    """Each rejection below returns before the library's first CUDA call."""
+    lib = dsa._lib
+    s = dsa.SeqDesc(B=1, T=1, max_ctx=1000, q_per_seq=1, q_seq=16, q_pos=16, block_table=16,
+                    bt_stride=16, page_size=64, cache_rows=4096)
+    # index-key writer: D_I in [4, 1024] and a multiple of 4, fp32 or bf16 sources, pointers non-NULL and aligned
+    assert lib.dsa_index_cache_append(ctypes.byref(s), 6, dsa.DSA_F32, 16, 16, 16, None) == 2
+    assert lib.dsa_index_cache_append(ctypes.byref(s), 64, dsa.DSA_E4M3, 16, 16, 16, None) == 2
+    assert lib.dsa_index_cache_append(ctypes.byref(s), 64, dsa.DSA_F32, None, 16, 16, None) == 1
+    assert lib.dsa_index_cache_append(ctypes.byref(s), 64, dsa.DSA_BF16, 16, 24, 16, None) == 1
+    assert "aligned" in dsa.last_error()
+    # latent writer: copied rows move 16-byte vectors; pointers non-NULL and aligned
+    m = dsa.MlaDesc(H=4, d_latent=60, d_rope=2, dtype=dsa.DSA_BF16, q=16, kv_cache=16, row_bytes=128,
+                    softmax_scale=0.1)
+    assert lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), 16, 16, None) == 2
+    m = dsa.MlaDesc(H=4, d_latent=64, d_rope=16, dtype=dsa.DSA_BF16, q=16, kv_cache=16, row_bytes=160,
+                    softmax_scale=0.1)
+    assert lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), None, 16, None) == 1
+    assert lib.dsa_latent_cache_append(ctypes.byref(s), ctypes.byref(m), 16, 8, None) == 1
+    # prolog: D_I == 128, 1 <= H_I <= 128, d_model and d_q positive multiples of 64
+    ok = dict(d_model=256, d_q=128, H_I=8, D_I=128, x=16, x_q=16, w_q=16, w_k=16, w_w=16, gamma=16, beta=16)
+    for bad in (dict(D_I=64), dict(H_I=0), dict(H_I=129), dict(d_model=100), dict(d_q=0)):
+        pd = dsa.PrologDesc(**{**ok, **bad})
+        assert lib.dsa_indexer_prolog_workspace_size(ctypes.byref(s), ctypes.byref(pd)) == 0, bad
+        assert lib.dsa_indexer_prolog(ctypes.byref(s), ctypes.byref(pd), 16, 16, 16, 16, 16, 16, 1 << 20,
+                                      None) == 2, bad
+    assert lib.dsa_indexer_prolog(ctypes.byref(s), None, 16, 16, 16, 16, 16, 16, 1 << 20, None) == 1
+    pd = dsa.PrologDesc(**{**ok, "x": None})
+    assert lib.dsa_indexer_prolog(ctypes.byref(s), ctypes.byref(pd), 16, 16, 16, 16, 16, 16, 1 << 20, None) == 1
+    pd = dsa.PrologDesc(**ok)
+    assert lib.dsa_indexer_prolog(ctypes.byref(s), ctypes.byref(pd), 8, 16, 16, 16, 16, 16, 1 << 20, None) == 1
+    # K outside [1, 16384]: no workspace size, and the static-workspace step says unsupported
+    m = dsa.MlaDesc(H=128, d_latent=512, d_rope=64, dtype=dsa.DSA_BF16, q=16, kv_cache=16, row_bytes=1152,
+                    softmax_scale=0.1)
+    x = dsa.IndexerDesc(H_I=64, D_I=128, dtype=dsa.DSA_E4M3, q=16, q_scale=16, w=16, k_cache=16, k_scale=16)
+    for K in (0, 16385):
+        assert lib.dsa_decode_workspace_size(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), K) == 0
+        assert lib.dsa_decode_step_static_ws(ctypes.byref(s), ctypes.byref(x), ctypes.byref(m), K, 16, None, None,
+                                             None) == 2
+    # failure-detection switch: the wait bound must lie in [1 us, 1 s]; switching off always succeeds
+    assert lib.dsa_debug_withhold_arrival(1, 999) == 1
+    assert lib.dsa_debug_withhold_arrival(1, 2_000_000_000) == 1
+    assert lib.dsa_debug_withhold_arrival(0, 0) == 0
+
+
 def test_product_package_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "dsa_indexed_sparse_gb300")
     for dirpath, _, files in os.walk(pkg):
