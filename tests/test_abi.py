@@ -129,6 +129,42 @@ def test_host_validation_of_writers_prolog_and_debug_switch(dsa):
     assert lib.dsa_debug_withhold_arrival(0, 0) == 0
 
 
+C_CALLER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "dsa.h"
+int main(void) {
+  if (dsa_abi_version() != 1) return 1;
+  /* a NULL descriptor is rejected on the host, before any CUDA call */
+  if (dsa_topk(NULL, NULL, 0, 1, NULL, NULL) != DSA_ERR_INVALID_ARG) return 2;
+  if (strcmp(dsa_status_string(DSA_ERR_TIMEOUT), "DSA_ERR_TIMEOUT") != 0) return 3;
+  if (strstr(dsa_last_error(), "NULL") == NULL) return 4;
+  printf("ok\n");
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_a_c_program_links(dsa, tmp_path):
+    """include/dsa.h compiles as strict C99, and a C program links against libdsa.so and calls it."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(dsa.LIB_PATH)
+    libname = os.path.basename(dsa.LIB_PATH)
+    assert libname.startswith("lib") and libname.endswith(".so")
+    cc = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I",
+                         os.path.join(ROOT, "include"), str(src), "-L", libdir, "-l" + libname[3:-3],
+                         "-Wl,-rpath," + libdir, "-o", str(exe)], capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert run.returncode == 0 and run.stdout.strip() == "ok", (run.returncode, run.stdout, run.stderr)
+
+
 def test_product_package_does_not_touch_the_oracle():
     pkg = os.path.join(ROOT, "dsa_indexed_sparse_gb300")
     for dirpath, _, files in os.walk(pkg):
